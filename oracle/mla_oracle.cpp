@@ -1,0 +1,297 @@
+// Plain fp64 CPU oracle for paged Multi-head Latent Attention (MLA) decode.
+//
+// TEST INFRASTRUCTURE ONLY. Nothing on the product path may call, link or
+// load this file: only the tests, the smoke check and the benchmark's CPU
+// baseline leg use it. It shares no code, header, table or constant with the
+// CUDA library, and includes nothing from it.
+//
+// What is computed (the plain definition; the GPU kernels reach the same
+// result up to rounding order):
+//   For every request b and query head h, with L = seq_lens[b]:
+//   1. gather   row_t = kv_cache[block_table[b][t / bs]][t % bs][0:576],
+//               t = 0..L-1 (bf16 -> double is exact);
+//   2. score    s_t = sm_scale * ( sum_{d<512} q_nope[b,h,d] * row_t[d]
+//                                + sum_{d<64}  q_pe[b,h,d]   * row_t[512+d] );
+//   3. softmax  m = max_t s_t, Z = sum_t exp(s_t - m), lse = m + ln Z;
+//   4. output   out[b,h,j] = sum_t exp(s_t - m) / Z * row_t[j], j < 512
+//               (V is the first 512 latent columns of the same row).
+// Sources: "SM100 Cutlass MLA decode with unrestricted num_heads (< 128) for
+// DeepSeek TP" (vLLM PR #20769), bot summary: split-KV partial results plus a
+// reduction kernel that combines them; "[Kernel] Flashinfer MLA (trtllm-gen)
+// decode kernel integration" (vLLM PR #21078), E2E Benchmark: paged latent
+// cache served with --block-size 32. The latent row layout (512 c_kv then
+// 64 k_pe, V = c_kv) and the natural-log LSE are the readings written down in
+// the design notes; the pages print neither formulas nor tensor shapes.
+//
+// Edge conventions: L = 0 gives out = 0 and lse = -inf. A block id outside
+// [0, num_blocks) makes the call return ORACLE_ERR_BAD_BLOCK.
+//
+// Also here, each as its own routine so tests can pin one against another:
+//   - oracle_mla_partial / oracle_mla_combine: the split-KV partial result of
+//     a token range and the log-sum-exp merge of several partials;
+//   - oracle_mla_decode_bruteforce: an independent second path (long double,
+//     dense K materialised, exp without max subtraction) for tiny inputs.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+constexpr int kDc = 512;              // latent c_kv columns (= V width)
+constexpr int kDr = 64;               // rope k_pe columns
+constexpr int kD = kDc + kDr;         // 576 columns per cached token row
+
+constexpr int ORACLE_OK = 0;
+constexpr int ORACLE_ERR_ARG = 1;
+constexpr int ORACLE_ERR_BAD_BLOCK = 2;
+
+// bf16 bit pattern -> double. bf16 is the top half of an IEEE binary32, so
+// the widening is exact.
+inline double bf16_to_double(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof(f));
+  return static_cast<double>(f);
+}
+
+struct Inputs {
+  int B, H;
+  const uint16_t* q_nope;     // [B, H, 512]
+  const uint16_t* q_pe;       // [B, H, 64]
+  const uint16_t* kv_cache;   // [num_blocks, block_size, 576]
+  int64_t num_blocks;
+  int block_size;
+  const int32_t* block_table; // [B, max_blocks]
+  int max_blocks;
+  const int32_t* seq_lens;    // [B]
+  double sm_scale;
+};
+
+// Step 1: address of cached row t of request b, or nullptr for a block id
+// that is out of range.
+const uint16_t* gather_row(const Inputs& in, int b, int64_t t) {
+  const int64_t page = t / in.block_size;
+  const int64_t slot = t % in.block_size;
+  const int32_t blk = in.block_table[static_cast<int64_t>(b) * in.max_blocks + page];
+  if (blk < 0 || blk >= in.num_blocks) return nullptr;
+  return in.kv_cache + (static_cast<int64_t>(blk) * in.block_size + slot) * kD;
+}
+
+// Step 2 for one token: the scaled score of head (b, h) against row.
+double score(const Inputs& in, int b, int h, const uint16_t* row) {
+  const uint16_t* qn = in.q_nope + (static_cast<int64_t>(b) * in.H + h) * kDc;
+  const uint16_t* qp = in.q_pe + (static_cast<int64_t>(b) * in.H + h) * kDr;
+  double acc = 0.0;
+  for (int d = 0; d < kDc; ++d) acc += bf16_to_double(qn[d]) * bf16_to_double(row[d]);
+  for (int d = 0; d < kDr; ++d) acc += bf16_to_double(qp[d]) * bf16_to_double(row[kDc + d]);
+  return in.sm_scale * acc;
+}
+
+// Steps 1-4 over the token range [t0, t1) of request b for head h. Writes the
+// normalised output (out[512]) and the range's log-sum-exp. An empty range
+// gives zeros and -inf.
+int attend_range(const Inputs& in, int b, int h, int64_t t0, int64_t t1,
+                 double* out, double* lse) {
+  for (int j = 0; j < kDc; ++j) out[j] = 0.0;
+  if (t1 <= t0) {
+    *lse = -std::numeric_limits<double>::infinity();
+    return ORACLE_OK;
+  }
+  std::vector<double> s(static_cast<size_t>(t1 - t0));
+  std::vector<const uint16_t*> rows(static_cast<size_t>(t1 - t0));
+  double m = -std::numeric_limits<double>::infinity();
+  for (int64_t t = t0; t < t1; ++t) {
+    const uint16_t* row = gather_row(in, b, t);
+    if (row == nullptr) return ORACLE_ERR_BAD_BLOCK;
+    rows[t - t0] = row;
+    s[t - t0] = score(in, b, h, row);
+    if (s[t - t0] > m) m = s[t - t0];
+  }
+  double z = 0.0;
+  for (size_t i = 0; i < s.size(); ++i) {
+    const double w = std::exp(s[i] - m);
+    z += w;
+    for (int j = 0; j < kDc; ++j) out[j] += w * bf16_to_double(rows[i][j]);
+  }
+  for (int j = 0; j < kDc; ++j) out[j] /= z;
+  *lse = m + std::log(z);
+  return ORACLE_OK;
+}
+
+bool valid_shape(const Inputs& in) {
+  if (in.B < 0 || in.H < 1 || in.block_size < 1 || in.max_blocks < 0 || in.num_blocks < 0)
+    return false;
+  for (int b = 0; b < in.B; ++b) {
+    if (in.seq_lens[b] < 0) return false;
+    if (static_cast<int64_t>(in.seq_lens[b]) >
+        static_cast<int64_t>(in.max_blocks) * in.block_size)
+      return false;
+  }
+  return true;
+}
+
+int set_threads(int n_threads) {
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+  return omp_get_max_threads();
+#else
+  (void)n_threads;
+  return 1;
+#endif
+}
+
+}  // namespace
+
+extern "C" {
+
+// Number of OpenMP threads the oracle will use after applying n_threads
+// (n_threads <= 0 keeps the runtime default).
+int oracle_num_threads(int n_threads) { return set_threads(n_threads); }
+
+// Full decode for a chosen list of (b, h) rows: out_rows[n_rows, 512],
+// lse_rows[n_rows]. Rows are independent, so this is also the whole decode
+// when the list holds every (b, h).
+int oracle_mla_decode_rows(int B, int H, const uint16_t* q_nope, const uint16_t* q_pe,
+                           const uint16_t* kv_cache, int64_t num_blocks, int block_size,
+                           const int32_t* block_table, int max_blocks,
+                           const int32_t* seq_lens, double sm_scale, int64_t n_rows,
+                           const int32_t* row_b, const int32_t* row_h, double* out_rows,
+                           double* lse_rows, int n_threads) {
+  Inputs in{B, H, q_nope, q_pe, kv_cache, num_blocks, block_size,
+            block_table, max_blocks, seq_lens, sm_scale};
+  if (!valid_shape(in)) return ORACLE_ERR_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (row_b[r] < 0 || row_b[r] >= B || row_h[r] < 0 || row_h[r] >= H) return ORACLE_ERR_ARG;
+  set_threads(n_threads);
+  int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int b = row_b[r];
+    const int rc = attend_range(in, b, row_h[r], 0, seq_lens[b], out_rows + r * kDc,
+                                lse_rows + r);
+    if (rc != ORACLE_OK) {
+#pragma omp critical
+      status = rc;
+    }
+  }
+  return status;
+}
+
+// Full decode over every (b, h): out[B, H, 512], lse[B, H].
+int oracle_mla_decode(int B, int H, const uint16_t* q_nope, const uint16_t* q_pe,
+                      const uint16_t* kv_cache, int64_t num_blocks, int block_size,
+                      const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                      double sm_scale, double* out, double* lse, int n_threads) {
+  if (B < 0 || H < 1) return ORACLE_ERR_ARG;
+  const int64_t n = static_cast<int64_t>(B) * H;
+  std::vector<int32_t> rb(static_cast<size_t>(n)), rh(static_cast<size_t>(n));
+  for (int64_t i = 0; i < n; ++i) {
+    rb[i] = static_cast<int32_t>(i / H);
+    rh[i] = static_cast<int32_t>(i % H);
+  }
+  return oracle_mla_decode_rows(B, H, q_nope, q_pe, kv_cache, num_blocks, block_size,
+                                block_table, max_blocks, seq_lens, sm_scale, n, rb.data(),
+                                rh.data(), out, lse, n_threads);
+}
+
+// Split-KV partial of one (b, h) over tokens [t0, t1): the normalised partial
+// output o[512] and that range's log-sum-exp. This is what one split of the
+// split-KV decode produces before the reduction step.
+int oracle_mla_partial(int B, int H, const uint16_t* q_nope, const uint16_t* q_pe,
+                       const uint16_t* kv_cache, int64_t num_blocks, int block_size,
+                       const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                       double sm_scale, int b, int h, int64_t t0, int64_t t1, double* o,
+                       double* lse) {
+  Inputs in{B, H, q_nope, q_pe, kv_cache, num_blocks, block_size,
+            block_table, max_blocks, seq_lens, sm_scale};
+  if (!valid_shape(in) || b < 0 || b >= B || h < 0 || h >= H) return ORACLE_ERR_ARG;
+  if (t0 < 0 || t1 > seq_lens[b] || t0 > t1) return ORACLE_ERR_ARG;
+  return attend_range(in, b, h, t0, t1, o, lse);
+}
+
+// Reduction of n split partials (o_parts[n, 512], lse_parts[n]) of one
+// (b, h): lse = ln sum_i exp(lse_i); out = sum_i exp(lse_i - lse) * o_i.
+// Partials with lse_i = -inf carry no tokens and get weight 0; if all are
+// -inf the result is out = 0, lse = -inf.
+int oracle_mla_combine(int n, const double* o_parts, const double* lse_parts, double* o,
+                       double* lse) {
+  if (n < 0) return ORACLE_ERR_ARG;
+  for (int j = 0; j < kDc; ++j) o[j] = 0.0;
+  double mx = -std::numeric_limits<double>::infinity();
+  for (int i = 0; i < n; ++i)
+    if (lse_parts[i] > mx) mx = lse_parts[i];
+  if (n == 0 || mx == -std::numeric_limits<double>::infinity()) {
+    *lse = -std::numeric_limits<double>::infinity();
+    return ORACLE_OK;
+  }
+  double z = 0.0;
+  for (int i = 0; i < n; ++i) z += std::exp(lse_parts[i] - mx);
+  const double total = mx + std::log(z);
+  for (int i = 0; i < n; ++i) {
+    if (lse_parts[i] == -std::numeric_limits<double>::infinity()) continue;
+    const double w = std::exp(lse_parts[i] - total);
+    for (int j = 0; j < kDc; ++j) o[j] += w * o_parts[static_cast<int64_t>(i) * kDc + j];
+  }
+  *lse = total;
+  return ORACLE_OK;
+}
+
+// Independent second path for tiny inputs: long double throughout, the K rows
+// of each request copied into a dense [L, 576] matrix first, every score
+// formed as one dot product of the concatenated query [q_nope | q_pe] with a
+// dense row, and exp taken without subtracting the maximum (valid only while
+// exp(s) cannot overflow, i.e. for small, N(0,1)-sized inputs).
+int oracle_mla_decode_bruteforce(int B, int H, const uint16_t* q_nope, const uint16_t* q_pe,
+                                 const uint16_t* kv_cache, int64_t num_blocks, int block_size,
+                                 const int32_t* block_table, int max_blocks,
+                                 const int32_t* seq_lens, double sm_scale, double* out,
+                                 double* lse) {
+  if (B < 0 || H < 1 || block_size < 1) return ORACLE_ERR_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int64_t L = seq_lens[b];
+    if (L < 0 || L > static_cast<int64_t>(max_blocks) * block_size) return ORACLE_ERR_ARG;
+    std::vector<long double> K(static_cast<size_t>(L) * kD);
+    for (int64_t t = 0; t < L; ++t) {
+      const int32_t blk = block_table[static_cast<int64_t>(b) * max_blocks + t / block_size];
+      if (blk < 0 || blk >= num_blocks) return ORACLE_ERR_BAD_BLOCK;
+      const uint16_t* src =
+          kv_cache + (static_cast<int64_t>(blk) * block_size + t % block_size) * kD;
+      for (int d = 0; d < kD; ++d) K[static_cast<size_t>(t) * kD + d] = bf16_to_double(src[d]);
+    }
+    for (int h = 0; h < H; ++h) {
+      long double q[kD];
+      for (int d = 0; d < kDc; ++d)
+        q[d] = bf16_to_double(q_nope[(static_cast<int64_t>(b) * H + h) * kDc + d]);
+      for (int d = 0; d < kDr; ++d)
+        q[kDc + d] = bf16_to_double(q_pe[(static_cast<int64_t>(b) * H + h) * kDr + d]);
+      double* o = out + (static_cast<int64_t>(b) * H + h) * kDc;
+      if (L == 0) {
+        for (int j = 0; j < kDc; ++j) o[j] = 0.0;
+        lse[static_cast<int64_t>(b) * H + h] = -std::numeric_limits<double>::infinity();
+        continue;
+      }
+      std::vector<long double> e(static_cast<size_t>(L));
+      long double z = 0.0L;
+      for (int64_t t = 0; t < L; ++t) {
+        long double dot = 0.0L;
+        for (int d = 0; d < kD; ++d) dot += q[d] * K[static_cast<size_t>(t) * kD + d];
+        e[t] = std::exp(static_cast<long double>(sm_scale) * dot);
+        z += e[t];
+      }
+      for (int j = 0; j < kDc; ++j) {
+        long double acc = 0.0L;
+        for (int64_t t = 0; t < L; ++t) acc += e[t] * K[static_cast<size_t>(t) * kD + j];
+        o[j] = static_cast<double>(acc / z);
+      }
+      lse[static_cast<int64_t>(b) * H + h] = static_cast<double>(std::log(z));
+    }
+  }
+  return ORACLE_OK;
+}
+
+}  // extern "C"
