@@ -1,0 +1,172 @@
+/*
+ * mla_decode.h — C ABI of the GB300 (sm_103a) paged MLA decode library.
+ *
+ * Operation. Multi-head Latent Attention decode over a paged latent KV cache:
+ * for every request b < B and query head h < H, with L = seq_lens[b],
+ *
+ *   row_t   = kv_cache[block_table[b][t / block_size]][t % block_size][0:576]
+ *   s_t     = sm_scale * ( q_nope[b,h,:] . row_t[0:512] + q_pe[b,h,:] . row_t[512:576] )
+ *   lse     = ln sum_t exp(s_t)                      (natural log, sm_scale included)
+ *   out     = sum_t exp(s_t - lse) * row_t[0:512]    (V is the first 512 latent columns)
+ *
+ * Sources: "SM100 Cutlass MLA decode with unrestricted num_heads (< 128) for
+ * DeepSeek TP" (vLLM PR #20769), opening post (fewer than 128 query heads) and
+ * bot summary (heads padded to 128 inside the kernel; KV split across blocks
+ * and SMs with a reduction kernel that combines the partial results; a tile
+ * scheduler; TMA and warp specialisation), plus the review thread (workspace
+ * sized by an op, allocated per instance by the caller, uninitialised memory
+ * is fine, sized for the decode batch only); "[Kernel] Flashinfer MLA
+ * (trtllm-gen) decode kernel integration" (vLLM PR #21078), E2E Benchmark
+ * (paged cache with --block-size 32) and Kernel-only microbenchmark
+ * (bs = 512 and bs = 1 decode latency).
+ *
+ * Conventions shared by every call below:
+ *  - All tensors are dense, row-major, owned by the caller. Device pointers
+ *    point to memory of the device that was current when the plan was made.
+ *  - bf16 tensors are passed as void* (IEEE bfloat16 bit patterns).
+ *  - A stream argument is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).
+ *  - Nothing here allocates device memory except mla_decode_plan (its small
+ *    work list). The workspace is caller-owned and needs no initialisation.
+ *  - The library loads on any machine; calls that need an sm_103 GPU return
+ *    MLA_ERR_UNSUPPORTED_DEVICE elsewhere (a missing-symbol import failure on
+ *    older GPUs is what the PR #20769 thread reports; this ABI avoids it).
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,         /* bad shape, pointer, alignment or value */
+  MLA_ERR_UNSUPPORTED_DEVICE = 2,  /* no sm_103 device current */
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < mla_plan_workspace_bytes */
+  MLA_ERR_CUDA = 4,                /* a CUDA runtime call failed (launch, alloc, copy) */
+  MLA_ERR_DEVICE_FAULT = 5         /* the kernels flagged bad input (see mla_check_device_error) */
+} mla_status_t;
+
+/* Device-side error bits reported through mla_check_device_error. */
+#define MLA_DEVERR_BAD_BLOCK 1u      /* a block_table entry outside [0, num_blocks) */
+#define MLA_DEVERR_SEQLEN_MISMATCH 2u /* device seq_lens[b] differs from the plan's */
+#define MLA_DEVERR_TIMEOUT 4u        /* an internal wait gave up (kernel returned early) */
+
+typedef struct mla_plan_s* mla_plan_t; /* opaque; owned by the library */
+
+/* Planner options; zero-initialise and set what you need. */
+typedef struct {
+  int num_clusters;   /* 0: query the device for co-resident CTA pairs; > 0: use this many */
+  int force_splits;   /* 0: automatic; > 0: split every request into this many KV chunks
+                         (testing aid; chunks are whole 96-token tiles, empty ones dropped) */
+  int host_only;      /* nonzero: build the schedule on the host only (no device upload,
+                         no device query unless num_clusters == 0); such a plan can be
+                         inspected but not passed to mla_decode */
+} mla_plan_options_t;
+
+/*
+ * mla_decode_plan — the split-KV scheduler ("tile scheduler" of PR #20769's
+ * bot summary; per-decode-batch sizing of its review thread).
+ *
+ * Reads seq_lens_host[B] (host memory, int32, each 0 <= L <= max_blocks *
+ * block_size), chooses how many KV chunks each request is split into and
+ * which CTA pair processes each chunk (longest first), and sizes the
+ * workspace. Launches no kernel. Copies the schedule (a few KB) to device
+ * memory owned by the plan, on the current device.
+ * Arguments: B >= 1 requests; 1 <= H <= 128 query heads (padded to 128 inside
+ * the kernel, never in memory); block_size in {16, 32, 64, 128};
+ * max_blocks >= 1 is the row length of block_table.
+ * On success *plan_out receives a new plan (free it with mla_plan_destroy).
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED_DEVICE, MLA_ERR_CUDA.
+ */
+mla_status_t mla_decode_plan(int B, int H, const int32_t* seq_lens_host, int block_size,
+                             int max_blocks, mla_plan_t* plan_out);
+
+/* Same as mla_decode_plan with explicit options (opts may be NULL). */
+mla_status_t mla_decode_plan_ex(int B, int H, const int32_t* seq_lens_host, int block_size,
+                                int max_blocks, const mla_plan_options_t* opts,
+                                mla_plan_t* plan_out);
+
+/*
+ * Rebuild an existing plan for new lengths with the same B, H, block_size and
+ * max_blocks, reusing its device allocation when large enough. The upload is
+ * an asynchronous copy on `stream` from host memory held by the plan, so a
+ * decode enqueued later on the same stream sees the new schedule. Do not
+ * update a plan while a decode that uses it may still be running on another
+ * stream. Errors as mla_decode_plan.
+ */
+mla_status_t mla_plan_update(mla_plan_t plan, const int32_t* seq_lens_host, void* stream);
+
+/* Workspace bytes mla_decode needs for this plan (0 if no request is split). */
+size_t mla_plan_workspace_bytes(mla_plan_t plan);
+
+/* Introspection (tests, logging). Return -1 on a bad argument. */
+int mla_plan_num_splits(mla_plan_t plan, int b);  /* KV chunks of request b */
+int mla_plan_num_work_items(mla_plan_t plan);     /* chunks over all requests */
+int mla_plan_num_clusters(mla_plan_t plan);       /* CTA pairs launched */
+/* Work item i: request, first token, end token, partial slot (-1: writes
+ * out/lse directly) and the CTA pair that runs it. */
+int mla_plan_work_item(mla_plan_t plan, int i, int32_t* b, int32_t* t0, int32_t* t1,
+                       int32_t* slot, int32_t* cluster);
+
+/*
+ * mla_decode — one decode step over the paged latent cache.
+ *
+ *  q_nope       device bf16 [B, H, 512]   16-byte aligned
+ *  q_pe         device bf16 [B, H, 64]    16-byte aligned
+ *  kv_cache     device bf16 [num_blocks, block_size, 576]; each row is 512
+ *               c_kv columns then 64 k_pe columns; 16-byte aligned
+ *  num_blocks   rows of the block pool (>= 1)
+ *  block_table  device int32 [B, max_blocks]; entry p of request b names the
+ *               physical block of its tokens [p*block_size, (p+1)*block_size).
+ *               Entries past a request's last page are never read.
+ *  seq_lens     device int32 [B]; must equal the host copy the plan was built
+ *               from (a mismatch raises MLA_DEVERR_SEQLEN_MISMATCH)
+ *  sm_scale     softmax scale applied to q.k (e.g. 1/sqrt(192))
+ *  out          device bf16 [B, H, 512], 16-byte aligned (written)
+ *  lse          device fp32 [B, H] (written): natural-log log-sum-exp of the
+ *               scaled scores; -inf and out = 0 for a request with L = 0
+ *  workspace    device memory of at least mla_plan_workspace_bytes(plan)
+ *               bytes, 256-byte aligned, contents ignored (may be NULL if 0)
+ *  stream       cudaStream_t as void*
+ *
+ * Asynchronous: returns after enqueueing the decode kernel (and, when some
+ * request is split, the combine kernel) on `stream`. Enqueues nothing else, so
+ * it can be captured in a CUDA graph. Block ids outside [0, num_blocks) are
+ * detected on the device: the affected rows are read as zeros and an error
+ * bit is raised (no trap); see mla_check_device_error.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED_DEVICE,
+ * MLA_ERR_WORKSPACE_TOO_SMALL, MLA_ERR_CUDA.
+ */
+mla_status_t mla_decode(mla_plan_t plan, const void* q_nope, const void* q_pe,
+                        const void* kv_cache, int64_t num_blocks, const int32_t* block_table,
+                        const int32_t* seq_lens, float sm_scale, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_check_device_error — synchronise `stream`, read and clear the plan's
+ * device error word (sticky across decodes since the last check). Writes the
+ * MLA_DEVERR_* bits to *bits_out (may be NULL) and returns
+ * MLA_ERR_DEVICE_FAULT if any bit was set, MLA_OK otherwise, MLA_ERR_CUDA if
+ * a CUDA call failed.
+ */
+mla_status_t mla_check_device_error(mla_plan_t plan, void* stream, uint32_t* bits_out);
+
+/* Free a plan and its device memory (synchronises its device). NULL is ok. */
+void mla_plan_destroy(mla_plan_t plan);
+
+/* Static description of a status code. */
+const char* mla_status_string(mla_status_t status);
+
+/* 1 if the current device can run mla_decode, 0 otherwise. */
+int mla_device_supported(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

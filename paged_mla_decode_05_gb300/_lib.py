@@ -1,0 +1,238 @@
+"""ctypes binding of ``include/mla_decode.h``: same names, argument marshalling only.
+
+Every step of the decode runs in the sm_103a kernels of the shared library;
+this module converts torch tensors to pointers, checks dtypes, shapes and
+devices, and turns status codes into exceptions. There is no fallback: if the
+library is missing the import of this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import List, Optional, Tuple
+
+import numpy as np
+
+from . import build as _build
+
+D_C = 512
+D_R = 64
+D = D_C + D_R
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "mla_decode.h")
+
+MLA_OK = 0
+STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED_DEVICE",
+                3: "MLA_ERR_WORKSPACE_TOO_SMALL", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_FAULT"}
+MLA_DEVERR_BAD_BLOCK = 1
+MLA_DEVERR_SEQLEN_MISMATCH = 2
+MLA_DEVERR_TIMEOUT = 4
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+class PlanOptions(ctypes.Structure):
+    _fields_ = [("num_clusters", ctypes.c_int), ("force_splits", ctypes.c_int),
+                ("host_only", ctypes.c_int)]
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"paged MLA decode library not built ({path}); run "
+                          "`python -m paged_mla_decode_05_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    p, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32
+    sz = ctypes.c_size_t
+    sigs = {
+        "mla_decode_plan": (i32, [i32, i32, p, i32, i32, p]),
+        "mla_decode_plan_ex": (i32, [i32, i32, p, i32, i32, ctypes.POINTER(PlanOptions), p]),
+        "mla_plan_update": (i32, [p, p, p]),
+        "mla_plan_workspace_bytes": (sz, [p]),
+        "mla_plan_num_splits": (i32, [p, i32]),
+        "mla_plan_num_work_items": (i32, [p]),
+        "mla_plan_num_clusters": (i32, [p]),
+        "mla_plan_work_item": (i32, [p, i32, p, p, p, p, p]),
+        "mla_decode": (i32, [p, p, p, p, i64, p, p, ctypes.c_float, p, p, p, sz, p]),
+        "mla_check_device_error": (i32, [p, p, ctypes.POINTER(u32)]),
+        "mla_plan_destroy": (None, [p]),
+        "mla_status_string": (ctypes.c_char_p, [i32]),
+        "mla_device_supported": (i32, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+def header_functions() -> List[str]:
+    """Names of the functions declared in include/mla_decode.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", text)))
+
+
+def _check(status: int, what: str):
+    if status != MLA_OK:
+        raise MLAError(status, what)
+
+
+def mla_device_supported() -> bool:
+    return bool(LIB.mla_device_supported())
+
+
+class Plan:
+    """Owns an ``mla_plan_t``; freed on ``destroy()`` or garbage collection."""
+
+    def __init__(self, handle: int, B: int, H: int, block_size: int, max_blocks: int,
+                 host_only: bool):
+        self._h = ctypes.c_void_p(handle)
+        self.B, self.H, self.block_size, self.max_blocks = B, H, block_size, max_blocks
+        self.host_only = host_only
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if not self._h:
+            raise ValueError("plan destroyed")
+        return self._h
+
+    def destroy(self):
+        if self._h:
+            LIB.mla_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(LIB.mla_plan_workspace_bytes(self.handle))
+
+    def num_splits(self, b: int) -> int:
+        return int(LIB.mla_plan_num_splits(self.handle, b))
+
+    @property
+    def num_work_items(self) -> int:
+        return int(LIB.mla_plan_num_work_items(self.handle))
+
+    @property
+    def num_clusters(self) -> int:
+        return int(LIB.mla_plan_num_clusters(self.handle))
+
+    def work_items(self) -> List[Tuple[int, int, int, int, int]]:
+        out = []
+        vals = [ctypes.c_int32() for _ in range(5)]
+        for i in range(self.num_work_items):
+            rc = LIB.mla_plan_work_item(self.handle, i, *(ctypes.byref(v) for v in vals))
+            if rc != 0:
+                raise MLAError(MLA_OK + 1, "mla_plan_work_item")
+            out.append(tuple(v.value for v in vals))
+        return out
+
+    def update(self, seq_lens_host, stream=None):
+        lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+        if lens.shape != (self.B,):
+            raise ValueError(f"seq_lens must have shape ({self.B},)")
+        _check(LIB.mla_plan_update(self.handle, lens.ctypes.data_as(ctypes.c_void_p),
+                                   _stream_ptr(stream)), "mla_plan_update")
+
+
+def mla_decode_plan(B: int, H: int, seq_lens_host, block_size: int, max_blocks: int,
+                    num_clusters: int = 0, force_splits: int = 0, host_only: bool = False) -> Plan:
+    """Build the split-KV schedule (host-only; uploads a small work list)."""
+    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError(f"seq_lens must have shape ({B},)")
+    opts = PlanOptions(int(num_clusters), int(force_splits), 1 if host_only else 0)
+    h = ctypes.c_void_p()
+    _check(LIB.mla_decode_plan_ex(B, H, lens.ctypes.data_as(ctypes.c_void_p), block_size,
+                                  max_blocks, ctypes.byref(opts), ctypes.byref(h)),
+           "mla_decode_plan")
+    return Plan(h.value, B, H, block_size, max_blocks, host_only)
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        import torch
+        if not torch.cuda.is_available():
+            return ctypes.c_void_p(0)
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _tensor(t, dtype, shape, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def mla_decode(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale: float, out,
+               lse, workspace=None, stream=None):
+    """Enqueue one decode (see mla_decode in include/mla_decode.h).
+
+    Tensors: q_nope bf16 [B,H,512], q_pe bf16 [B,H,64], kv_cache bf16
+    [num_blocks, block_size, 576], block_table int32 [B, max_blocks], seq_lens
+    int32 [B] (all CUDA); out bf16 [B,H,512] and lse fp32 [B,H] are written;
+    workspace is a CUDA uint8 tensor of at least plan.workspace_bytes bytes.
+    """
+    import torch
+    B, H = plan.B, plan.H
+    if kv_cache.dim() != 3 or kv_cache.shape[1] != plan.block_size or kv_cache.shape[2] != D:
+        raise ValueError(f"kv_cache must have shape [num_blocks, {plan.block_size}, {D}]")
+    nb = int(kv_cache.shape[0])
+    args = [
+        _tensor(q_nope, torch.bfloat16, (B, H, D_C), "q_nope"),
+        _tensor(q_pe, torch.bfloat16, (B, H, D_R), "q_pe"),
+        _tensor(kv_cache, torch.bfloat16, (nb, plan.block_size, D), "kv_cache"),
+    ]
+    bt = _tensor(block_table, torch.int32, (B, plan.max_blocks), "block_table")
+    sl = _tensor(seq_lens, torch.int32, (B,), "seq_lens")
+    o = _tensor(out, torch.bfloat16, (B, H, D_C), "out")
+    l = _tensor(lse, torch.float32, (B, H), "lse")
+    if workspace is None:
+        ws, ws_bytes = ctypes.c_void_p(0), 0
+    else:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws = ctypes.c_void_p(workspace.data_ptr())
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(LIB.mla_decode(plan.handle, args[0], args[1], args[2], nb, bt, sl,
+                          ctypes.c_float(sm_scale), o, l, ws, ws_bytes, _stream_ptr(stream)),
+           "mla_decode")
+
+
+def mla_check_device_error(plan: Plan, stream=None) -> int:
+    """Synchronise, read and clear the plan's device error bits (0 = none)."""
+    bits = ctypes.c_uint32(0)
+    st = LIB.mla_check_device_error(plan.handle, _stream_ptr(stream), ctypes.byref(bits))
+    if st not in (MLA_OK, 5):
+        raise MLAError(st, "mla_check_device_error")
+    return int(bits.value)
+
+
+def mla_status_string(status: int) -> str:
+    return LIB.mla_status_string(int(status)).decode()

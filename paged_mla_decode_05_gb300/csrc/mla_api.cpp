@@ -1,0 +1,571 @@
+// C ABI of the paged MLA decode library: the split-KV planner, argument
+// checks, the TMA descriptor of the paged cache, and the kernel launches.
+//
+// The planner is the "tile scheduler" and split-KV choice of "SM100 Cutlass
+// MLA decode with unrestricted num_heads (< 128) for DeepSeek TP" (vLLM PR
+// #20769, bot summary), sized per decode batch as its review thread asks; the
+// workspace it sizes belongs to the caller, who may pass uninitialised memory
+// (the same review asks for torch.empty rather than torch.zeros).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <queue>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/mla_decode.h"
+#include "mla_internal.h"
+
+using mla::CombineItem;
+using mla::WorkItem;
+
+struct mla_plan_s {
+  int B = 0, H = 0, block_size = 0, max_blocks = 0;
+  int device = -1;
+  bool host_only = false;
+  int num_clusters = 0;
+  int force_splits = 0;
+  std::vector<int32_t> seq_lens;
+  std::vector<int32_t> splits;           // per request
+  std::vector<WorkItem> items;           // grouped by CTA pair
+  std::vector<int32_t> item_cluster;     // parallel to items
+  std::vector<int32_t> cluster_offsets;  // num_clusters + 1
+  std::vector<CombineItem> combine;
+  int num_slots = 0;
+  size_t workspace_bytes = 0;
+  // Device copy of the schedule: [error word | items | offsets | combine].
+  uint8_t* d_buf = nullptr;
+  size_t d_cap = 0;
+  uint8_t* h_stage = nullptr;  // pinned staging for asynchronous uploads
+  size_t h_cap = 0;
+  cudaEvent_t upload_done = nullptr;
+  size_t off_items = 0, off_offsets = 0, off_combine = 0, sched_bytes = 0;
+  // Cached TMA descriptor of the last cache seen.
+  CUtensorMap tmap;
+  const void* tmap_ptr = nullptr;
+  int64_t tmap_blocks = -1;
+};
+
+namespace {
+
+constexpr size_t kErrBytes = 256;
+constexpr int kMaxForcedSplits = 4096;
+
+mla_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool device_is_sm103(int dev) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return false;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return false;
+  return major == 10 && minor == 3;
+}
+
+// One-time per-device setup (kernel attributes) and the co-resident pair count.
+struct DeviceInfo {
+  bool prepared = false;
+  int clusters = 0;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+mla_status_t prepare_device(int dev, int* clusters) {
+  if (dev < 0 || dev >= 64) return MLA_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.prepared) {
+    if (!device_is_sm103(dev)) return MLA_ERR_UNSUPPORTED_DEVICE;
+    if (mla::decode_prepare_device() != cudaSuccess) return MLA_ERR_CUDA;
+    int n = 0;
+    if (mla::decode_max_clusters(&n) != cudaSuccess || n <= 0) return MLA_ERR_CUDA;
+    d.clusters = n;
+    d.prepared = true;
+  }
+  if (clusters) *clusters = d.clusters;
+  return MLA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// ------------------------------------------------------------ the scheduler
+
+struct Piece {
+  int b;
+  int tile_begin, tile_end;
+};
+
+// Split request b's tiles into n near-equal contiguous pieces.
+void split_request(int b, int tiles, int n, std::vector<Piece>& out) {
+  if (tiles == 0) {
+    out.push_back({b, 0, 0});
+    return;
+  }
+  n = std::max(1, std::min(n, tiles));
+  const int q = tiles / n, r = tiles % n;
+  int t = 0;
+  for (int i = 0; i < n; ++i) {
+    const int len = q + (i < r ? 1 : 0);
+    out.push_back({b, t, t + len});
+    t += len;
+  }
+}
+
+// Longest-processing-time-first assignment; returns the makespan in cost
+// units and fills owner[i] with the CTA pair of piece i (in assignment order).
+double lpt(const std::vector<double>& cost, int nc, std::vector<int>* order,
+           std::vector<int>* owner) {
+  std::vector<int> idx(cost.size());
+  for (size_t i = 0; i < idx.size(); ++i) idx[i] = static_cast<int>(i);
+  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+  using Slot = std::pair<double, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < nc; ++c) heap.push({0.0, c});
+  double makespan = 0.0;
+  if (owner) owner->assign(cost.size(), 0);
+  for (int i : idx) {
+    Slot s = heap.top();
+    heap.pop();
+    s.first += cost[i];
+    makespan = std::max(makespan, s.first);
+    if (owner) (*owner)[i] = s.second;
+    heap.push(s);
+  }
+  if (order) *order = idx;
+  return makespan;
+}
+
+// Cost model in units of one 96-token tile of the steady-state pipeline:
+//  - every item costs its tiles plus a fixed start/finish overhead (Q load
+//    into tensor memory, pipeline fill, epilogue);
+//  - every split item also writes an fp32 partial of H x 512 that the
+//    combine kernel reads back, spread over all pairs; the combine launch
+//    adds a fixed cost when any request is split.
+constexpr double kItemOverheadTiles = 2.5;
+constexpr double kCombineLaunchTiles = 3.0;
+
+double split_cost_tiles(int H) {
+  const double bytes = 2.0 * (static_cast<double>(H) * mla::kDc * 4 + H * 4);
+  return bytes / (static_cast<double>(mla::kTile) * mla::kD * 2);
+}
+
+void build_schedule(mla_plan_s* p) {
+  const int B = p->B;
+  std::vector<int> tiles(B);
+  int max_tiles = 0;
+  for (int b = 0; b < B; ++b) {
+    tiles[b] = (p->seq_lens[b] + mla::kTile - 1) / mla::kTile;
+    max_tiles = std::max(max_tiles, tiles[b]);
+  }
+  const int nc = p->num_clusters;
+  const double pen = split_cost_tiles(p->H);
+
+  auto make_pieces = [&](int chunk, std::vector<Piece>& pieces) {
+    pieces.clear();
+    for (int b = 0; b < B; ++b) {
+      int n;
+      if (p->force_splits > 0) n = std::min(p->force_splits, std::max(tiles[b], 1));
+      else n = tiles[b] == 0 ? 1 : (tiles[b] + chunk - 1) / chunk;
+      split_request(b, tiles[b], n, pieces);
+    }
+  };
+  auto evaluate = [&](const std::vector<Piece>& pieces, std::vector<int>* order,
+                      std::vector<int>* owner) {
+    std::vector<double> cost(pieces.size());
+    std::vector<int> count(B, 0);
+    for (const Piece& pc : pieces) count[pc.b]++;
+    int split_items = 0;
+    for (size_t i = 0; i < pieces.size(); ++i) {
+      cost[i] = (pieces[i].tile_end - pieces[i].tile_begin) + kItemOverheadTiles;
+      if (count[pieces[i].b] > 1) ++split_items;
+    }
+    double m = lpt(cost, nc, order, owner);
+    if (split_items > 0) m += kCombineLaunchTiles + split_items * pen / nc;
+    return m;
+  };
+
+  std::vector<Piece> best, cand;
+  if (p->force_splits > 0 || max_tiles <= 1) {
+    make_pieces(std::max(max_tiles, 1), best);
+  } else {
+    double best_cost = 0.0;
+    int last_chunk = -1;
+    for (int k = 1; k <= 256; ++k) {
+      const int chunk = std::max(1, (max_tiles + k - 1) / k);
+      if (chunk == last_chunk) continue;
+      last_chunk = chunk;
+      make_pieces(chunk, cand);
+      if (cand.size() > static_cast<size_t>(std::max(64 * nc, B))) break;
+      const double c = evaluate(cand, nullptr, nullptr);
+      if (best.empty() || c < best_cost - 1e-9) {
+        best_cost = c;
+        best = cand;
+      }
+      if (chunk == 1) break;
+    }
+  }
+  std::vector<int> order, owner;
+  evaluate(best, &order, &owner);
+
+  // Slots for split pieces, combine list, per-request split counts.
+  std::vector<int> count(B, 0);
+  for (const Piece& pc : best) count[pc.b]++;
+  p->splits.assign(B, 0);
+  std::vector<int> first_slot(B, -1);
+  int slots = 0;
+  p->combine.clear();
+  for (int b = 0; b < B; ++b) {
+    p->splits[b] = count[b];
+    if (count[b] > 1) {
+      first_slot[b] = slots;
+      p->combine.push_back({b, slots, count[b], 0});
+      slots += count[b];
+    }
+  }
+  std::vector<int> next_slot = first_slot;
+  std::vector<WorkItem> piece_item(best.size());
+  for (size_t i = 0; i < best.size(); ++i) {
+    const Piece& pc = best[i];
+    WorkItem w{};
+    w.b = pc.b;
+    w.t0 = pc.tile_begin * mla::kTile;
+    w.t1 = std::min(pc.tile_end * mla::kTile, p->seq_lens[pc.b]);
+    w.slot = count[pc.b] > 1 ? next_slot[pc.b]++ : -1;
+    w.seq_len = p->seq_lens[pc.b];
+    piece_item[i] = w;
+  }
+  // Group by pair, each pair's list in assignment order (longest first).
+  std::vector<std::vector<int>> per(nc);
+  for (int i : order) per[owner[i]].push_back(i);
+  p->items.clear();
+  p->item_cluster.clear();
+  p->cluster_offsets.assign(nc + 1, 0);
+  for (int c = 0; c < nc; ++c) {
+    p->cluster_offsets[c] = static_cast<int32_t>(p->items.size());
+    for (int i : per[c]) {
+      p->items.push_back(piece_item[i]);
+      p->item_cluster.push_back(c);
+    }
+  }
+  p->cluster_offsets[nc] = static_cast<int32_t>(p->items.size());
+  p->num_slots = slots;
+  const size_t o_bytes = static_cast<size_t>(slots) * p->H * mla::kDc * 4;
+  const size_t l_bytes = static_cast<size_t>(slots) * p->H * 4;
+  p->workspace_bytes = slots ? align_up(align_up(o_bytes, 256) + l_bytes, 256) : 0;
+
+  p->off_items = kErrBytes;
+  p->off_offsets = align_up(p->off_items + p->items.size() * sizeof(WorkItem), 16);
+  p->off_combine = align_up(p->off_offsets + p->cluster_offsets.size() * 4, 16);
+  p->sched_bytes = align_up(p->off_combine + p->combine.size() * sizeof(CombineItem), 256);
+}
+
+mla_status_t check_plan_args(int B, int H, const int32_t* seq_lens, int block_size,
+                             int max_blocks) {
+  if (B < 1 || H < 1 || H > mla::kMaxHeads || !seq_lens || max_blocks < 1) return MLA_ERR_INVALID_ARG;
+  if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
+    return MLA_ERR_INVALID_ARG;
+  const int64_t cap = static_cast<int64_t>(max_blocks) * block_size;
+  if (cap >= (int64_t{1} << 30)) return MLA_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens[b] < 0 || seq_lens[b] > cap) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+// Copy the schedule to the device. Synchronous when stream_or_null is
+// nullptr-and-sync, else asynchronous on the stream from pinned staging.
+mla_status_t upload(mla_plan_s* p, cudaStream_t stream, bool sync) {
+  if (p->host_only) return MLA_OK;
+  if (p->sched_bytes > p->d_cap) {
+    // Growing: the old buffer may still be read by queued decodes.
+    if (p->d_buf) {
+      if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+      uint32_t bits = 0;
+      cudaMemcpy(&bits, p->d_buf, 4, cudaMemcpyDeviceToHost);
+      cudaFree(p->d_buf);
+      p->d_buf = nullptr;
+      const size_t cap = align_up(p->sched_bytes * 2, 4096);
+      if (cudaMalloc(&p->d_buf, cap) != cudaSuccess) return MLA_ERR_CUDA;
+      p->d_cap = cap;
+      if (cudaMemcpy(p->d_buf, &bits, 4, cudaMemcpyHostToDevice) != cudaSuccess) return MLA_ERR_CUDA;
+    } else {
+      const size_t cap = align_up(p->sched_bytes * 2, 4096);
+      if (cudaMalloc(&p->d_buf, cap) != cudaSuccess) return MLA_ERR_CUDA;
+      p->d_cap = cap;
+      if (cudaMemset(p->d_buf, 0, kErrBytes) != cudaSuccess) return MLA_ERR_CUDA;
+    }
+  }
+  if (p->sched_bytes > p->h_cap) {
+    if (p->h_stage) {
+      if (p->upload_done) cudaEventSynchronize(p->upload_done);
+      cudaFreeHost(p->h_stage);
+      p->h_stage = nullptr;
+    }
+    const size_t cap = align_up(p->sched_bytes * 2, 4096);
+    if (cudaMallocHost(&p->h_stage, cap) != cudaSuccess) return MLA_ERR_CUDA;
+    p->h_cap = cap;
+  }
+  if (!p->upload_done &&
+      cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  // The staging buffer may still feed the previous asynchronous copy.
+  if (cudaEventSynchronize(p->upload_done) != cudaSuccess) return MLA_ERR_CUDA;
+  uint8_t* h = p->h_stage;
+  std::memcpy(h + p->off_items, p->items.data(), p->items.size() * sizeof(WorkItem));
+  std::memcpy(h + p->off_offsets, p->cluster_offsets.data(), p->cluster_offsets.size() * 4);
+  std::memcpy(h + p->off_combine, p->combine.data(), p->combine.size() * sizeof(CombineItem));
+  const size_t n = p->sched_bytes - kErrBytes;
+  if (sync) {
+    if (cudaMemcpy(p->d_buf + kErrBytes, h + kErrBytes, n, cudaMemcpyHostToDevice) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  } else {
+    if (cudaMemcpyAsync(p->d_buf + kErrBytes, h + kErrBytes, n, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  if (cudaEventRecord(p->upload_done, sync ? nullptr : stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+void free_plan(mla_plan_s* p) {
+  if (!p) return;
+  if (p->d_buf) {
+    cudaDeviceSynchronize();
+    cudaFree(p->d_buf);
+  }
+  if (p->upload_done) {
+    cudaEventSynchronize(p->upload_done);
+    cudaEventDestroy(p->upload_done);
+  }
+  if (p->h_stage) cudaFreeHost(p->h_stage);
+  delete p;
+}
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode_plan_ex(int B, int H, const int32_t* seq_lens_host, int block_size,
+                                int max_blocks, const mla_plan_options_t* opts,
+                                mla_plan_t* plan_out) {
+  if (!plan_out) return MLA_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  mla_status_t st = check_plan_args(B, H, seq_lens_host, block_size, max_blocks);
+  if (st != MLA_OK) return st;
+  mla_plan_options_t o{};
+  if (opts) o = *opts;
+  if (o.num_clusters < 0 || o.force_splits < 0 || o.force_splits > kMaxForcedSplits)
+    return MLA_ERR_INVALID_ARG;
+  mla_plan_s* p = new (std::nothrow) mla_plan_s();
+  if (!p) return MLA_ERR_INVALID_ARG;
+  p->B = B;
+  p->H = H;
+  p->block_size = block_size;
+  p->max_blocks = max_blocks;
+  p->host_only = o.host_only != 0;
+  p->force_splits = o.force_splits;
+  p->seq_lens.assign(seq_lens_host, seq_lens_host + B);
+  if (!p->host_only || o.num_clusters == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      free_plan(p);
+      return MLA_ERR_UNSUPPORTED_DEVICE;
+    }
+    int clusters = 0;
+    st = prepare_device(dev, &clusters);
+    if (st != MLA_OK) {
+      free_plan(p);
+      return st;
+    }
+    p->device = dev;
+    p->num_clusters = o.num_clusters > 0 ? std::min(o.num_clusters, clusters) : clusters;
+  } else {
+    p->num_clusters = o.num_clusters;
+  }
+  build_schedule(p);
+  st = upload(p, nullptr, true);
+  if (st != MLA_OK) {
+    free_plan(p);
+    return st;
+  }
+  *plan_out = p;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_plan(int B, int H, const int32_t* seq_lens_host, int block_size,
+                             int max_blocks, mla_plan_t* plan_out) {
+  return mla_decode_plan_ex(B, H, seq_lens_host, block_size, max_blocks, nullptr, plan_out);
+}
+
+mla_status_t mla_plan_update(mla_plan_t p, const int32_t* seq_lens_host, void* stream) {
+  if (!p) return MLA_ERR_INVALID_ARG;
+  mla_status_t st = check_plan_args(p->B, p->H, seq_lens_host, p->block_size, p->max_blocks);
+  if (st != MLA_OK) return st;
+  if (!p->host_only) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device) return MLA_ERR_INVALID_ARG;
+  }
+  p->seq_lens.assign(seq_lens_host, seq_lens_host + p->B);
+  build_schedule(p);
+  return upload(p, static_cast<cudaStream_t>(stream), false);
+}
+
+size_t mla_plan_workspace_bytes(mla_plan_t p) { return p ? p->workspace_bytes : 0; }
+
+int mla_plan_num_splits(mla_plan_t p, int b) {
+  if (!p || b < 0 || b >= p->B) return -1;
+  return p->splits[b];
+}
+
+int mla_plan_num_work_items(mla_plan_t p) { return p ? static_cast<int>(p->items.size()) : -1; }
+
+int mla_plan_num_clusters(mla_plan_t p) { return p ? p->num_clusters : -1; }
+
+int mla_plan_work_item(mla_plan_t p, int i, int32_t* b, int32_t* t0, int32_t* t1, int32_t* slot,
+                       int32_t* cluster) {
+  if (!p || i < 0 || i >= static_cast<int>(p->items.size())) return -1;
+  const WorkItem& w = p->items[i];
+  if (b) *b = w.b;
+  if (t0) *t0 = w.t0;
+  if (t1) *t1 = w.t1;
+  if (slot) *slot = w.slot;
+  if (cluster) *cluster = p->item_cluster[i];
+  return 0;
+}
+
+mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, const void* kv_cache,
+                        int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                        float sm_scale, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!p || p->host_only) return MLA_ERR_INVALID_ARG;
+  if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || num_blocks * p->block_size + 64 >= (int64_t{1} << 31))
+    return MLA_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+  if (p->workspace_bytes > 0) {
+    if (!workspace || workspace_bytes < p->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_UNSUPPORTED_DEVICE;
+  if (dev != p->device) return MLA_ERR_INVALID_ARG;
+  mla_status_t st = prepare_device(dev, nullptr);
+  if (st != MLA_OK) return st;
+
+  if (p->tmap_ptr != kv_cache || p->tmap_blocks != num_blocks) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return MLA_ERR_CUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kD),
+                                static_cast<cuuint64_t>(num_blocks) * p->block_size};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kD) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kPanelCols),
+                               static_cast<cuuint32_t>(std::min(p->block_size, 32))};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache),
+                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      p->tmap_ptr = nullptr;
+      return MLA_ERR_INVALID_ARG;
+    }
+    p->tmap_ptr = kv_cache;
+    p->tmap_blocks = num_blocks;
+  }
+
+  mla::DecodeParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.tmap_kv = p->tmap;
+  dp.q_nope = static_cast<const uint16_t*>(q_nope);
+  dp.q_pe = static_cast<const uint16_t*>(q_pe);
+  dp.block_table = block_table;
+  dp.seq_lens = seq_lens;
+  dp.out = static_cast<uint16_t*>(out);
+  dp.lse = lse;
+  const size_t o_bytes = static_cast<size_t>(p->num_slots) * p->H * mla::kDc * 4;
+  dp.part_o = static_cast<float*>(workspace);
+  dp.part_lse = p->num_slots
+                    ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align_up(o_bytes, 256))
+                    : nullptr;
+  dp.items = reinterpret_cast<const WorkItem*>(p->d_buf + p->off_items);
+  dp.cluster_offsets = reinterpret_cast<const int32_t*>(p->d_buf + p->off_offsets);
+  dp.err = reinterpret_cast<uint32_t*>(p->d_buf);
+  dp.H = p->H;
+  dp.block_size = p->block_size;
+  dp.max_blocks = p->max_blocks;
+  dp.rows_per_box = std::min(p->block_size, 32);
+  dp.num_blocks = num_blocks;
+  dp.scale_log2 = sm_scale * 1.4426950408889634f;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mla::launch_decode(dp, p->num_clusters, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (!p->combine.empty()) {
+    mla::CombineParams cp;
+    cp.items = reinterpret_cast<const CombineItem*>(p->d_buf + p->off_combine);
+    cp.part_o = dp.part_o;
+    cp.part_lse = dp.part_lse;
+    cp.out = dp.out;
+    cp.lse = lse;
+    cp.H = p->H;
+    if (mla::launch_combine(cp, static_cast<int>(p->combine.size()), s) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+mla_status_t mla_check_device_error(mla_plan_t p, void* stream, uint32_t* bits_out) {
+  if (bits_out) *bits_out = 0;
+  if (!p || p->host_only || !p->d_buf) return MLA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  uint32_t bits = 0;
+  if (cudaMemcpy(&bits, p->d_buf, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (bits && cudaMemset(p->d_buf, 0, 4) != cudaSuccess) return MLA_ERR_CUDA;
+  if (bits_out) *bits_out = bits;
+  return bits ? MLA_ERR_DEVICE_FAULT : MLA_OK;
+}
+
+void mla_plan_destroy(mla_plan_t p) { free_plan(p); }
+
+const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MLA_ERR_CUDA: return "CUDA runtime error";
+    case MLA_ERR_DEVICE_FAULT: return "device reported bad input";
+  }
+  return "unknown status";
+}
+
+int mla_device_supported(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  return device_is_sm103(dev) ? 1 : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,602 @@
+// Paged MLA decode kernel for sm_103a (GB300).
+//
+// What it computes: for each work item (tokens [t0, t1) of request b) and each
+// query head h, softmax(sm_scale * [q_nope|q_pe] . [c_kv|k_pe]^T) . c_kv over
+// the item's tokens, gathered from the paged latent cache through the block
+// table — the MLA decode of "SM100 Cutlass MLA decode with unrestricted
+// num_heads (< 128) for DeepSeek TP" (vLLM PR #20769) and "[Kernel] Flashinfer
+// MLA (trtllm-gen) decode kernel integration" (vLLM PR #21078). An item that
+// covers a whole request writes out (bf16) and lse; a split item writes its
+// normalised partial output and LSE for the combine kernel (the split-KV plus
+// reduction scheme of PR #20769's bot summary).
+//
+// Design (GB300-first; the pages' kernels are prior art, not the blueprint):
+// one 2-CTA cluster per work list, with split roles, because the fp32 output
+// accumulator of 128 heads x 512 columns fills a whole SM's tensor memory:
+//  * score CTA (cluster rank 0): streams 96-token KV tiles (all 576 columns)
+//    into two 108 KB shared-memory stages with TMA (one 32-row box per page
+//    slice and 64-column panel, block ids resolved from the block table),
+//    keeps Q [128 heads x 576] in tensor memory, issues S = Q.K^T with
+//    tcgen05 (M = 128 heads, N = 96 tokens, A from tensor memory), runs the
+//    fp32 online softmax (one thread per head row, lazy rescaling), and sends
+//    P (bf16) plus per-row rescale factors to the output CTA with st.async.
+//  * output CTA (rank 1): holds O [128 x 512] fp32 in tensor memory, streams
+//    V half-tiles (256 columns) into a 3-slot ring with its own TMA loads
+//    (L2 hits: the score CTA just read the same lines), issues O += P.V with
+//    tcgen05 (N = 256), applies the rescale when the softmax max moved, and
+//    writes the normalised output.
+// Heads below 128 are padded inside the kernel: zero Q rows in tensor memory
+// and zero P rows in shared memory, never stored.
+#include <cuda_runtime.h>
+
+#include "mla_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace mla {
+namespace {
+
+// Control block: identical offsets in both CTAs of the pair, so a barrier can
+// be addressed in the peer by offset (mapa, multicast commit).
+struct Ctrl {
+  uint64_t kv_full[kNumStages];   // score: stage landed (TMA bytes)
+  uint64_t kv_empty[kNumStages];  // score: S MMAs done reading the stage
+  uint64_t s_full[2];             // score: S tile in tensor memory
+  uint64_t s_free[2];             // score: softmax copied S out
+  uint64_t q_ready;               // score: Q of the next item in tensor memory
+  uint64_t p_empty[kNumPBufs];    // score: peer finished P.V on P buffer k
+  uint64_t v_full[kNumVSlots];    // output: V half landed
+  uint64_t v_empty[kNumVSlots];   // output: P.V done reading the V half
+  uint64_t p_full[kNumPBufs];     // output: P tile and row record landed (st.async bytes)
+  uint64_t o_ready[2];            // output: O rescaled / drained for tile g (alternating)
+  uint64_t o_done[2];             // output: P.V of tile g complete (alternating)
+  uint32_t tmem_base;
+  uint32_t pad;
+};
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTile, 0, 0);   // K-major A and B
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);    // V is MN-major
+constexpr float kRescaleThreshold = 8.0f;                        // log2 units
+constexpr int kRowBytesSent = kTile * 2 + kRecFloats * 4;        // 204 per head row
+
+MLA_DEVI int tiles_of(const WorkItem& it) {
+  return it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
+}
+
+// Row of the 2-D cache view holding token t of request b, or the first row
+// past the pool (a TMA box there reads zeros) for tokens at or past t_end and
+// for out-of-range block ids (which also raise MLA_DEVERR_BAD_BLOCK).
+MLA_DEVI int cache_row(const DecodeParams& p, int b, int t, int t_end, uint32_t& err) {
+  const int oob = static_cast<int>(p.num_blocks * p.block_size);
+  if (t >= t_end) return oob;
+  const int page = t / p.block_size;
+  const int blk = __ldg(&p.block_table[static_cast<int64_t>(b) * p.max_blocks + page]);
+  if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
+    err |= 1u;  // MLA_DEVERR_BAD_BLOCK
+    return oob;
+  }
+  return blk * p.block_size + (t % p.block_size);
+}
+
+MLA_DEVI void report(const DecodeParams& p, uint32_t bits) {
+  if (bits) atomicOr(p.err, bits);
+}
+
+// ------------------------------------------------------------ score CTA roles
+
+// TMA producer: all 9 panels of each 96-token tile into stage g % 2.
+MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int it0, int it1) {
+  uint32_t err = 0;
+  const uint64_t policy = policy_evict_normal();
+  const int R = p.rows_per_box;
+  const int nsub = kTile / R;
+  int g = 0;
+  bool ok = true;
+  for (int it = it0; it < it1 && ok; ++it) {
+    const WorkItem w = p.items[it];
+    if (__ldg(&p.seq_lens[w.b]) != w.seq_len) err |= 2u;  // MLA_DEVERR_SEQLEN_MISMATCH
+    // Warm L2 with the Q rows of the next non-empty item.
+    for (int nx = it + 1; nx < it1; ++nx) {
+      const WorkItem wn = p.items[nx];
+      if (tiles_of(wn) == 0) continue;
+      const uint16_t* qn = p.q_nope + static_cast<int64_t>(wn.b) * p.H * kDc;
+      const uint16_t* qp = p.q_pe + static_cast<int64_t>(wn.b) * p.H * kDr;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qn), "r"(p.H * kDc * 2) : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qp), "r"(p.H * kDr * 2) : "memory");
+      break;
+    }
+    const int nt = tiles_of(w);
+    for (int i = 0; i < nt; ++i, ++g) {
+      const int s = g & 1;
+      if (g >= kNumStages && !mbar_wait(smem_addr(&c->kv_empty[s]), ((g >> 1) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint32_t full = smem_addr(&c->kv_full[s]);
+      mbar_arrive_expect_tx(full, kStageBytes);
+      const uint32_t stage = smem_addr(data + s * kStageBytes);
+      const int tile_t0 = w.t0 + i * kTile;
+      for (int sb = 0; sb < nsub; ++sb) {
+        const int y = cache_row(p, w.b, tile_t0 + sb * R, w.t1, err);
+        const uint32_t dst = stage + sb * R * 128;
+#pragma unroll
+        for (int pc = 0; pc < kNumPanels; ++pc)
+          tma_load_2d(dst + pc * kPanelBytes, &p.tmap_kv, pc * kPanelCols, y, full, policy);
+      }
+    }
+  }
+  if (!ok) err |= 4u;
+  report(p, err);
+}
+
+// MMA issuer: S[g%2] = Q . K^T over the 576 columns (36 k-steps of 16).
+MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
+                        int it1) {
+  int g = 0, n_items = 0;
+  bool ok = true;
+  for (int it = it0; it < it1 && ok; ++it) {
+    const WorkItem w = p.items[it];
+    const int nt = tiles_of(w);
+    if (nt == 0) continue;
+    if (!mbar_wait(smem_addr(&c->q_ready), n_items & 1)) { ok = false; break; }
+    ++n_items;
+    for (int i = 0; i < nt; ++i, ++g) {
+      const int s = g & 1;
+      if (!mbar_wait(smem_addr(&c->kv_full[s]), (g >> 1) & 1)) { ok = false; break; }
+      if (g >= 2 && !mbar_wait(smem_addr(&c->s_free[s]), ((g >> 1) - 1) & 1)) { ok = false; break; }
+      tc_after_sync();
+      const uint32_t d = tmem + kTmemS0 + s * kTile;
+      const uint64_t b0 = smem_desc(smem_addr(data + s * kStageBytes), 16, 1024);
+#pragma unroll
+      for (int k = 0; k < kD / 16; ++k) {
+        // panel k/4, 32 bytes per k-step inside the 128-byte swizzle row
+        const uint64_t bd = b0 + static_cast<uint64_t>(((k >> 2) * kPanelBytes + (k & 3) * 32) >> 4);
+        mma_ts(d, tmem + kTmemQ + k * 8, bd, kIdescS, k > 0 ? 1u : 0u);
+      }
+      tc_commit(smem_addr(&c->s_full[s]));
+      tc_commit(smem_addr(&c->kv_empty[s]));
+    }
+  }
+  if (!ok) report(p, 4u);
+}
+
+// Load Q rows of request b into tensor memory columns [0, 288): lane = head,
+// two bf16 per column. Rows at or past H are zero (in-kernel head padding).
+MLA_DEVI void load_q(const DecodeParams& p, int b, int row, uint32_t trow) {
+  const bool valid = row < p.H;
+  const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<int64_t>(b) * p.H + row) * kDc);
+  const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + (static_cast<int64_t>(b) * p.H + row) * kDr);
+#pragma unroll
+  for (int grp = 0; grp < 3; ++grp) {
+    uint4 v[3][8];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int cc = grp * 3 + j;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        v[j][e] = valid ? __ldg(cc < 8 ? qn + cc * 8 + e : qp + e) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      uint32_t r[32];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        r[4 * e + 0] = v[j][e].x;
+        r[4 * e + 1] = v[j][e].y;
+        r[4 * e + 2] = v[j][e].z;
+        r[4 * e + 3] = v[j][e].w;
+      }
+      tmem_st32(trow + kTmemQ + (grp * 3 + j) * 32, r);
+    }
+  }
+  tmem_wait_st();
+}
+
+// Softmax warps: one thread per head row (TMEM lane).
+MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint32_t tmem, int warp, int lane,
+                            int it0, int it1) {
+  const int row = (warp & 3) * 32 + lane;
+  const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const bool active = row < p.H;
+  const float sl2 = p.scale_log2;
+  // Peer (output CTA) addresses of the P buffers and their barriers.
+  const uint32_t pbuf0 = map_to_rank(smem_addr(reinterpret_cast<uint8_t*>(c) + kCtrlBytes +
+                                               kNumVSlots * kVHalfBytes), 1);
+  const uint32_t pfull0 = map_to_rank(smem_addr(&c->p_full[0]), 1);
+
+  auto next_nonempty = [&](int from) {
+    for (int nx = from; nx < it1; ++nx)
+      if (tiles_of(p.items[nx]) > 0) return nx;
+    return it1;
+  };
+
+  int g = 0;
+  bool ok = true;
+  int cur = next_nonempty(it0);
+  if (cur < it1) {
+    load_q(p, p.items[cur].b, row, trow);
+    tc_before_sync();
+    mbar_arrive(smem_addr(&c->q_ready));
+  }
+  while (cur < it1 && ok) {
+    const WorkItem w = p.items[cur];
+    const int nt = tiles_of(w);
+    const int nxt = next_nonempty(cur + 1);
+    float m_used = -INFINITY, l = 0.0f;
+    for (int i = 0; i < nt; ++i, ++g) {
+      const int s = g & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&c->s_full[s]), (g >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_after_sync();
+      uint32_t ra[32], rb[32], rc[32];
+      tmem_ld32(trow + kTmemS0 + s * kTile + 0, ra);
+      tmem_ld32(trow + kTmemS0 + s * kTile + 32, rb);
+      tmem_ld32(trow + kTmemS0 + s * kTile + 64, rc);
+      tmem_wait_ld();
+      tc_before_sync();
+      mbar_arrive(smem_addr(&c->s_free[s]));
+      if (i == nt - 1 && nxt < it1) {
+        // All S MMAs of this item are complete: Q's columns are free.
+        load_q(p, p.items[nxt].b, row, trow);
+        tc_before_sync();
+        mbar_arrive(smem_addr(&c->q_ready));
+      }
+      const int k = g & 1;
+      if (g >= kNumPBufs &&
+          !__all_sync(0xffffffffu, mbar_wait_cluster(smem_addr(&c->p_empty[k]), ((g >> 1) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      if (!active) continue;
+      float x[kTile];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        x[j] = __uint_as_float(ra[j]);
+        x[32 + j] = __uint_as_float(rb[j]);
+        x[64 + j] = __uint_as_float(rc[j]);
+      }
+      const int valid = min(kTile, w.t1 - (w.t0 + i * kTile));
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kTile; j += 4) {
+        if (j + 0 >= valid) x[j + 0] = -INFINITY;
+        if (j + 1 >= valid) x[j + 1] = -INFINITY;
+        if (j + 2 >= valid) x[j + 2] = -INFINITY;
+        if (j + 3 >= valid) x[j + 3] = -INFINITY;
+        mx0 = fmaxf(mx0, x[j + 0]);
+        mx1 = fmaxf(mx1, x[j + 1]);
+        mx2 = fmaxf(mx2, x[j + 2]);
+        mx3 = fmaxf(mx3, x[j + 3]);
+      }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      float alpha = 1.0f;
+      if (m_tile > m_used + kRescaleThreshold) {
+        alpha = fast_exp2(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
+        l *= alpha;
+        m_used = m_tile;
+      }
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      uint32_t pk[kTile / 2];
+#pragma unroll
+      for (int j = 0; j < kTile; j += 4) {
+        const float e0 = fast_exp2(fmaf(x[j + 0], sl2, -m_used));
+        const float e1 = fast_exp2(fmaf(x[j + 1], sl2, -m_used));
+        const float e2 = fast_exp2(fmaf(x[j + 2], sl2, -m_used));
+        const float e3 = fast_exp2(fmaf(x[j + 3], sl2, -m_used));
+        l0 += e0;
+        l1 += e1;
+        l2 += e2;
+        l3 += e3;
+        pk[j / 2] = pack_bf16x2(e0, e1);
+        pk[j / 2 + 1] = pack_bf16x2(e2, e3);
+      }
+      l += (l0 + l1) + (l2 + l3);
+      const uint32_t pb = pbuf0 + k * kPBufBytes;
+      const uint32_t bar = pfull0 + k * 8;
+#pragma unroll
+      for (int q = 0; q < kTile / 8; ++q) {
+        const uint32_t addr = pb + (q >> 3) * kPPanelBytes + row * 128 + (((q & 7) ^ (row & 7)) << 4);
+        st_async_v4(addr, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3], bar);
+      }
+      st_async_b32(pb + kPBytes + row * 4, __float_as_uint(alpha), bar);
+      st_async_b32(pb + kPBytes + 512 + row * 4, __float_as_uint(l), bar);
+      st_async_b32(pb + kPBytes + 1024 + row * 4, __float_as_uint(m_used), bar);
+    }
+    cur = nxt;
+  }
+  // Drain: the peer's last commits arrive on p_empty; consume them so no
+  // remote arrival is still in flight when this CTA exits.
+  for (int gg = (g > 2 ? g - 2 : 0); gg < g && ok; ++gg)
+    if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_addr(&c->p_empty[gg & 1]), (gg >> 1) & 1)))
+      ok = false;
+  if (!ok) report(p, 4u);
+}
+
+// ----------------------------------------------------------- output CTA roles
+
+// TMA producer: V half-tiles (4 panels = 256 columns) into a 3-slot ring.
+MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int it0, int it1) {
+  uint32_t err = 0;
+  const uint64_t policy = policy_evict_first();   // last use of these lines
+  const int R = p.rows_per_box;
+  const int nsub = kTile / R;
+  int h = 0;
+  bool ok = true;
+  for (int it = it0; it < it1 && ok; ++it) {
+    const WorkItem w = p.items[it];
+    const int nt = tiles_of(w);
+    for (int i = 0; i < nt && ok; ++i) {
+      const int tile_t0 = w.t0 + i * kTile;
+      int ys[kTile / 16];
+      for (int sb = 0; sb < nsub; ++sb) ys[sb] = cache_row(p, w.b, tile_t0 + sb * R, w.t1, err);
+      for (int half = 0; half < 2; ++half, ++h) {
+        const int v = h % kNumVSlots;
+        if (h >= kNumVSlots && !mbar_wait(smem_addr(&c->v_empty[v]), ((h / kNumVSlots) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = smem_addr(&c->v_full[v]);
+        mbar_arrive_expect_tx(full, kVHalfBytes);
+        const uint32_t slot = smem_addr(data + v * kVHalfBytes);
+        for (int sb = 0; sb < nsub; ++sb) {
+          const uint32_t dst = slot + sb * R * 128;
+#pragma unroll
+          for (int pc = 0; pc < kVHalfPanels; ++pc)
+            tma_load_2d(dst + pc * kPanelBytes, &p.tmap_kv, (half * kVHalfPanels + pc) * kPanelCols,
+                        ys[sb], full, policy);
+        }
+      }
+    }
+  }
+  if (!ok) err |= 4u;
+  report(p, err);
+}
+
+// MMA issuer: O[:, 256*half ...] += P . V_half (6 k-steps of 16 tokens each).
+MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
+                      int it1) {
+  int g = 0, h = 0;
+  bool ok = true;
+  uint8_t* pbufs = data + kNumVSlots * kVHalfBytes;
+  for (int it = it0; it < it1 && ok; ++it) {
+    const WorkItem w = p.items[it];
+    const int nt = tiles_of(w);
+    for (int i = 0; i < nt; ++i, ++g) {
+      const int k = g & 1;
+      if (!mbar_wait(smem_addr(&c->o_ready[g & 1]), (g >> 1) & 1)) { ok = false; break; }
+      tc_after_sync();
+      const uint64_t a0 = smem_desc(smem_addr(pbufs + k * kPBufBytes), 16, 1024);
+      for (int half = 0; half < 2; ++half, ++h) {
+        const int v = h % kNumVSlots;
+        if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
+        tc_after_sync();
+        const uint64_t b0 = smem_desc(smem_addr(data + v * kVHalfBytes), kPanelBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t ad = a0 + static_cast<uint64_t>(((kk >> 2) * kPPanelBytes + (kk & 3) * 32) >> 4);
+          const uint64_t bd = b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+          mma_ss(tmem + half * 256, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_addr(&c->v_empty[v]));
+      }
+      if (!ok) break;
+      tc_commit(smem_addr(&c->o_done[g & 1]));
+      tc_commit_multicast(smem_addr(&c->p_empty[k]), static_cast<uint16_t>(0x1));
+    }
+  }
+  if (!ok) report(p, 4u);
+}
+
+// Correction + epilogue warps: one thread per head row (TMEM lane).
+MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int warp,
+                          int lane, int it0, int it1) {
+  const int row = (warp & 3) * 32 + lane;
+  const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const bool active = row < p.H;
+  const bool elected = (warp == 2 && lane == 0);
+  const uint8_t* pbufs = data + kNumVSlots * kVHalfBytes;
+  int g = 0;
+  bool ok = true;
+  for (int it = it0; it < it1 && ok; ++it) {
+    const WorkItem w = p.items[it];
+    const int nt = tiles_of(w);
+    const int64_t orow = static_cast<int64_t>(w.b) * p.H + row;
+    if (nt == 0) {  // empty request: out = 0, lse = -inf
+      if (active && w.slot < 0) {
+        uint4* o = reinterpret_cast<uint4*>(p.out + orow * kDc);
+        for (int e = 0; e < kDc / 8; ++e) o[e] = make_uint4(0u, 0u, 0u, 0u);
+        p.lse[orow] = -INFINITY;
+      }
+      continue;
+    }
+    float l_fin = 1.0f, m_fin = 0.0f;
+    for (int i = 0; i < nt; ++i, ++g) {
+      const int k = g & 1;
+      if (elected) mbar_arrive_expect_tx(smem_addr(&c->p_full[k]), p.H * kRowBytesSent);
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_addr(&c->p_full[k]), (g >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      const float* rec = reinterpret_cast<const float*>(pbufs + k * kPBufBytes + kPBytes);
+      const float alpha = active ? rec[row] : 1.0f;
+      const float lv = rec[128 + row];
+      const float mv = rec[256 + row];
+      fence_proxy_async_smem();
+      if (i > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_after_sync();
+#pragma unroll 1
+        for (int cc = 0; cc < kDc / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(trow + cc * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+          tmem_st32(trow + cc * 32, r);
+        }
+        tmem_wait_st();
+      }
+      tc_before_sync();
+      mbar_arrive(smem_addr(&c->o_ready[g & 1]));
+      if (i == nt - 1) {
+        l_fin = lv;
+        m_fin = mv;
+      }
+    }
+    if (!ok) break;
+    // Epilogue: O / l -> out (bf16) or the split partial (fp32).
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
+      ok = false;
+      break;
+    }
+    tc_after_sync();
+    const float inv_l = 1.0f / l_fin;
+    const float lse_val = (m_fin + __log2f(l_fin)) * 0.69314718055994531f;
+#pragma unroll 1
+    for (int cc = 0; cc < kDc / 32; ++cc) {
+      uint32_t r[32];
+      tmem_ld32(trow + cc * 32, r);
+      tmem_wait_ld();
+      if (!active) continue;
+      if (w.slot < 0) {
+        uint4* o = reinterpret_cast<uint4*>(p.out + orow * kDc + cc * 32);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
+          v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
+          v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
+          v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
+          o[e] = v;
+        }
+      } else {
+        float4* o = reinterpret_cast<float4*>(p.part_o + (static_cast<int64_t>(w.slot) * p.H + row) * kDc + cc * 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          o[e] = make_float4(__uint_as_float(r[4 * e + 0]) * inv_l, __uint_as_float(r[4 * e + 1]) * inv_l,
+                             __uint_as_float(r[4 * e + 2]) * inv_l, __uint_as_float(r[4 * e + 3]) * inv_l);
+      }
+    }
+    if (active) {
+      if (w.slot < 0) p.lse[orow] = lse_val;
+      else p.part_lse[static_cast<int64_t>(w.slot) * p.H + row] = lse_val;
+    }
+    tc_before_sync();
+  }
+  if (!ok) report(p, 4u);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mla_decode_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Ctrl* c = reinterpret_cast<Ctrl*>(base);
+  uint8_t* data = base + kCtrlBytes;
+  const uint32_t rank = cluster_rank();
+  const int cid = static_cast<int>(cluster_id_x());
+  const int it0 = p.cluster_offsets[cid];
+  const int it1 = p.cluster_offsets[cid + 1];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNumStages; ++s) {
+      mbar_init(smem_addr(&c->kv_full[s]), 1);
+      mbar_init(smem_addr(&c->kv_empty[s]), 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(smem_addr(&c->s_full[j]), 1);
+      mbar_init(smem_addr(&c->s_free[j]), 128);
+      mbar_init(smem_addr(&c->o_ready[j]), 128);
+      mbar_init(smem_addr(&c->o_done[j]), 1);
+    }
+    mbar_init(smem_addr(&c->q_ready), 128);
+    for (int k = 0; k < kNumPBufs; ++k) {
+      mbar_init(smem_addr(&c->p_empty[k]), 1);
+      mbar_init(smem_addr(&c->p_full[k]), 1);
+    }
+    for (int v = 0; v < kNumVSlots; ++v) {
+      mbar_init(smem_addr(&c->v_full[v]), 1);
+      mbar_init(smem_addr(&c->v_empty[v]), 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&p.tmap_kv);
+  if (rank == 1) {
+    // Zero both P buffers once: rows >= H stay zero (padded heads).
+    uint4* pz = reinterpret_cast<uint4*>(data + kNumVSlots * kVHalfBytes);
+    for (int e = threadIdx.x; e < kNumPBufs * kPBufBytes / 16; e += kThreads)
+      pz[e] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&c->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_before_sync();
+  cluster_barrier();
+  tc_after_sync();
+  const uint32_t tmem = c->tmem_base;
+
+  if (rank == 0) {
+    if (warp == 0) {
+      if (lane == 0) score_producer(p, c, data, it0, it1);
+    } else if (warp == 1) {
+      if (lane == 0) score_mma(p, c, data, tmem, it0, it1);
+    } else {
+      score_softmax(p, c, tmem, warp, lane, it0, it1);
+    }
+  } else {
+    if (warp == 0) {
+      if (lane == 0) out_producer(p, c, data, it0, it1);
+    } else if (warp == 1) {
+      if (lane == 0) out_mma(p, c, data, tmem, it0, it1);
+    } else {
+      out_correct(p, c, data, tmem, warp, lane, it0, it1);
+    }
+  }
+  __syncwarp();
+  tc_before_sync();
+  cluster_barrier();
+  if (warp == 1) {
+    tc_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t decode_prepare_device() {
+  return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytes);
+}
+
+cudaError_t decode_max_clusters(int* num_clusters) {
+  cudaError_t e = decode_prepare_device();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(num_clusters, mla_decode_kernel, &cfg);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int num_clusters, cudaStream_t stream) {
+  mla_decode_kernel<<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1), kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,98 @@
+// Internal types shared by the planner, the C ABI layer and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+constexpr int kDc = 512;                 // latent c_kv columns (= V width)
+constexpr int kDr = 64;                  // rope k_pe columns
+constexpr int kD = kDc + kDr;            // 576 bf16 per cached token row
+constexpr int kMaxHeads = 128;           // MMA M; fewer heads are padded inside the kernel
+constexpr int kTile = 96;                // tokens per KV tile (MMA N of the score product)
+constexpr int kPanelCols = 64;           // bf16 columns of one 128-byte swizzle panel
+constexpr int kNumPanels = kD / kPanelCols;            // 9 panels per row
+constexpr int kPanelBytes = kTile * 128;               // one panel of one tile: 12 KB
+constexpr int kStageBytes = kNumPanels * kPanelBytes;  // full 576-wide tile: 108 KB
+constexpr int kVHalfPanels = 4;                        // V half = 256 columns
+constexpr int kVHalfBytes = kVHalfPanels * kPanelBytes;  // 48 KB
+constexpr int kNumStages = 2;            // score CTA: KV tiles in flight
+constexpr int kNumVSlots = 3;            // output CTA: V half-tiles in flight
+constexpr int kNumPBufs = 2;             // output CTA: P tiles in flight
+constexpr int kPPanelBytes = kMaxHeads * 128;          // 128 rows x 64 tokens (bf16)
+constexpr int kPBytes = 2 * kPPanelBytes;              // 96 tokens need two K panels
+constexpr int kRecFloats = 3;                          // per row: alpha, l, m
+constexpr int kPBufBytes = kPBytes + 2048;             // P plus the per-row record
+constexpr int kThreads = 192;            // 6 warps per CTA
+constexpr int kTmemCols = 512;
+// Score CTA TMEM columns: Q (576 bf16 packed in pairs) then two S buffers.
+constexpr int kTmemQ = 0;
+constexpr int kTmemS0 = kD / 2;          // 288
+// Shared-memory data region (after the 1 KB control block).
+constexpr int kCtrlBytes = 1024;
+constexpr int kScoreDataBytes = kNumStages * kStageBytes;                         // 216 KB
+constexpr int kOutDataBytes = kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes;  // 212 KB
+constexpr int kDataBytes = kScoreDataBytes > kOutDataBytes ? kScoreDataBytes : kOutDataBytes;
+constexpr int kSmemBytes = kCtrlBytes + kDataBytes + 1024;  // + alignment slack
+
+// One unit of work: tokens [t0, t1) of request b. slot >= 0 means the result
+// is a split partial written to the workspace; -1 writes out/lse directly.
+struct WorkItem {
+  int32_t b;
+  int32_t t0;
+  int32_t t1;
+  int32_t slot;
+  int32_t seq_len;   // the plan's length of request b (checked against device seq_lens)
+  int32_t pad[3];
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+
+// Requests whose KV was split: merge n partial slots starting at first_slot.
+struct CombineItem {
+  int32_t b;
+  int32_t first_slot;
+  int32_t n_slots;
+  int32_t pad;
+};
+
+struct DecodeParams {
+  CUtensorMap tmap_kv;            // 2-D view [num_blocks*block_size rows][576] bf16
+  const uint16_t* q_nope;         // [B, H, 512]
+  const uint16_t* q_pe;           // [B, H, 64]
+  const int32_t* block_table;     // [B, max_blocks]
+  const int32_t* seq_lens;        // [B] device copy
+  uint16_t* out;                  // [B, H, 512]
+  float* lse;                     // [B, H]
+  float* part_o;                  // [slots, H, 512]
+  float* part_lse;                // [slots, H]
+  const WorkItem* items;          // grouped by CTA pair
+  const int32_t* cluster_offsets; // [num_clusters + 1]
+  uint32_t* err;                  // device error word
+  int H;
+  int block_size;
+  int max_blocks;
+  int rows_per_box;               // min(block_size, 32)
+  int64_t num_blocks;
+  float scale_log2;               // sm_scale * log2(e)
+};
+
+struct CombineParams {
+  const CombineItem* items;
+  const float* part_o;
+  const float* part_lse;
+  uint16_t* out;
+  float* lse;
+  int H;
+};
+
+// Launchers (defined in the .cu files).
+cudaError_t launch_decode(const DecodeParams& p, int num_clusters, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int num_items, cudaStream_t stream);
+cudaError_t decode_max_clusters(int* num_clusters);
+cudaError_t decode_prepare_device();
+
+}  // namespace mla
