@@ -3,8 +3,24 @@
 The compute path is the C-ABI shared library declared in include/mla_decode.h
 (hand-written tcgen05/TMA kernels). This package is its thin Python binding;
 PyTorch supplies device memory and streams only.
+
+The binding loads the library on first use of any exported name; if the
+library has not been built (``python -m paged_mla_decode_05_gb300.build``)
+that first use raises ImportError. There is no fallback path.
 """
-from ._lib import (MLAError, Plan, mla_check_device_error, mla_decode, mla_decode_plan,  # noqa: F401
-                   mla_device_supported, mla_status_string, header_functions,
-                   MLA_DEVERR_BAD_BLOCK, MLA_DEVERR_SEQLEN_MISMATCH, MLA_DEVERR_TIMEOUT)
-from .api import decode  # noqa: F401
+_EXPORTS = ("MLAError", "Plan", "mla_check_device_error", "mla_decode", "mla_decode_plan",
+            "mla_device_supported", "mla_status_string", "header_functions",
+            "MLA_DEVERR_BAD_BLOCK", "MLA_DEVERR_SEQLEN_MISMATCH", "MLA_DEVERR_TIMEOUT")
+
+
+def __getattr__(name):
+    if name in _EXPORTS:
+        from . import _lib
+        return getattr(_lib, name)
+    if name == "decode":
+        from .api import decode
+        return decode
+    raise AttributeError(name)
+
+
+__all__ = list(_EXPORTS) + ["decode"]
