@@ -1,0 +1,434 @@
+"""Benchmark of the paged MLA decode (one JSON line on stdout, rank 0).
+
+Default workload: the high-concurrency decode, B=512 requests, H=128 heads,
+lengths 1024 + U{0..2048}, block size 32, a 35,265-block (~1.3 GB) bf16 latent
+cache (seeded synthetic data; the pages' kernel-only microbenchmark shape at
+bs=512, see "[Kernel] Flashinfer MLA (trtllm-gen) decode kernel integration",
+Kernel-only microbenchmark). A step is one ``mla_decode`` call (decode kernel,
+plus the combine kernel when the plan splits a request) with inputs resident
+in HBM; the cache alone is ten times the 129 MB L2, so no flush is needed
+between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME]
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload on the host cores (the slow baseline). Under torchrun (N > 1)
+every rank runs its own replica of the workload (the decode needs no
+collective); the timing is max-reduced over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import mla_workloads as wl  # noqa: E402
+
+METRIC = "MLA decode µs/call + KV-read HBM GB/s at B=512,H=128 vs roofline fraction"
+UNIT = "us/call"
+DEFAULT_CONFIG = "r1_b512_h128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_SRC = os.path.join(ROOT, "paged_mla_decode_05_gb300", "csrc", "mla_decode_sm103.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_r1_b512_h128_traffic.txt")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- measurements
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    with open(DECODE_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    vals = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != source_digest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_workload"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- our GPU path
+
+def bench_ours(args, world, rank, local):
+    import torch
+    dist = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import paged_mla_decode_05_gb300 as m
+    from paged_mla_decode_05_gb300 import build as _b
+    _b.build()
+
+    spec = wl.WORKLOADS_BY_NAME[args.config]
+    t0 = time.time()
+    w = wl.generate(spec)
+    log(f"[bench] generated {spec.name} in {time.time() - t0:.1f}s")
+    counts = wl.expected_counts(w)
+    B, H, bs = w["B"], w["H"], w["block_size"]
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q_nope, q_pe, kv = bf16(w["q_nope"]), bf16(w["q_pe"]), bf16(w["kv_cache"])
+    table = torch.from_numpy(w["block_table"]).to(dev)
+    lens = torch.from_numpy(w["seq_lens"]).to(dev)
+    plan = m.mla_decode_plan(B, H, w["seq_lens"], bs, int(w["max_blocks"]))
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    launches_per_step = 1 + (1 if plan.workspace_bytes else 0)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m.mla_decode(plan, q_nope, q_pe, kv, table, lens, w["sm_scale"], out, lse, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert m.mla_check_device_error(plan) == 0
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clocks = sampler.stop()
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    ms_per_step = total_ms / args.steps
+    us = ms_per_step * 1e3
+    assert m.mla_check_device_error(plan) == 0
+
+    # End to end through the public API with host buffers: pinned host inputs
+    # of the step (queries, block table, lengths) copied in, plan rebuilt from
+    # the host lengths, decode, and out + lse copied back. The cache is state
+    # resident on the device across steps, as in serving.
+    h_qn = torch.from_numpy(w["q_nope"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_qp = torch.from_numpy(w["q_pe"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_tab = torch.from_numpy(w["block_table"]).pin_memory()
+    h_len = torch.from_numpy(w["seq_lens"]).pin_memory()
+    h_out = torch.empty((B, H, 512), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    lens_np = w["seq_lens"].copy()
+    e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        q_nope.copy_(h_qn, non_blocking=True)
+        q_pe.copy_(h_qp, non_blocking=True)
+        table.copy_(h_tab, non_blocking=True)
+        lens.copy_(h_len, non_blocking=True)
+        plan.update(lens_np, stream)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    barrier(dist)
+    t_e = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - t_e) * 1e3 / e_steps
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_qn, h_qp, h_tab, h_len))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    t_bytes_us = counts["bytes"] / (hbm * 1e9) * 1e6
+    t_flops_us = counts["flops"] / (tf * 1e12) * 1e6
+    # Dominant kernel: the decode kernel. Without a split the step is exactly
+    # that one launch, so the step time is its duration.
+    dominant_us = us if launches_per_step == 1 else None
+    achieved = counts["bytes"] / (ms_per_step * 1e-3) / 1e9
+    traffic = recorded_traffic()
+    result = {
+        "metric": METRIC,
+        "value": round(us, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 latent cache and queries, sentinel-filled spare "
+                "blocks and tail slots)",
+        "config": {"workload": spec.name, "B": B, "H": H, "block_size": bs,
+                   "seq_lens": "1024+U{0..2048}" if spec.name.startswith("r1_") else spec.description,
+                   "tokens": counts["tokens"], "num_blocks": int(w["num_blocks"]),
+                   "cache_bytes": int(w["kv_cache"].nbytes),
+                   "l2": "inputs larger than L2 (cache ~10x the 129 MB L2); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "cta_pairs": plan.num_clusters, "work_items": plan.num_work_items,
+                   "split_requests": int(sum(plan.num_splits(b) > 1 for b in range(B)))},
+        "kv_read_gbs": round(counts["kv_bytes"] / (ms_per_step * 1e-3) / 1e9, 1),
+        "alg_bytes_per_call": counts["bytes"],
+        "alg_flops_per_call": counts["flops"],
+        "roofline": {
+            "bound": "hbm" if t_bytes_us >= t_flops_us else "tensor",
+            "achieved": round(achieved, 1),
+            "peak": hbm,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm, 4),
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                           else "fallback 6.8 TB/s",
+            "traffic": traffic,
+            "t_bytes_us": round(t_bytes_us, 2),
+            "t_flops_us": round(t_flops_us, 2),
+            "roofline_fraction": round(max(t_bytes_us, t_flops_us) / us, 4),
+            "dominant_kernel": "mla_decode_kernel",
+            "dominant_kernel_us": round(dominant_us, 2) if dominant_us else None,
+        },
+        "step_us_min": round(min(per_step) * 1e3, 2),
+        "step_us_median": round(statistics.median(per_step) * 1e3, 2),
+        "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ------------------------------------------------------------- CPU oracle leg
+
+def cpu_baseline(w, budget_s: float):
+    """The fp64 oracle as it stands, on a bounded sample of (request, head)
+    rows of the same workload, scaled to one full call."""
+    import oracle
+    oracle.build()
+    B, H = int(w["B"]), int(w["H"])
+    cores = oracle.num_threads(0)
+    rng = np.random.default_rng(123)
+    order = rng.permutation(B * H)
+    args = (w["q_nope"], w["q_pe"], w["kv_cache"], w["block_table"], w["seq_lens"], w["sm_scale"])
+    n = min(B * H, max(cores * 4, 64))
+    t0 = time.perf_counter()
+    rows = order[:n]
+    oracle.mla_decode_rows(*args, rows // H, rows % H)
+    pilot = time.perf_counter() - t0
+    n2 = int(min(B * H, max(n, n * budget_s / max(pilot, 1e-6))))
+    rows = order[:n2]
+    t0 = time.perf_counter()
+    oracle.mla_decode_rows(*args, rows // H, rows % H)
+    dt = time.perf_counter() - t0
+    seq = np.asarray(w["seq_lens"], dtype=np.int64)
+    frac_tokens = seq[rows // H].sum() / (seq.sum() * H)
+    per_call_s = dt / frac_tokens
+    return {"value": round(per_call_s * 1e6, 1), "unit": UNIT, "cores": int(cores), "kind": "oracle",
+            "sample": f"{n2} of {B * H} (request, head) rows, {dt:.1f} s, scaled by token share "
+                      f"{frac_tokens:.4f}"}
+
+
+def bench_reference(args, world, rank, local):
+    """--impl reference: the oracle on the host cores, each step a bounded sample."""
+    if world > 1:
+        init_dist(world, "gloo")
+        if rank != 0:
+            return None
+    spec = wl.WORKLOADS_BY_NAME[args.config]
+    w = wl.generate(spec)
+    import oracle
+    oracle.build()
+    B, H = int(w["B"]), int(w["H"])
+    cores = oracle.num_threads(0)
+    seq = np.asarray(w["seq_lens"], dtype=np.int64)
+    args_o = (w["q_nope"], w["q_pe"], w["kv_cache"], w["block_table"], w["seq_lens"], w["sm_scale"])
+    rng = np.random.default_rng(7)
+    total_steps = args.warmup + args.steps
+    # Each step: a fixed-size random sample of rows sized so the run stays
+    # within a few minutes.
+    pilot_rows = rng.permutation(B * H)[:max(cores * 2, 32)]
+    t0 = time.perf_counter()
+    oracle.mla_decode_rows(*args_o, pilot_rows // H, pilot_rows % H)
+    per_row = (time.perf_counter() - t0) / len(pilot_rows)
+    n_rows = int(max(16, min(B * H, (120.0 / max(total_steps, 1)) / max(per_row, 1e-9))))
+    times = []
+    for s in range(total_steps):
+        rows = rng.permutation(B * H)[:n_rows]
+        t0 = time.perf_counter()
+        oracle.mla_decode_rows(*args_o, rows // H, rows % H)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            share = seq[rows // H].sum() / (seq.sum() * H)
+            times.append(dt / share)
+    us = statistics.mean(times) * 1e6
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "B": B, "H": H, "block_size": int(w["block_size"])},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": int(cores), "kind": "oracle",
+                         "sample": f"{n_rows} random (request, head) rows per step, scaled by "
+                                   "token share to one full call"},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.WORKLOADS_BY_NAME))
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if world != args.gpus and world > 1:
+        log(f"[bench] WORLD_SIZE={world} differs from --gpus {args.gpus}; using WORLD_SIZE")
+    fn = bench_reference if args.impl == "reference" else bench_ours
+    res = fn(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

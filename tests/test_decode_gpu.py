@@ -78,8 +78,10 @@ def test_forced_splits_match_oracle_and_unsplit(lib, oracle_mod, splits):
     out1, lse1, _ = full_parity(oracle_mod, w)
     out2, lse2, plan = full_parity(oracle_mod, w, force_splits=splits)
     assert plan.num_splits(0) == splits and plan.workspace_bytes > 0
-    # Split invariance: different partitions agree within rounding.
-    assert np.max(np.abs(out1 - out2)) < 2e-2 and np.max(np.abs(lse1 - lse2)) < 2e-3
+    # Split invariance: different partitions agree within the parity tolerance
+    # (they differ by fp32 summation order and one bf16 rounding of out).
+    assert np.all(np.abs(out1 - out2) <= 2e-2 + 2e-2 * np.abs(out1))
+    assert np.max(np.abs(lse1 - lse2)) < 2e-3
 
 
 def test_block_permutation_is_bit_identical(lib, oracle_mod):
