@@ -82,6 +82,25 @@ MLA_DEVI void report(const DecodeParams& p, uint32_t bits) {
   if (bits) atomicOr(p.err, bits);
 }
 
+// Optional timeline instrumentation (compiled only with -DMLA_TRACE): each
+// role of the CTA pairs listed in the trace buffer records %globaltimer at
+// fixed points of every tile. Records time only; skips no work.
+#ifdef MLA_TRACE
+__device__ uint64_t* g_mla_trace = nullptr;   // [pairs][2 ranks][kTraceEvents][kTraceTiles]
+constexpr int kTracePairs = 4, kTraceEvents = 16, kTraceTiles = 256;
+MLA_DEVI void trace(int ev, int g) {
+  uint64_t* t = g_mla_trace;
+  const int pair = static_cast<int>(cluster_id_x());
+  if (t == nullptr || pair >= kTracePairs || g >= kTraceTiles) return;
+  uint64_t now;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+  t[((pair * 2 + cluster_rank()) * kTraceEvents + ev) * kTraceTiles + g] = now;
+}
+#define MLA_TRACE_AT(ev, g) trace(ev, g)
+#else
+#define MLA_TRACE_AT(ev, g) ((void)0)
+#endif
+
 // ------------------------------------------------------------ score CTA roles
 
 // TMA producer: all 9 panels of each 96-token tile into stage g % 2.
@@ -112,6 +131,7 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
         ok = false;
         break;
       }
+      MLA_TRACE_AT(0, g);
       const uint32_t full = smem_addr(&c->kv_full[s]);
       mbar_arrive_expect_tx(full, kStageBytes);
       const uint32_t stage = smem_addr(data + s * kStageBytes);
@@ -143,7 +163,9 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
       if (!mbar_wait(smem_addr(&c->kv_full[s]), (g >> 1) & 1)) { ok = false; break; }
+      MLA_TRACE_AT(1, g);
       if (g >= 2 && !mbar_wait(smem_addr(&c->s_free[s]), ((g >> 1) - 1) & 1)) { ok = false; break; }
+      MLA_TRACE_AT(2, g);
       tc_after_sync();
       const uint32_t d = tmem + kTmemS0 + s * kTile;
       const uint64_t b0 = smem_desc(smem_addr(data + s * kStageBytes), 16, 1024);
@@ -155,6 +177,7 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
       }
       tc_commit(smem_addr(&c->s_full[s]));
       tc_commit(smem_addr(&c->kv_empty[s]));
+      MLA_TRACE_AT(3, g);
     }
   }
   if (!ok) report(p, 4u);
@@ -229,6 +252,7 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint32_t tmem, int w
         ok = false;
         break;
       }
+      if (row == 0) MLA_TRACE_AT(4, g);
       tc_after_sync();
       uint32_t ra[32], rb[32], rc[32];
       tmem_ld32(trow + kTmemS0 + s * kTile + 0, ra);
@@ -249,6 +273,7 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint32_t tmem, int w
         ok = false;
         break;
       }
+      if (row == 0) MLA_TRACE_AT(5, g);
       if (!active) continue;
       float x[kTile];
 #pragma unroll
@@ -303,6 +328,7 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint32_t tmem, int w
       st_async_b32(pb + kPBytes + row * 4, __float_as_uint(alpha), bar);
       st_async_b32(pb + kPBytes + 512 + row * 4, __float_as_uint(l), bar);
       st_async_b32(pb + kPBytes + 1024 + row * 4, __float_as_uint(m_used), bar);
+      if (row == 0) MLA_TRACE_AT(6, g);
     }
     cur = nxt;
   }
@@ -337,6 +363,7 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int it
           ok = false;
           break;
         }
+        MLA_TRACE_AT(8 + half, h >> 1);
         const uint32_t full = smem_addr(&c->v_full[v]);
         mbar_arrive_expect_tx(full, kVHalfBytes);
         const uint32_t slot = smem_addr(data + v * kVHalfBytes);
@@ -366,11 +393,13 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
     for (int i = 0; i < nt; ++i, ++g) {
       const int k = g & 1;
       if (!mbar_wait(smem_addr(&c->o_ready[g & 1]), (g >> 1) & 1)) { ok = false; break; }
+      MLA_TRACE_AT(10, g);
       tc_after_sync();
       const uint64_t a0 = smem_desc(smem_addr(pbufs + k * kPBufBytes), 16, 1024);
       for (int half = 0; half < 2; ++half, ++h) {
         const int v = h % kNumVSlots;
         if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
+        MLA_TRACE_AT(11 + half, g);
         tc_after_sync();
         const uint64_t b0 = smem_desc(smem_addr(data + v * kVHalfBytes), kPanelBytes, 1024);
 #pragma unroll
@@ -383,6 +412,7 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
       }
       if (!ok) break;
       tc_commit(smem_addr(&c->o_done[g & 1]));
+      MLA_TRACE_AT(13, g);
       tc_commit_multicast(smem_addr(&c->p_empty[k]), static_cast<uint16_t>(0x1));
     }
   }
@@ -419,6 +449,7 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
         ok = false;
         break;
       }
+      if (row == 0) MLA_TRACE_AT(14, g);
       const float* rec = reinterpret_cast<const float*>(pbufs + k * kPBufBytes + kPBytes);
       const float alpha = active ? rec[row] : 1.0f;
       const float lv = rec[128 + row];
@@ -443,6 +474,7 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
       }
       tc_before_sync();
       mbar_arrive(smem_addr(&c->o_ready[g & 1]));
+      if (row == 0) MLA_TRACE_AT(15, g);
       if (i == nt - 1) {
         l_fin = lv;
         m_fin = mv;
@@ -571,6 +603,12 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
 }
 
 }  // namespace
+
+#ifdef MLA_TRACE
+extern "C" cudaError_t mla_trace_set_buffer(void* dev_ptr) {
+  return cudaMemcpyToSymbol(g_mla_trace, &dev_ptr, sizeof(dev_ptr));
+}
+#endif
 
 cudaError_t decode_prepare_device() {
   return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

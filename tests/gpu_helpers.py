@@ -67,6 +67,10 @@ def assert_parity(out, lse, ref_out, ref_lse, what=""):
                              f"at {idx}: got {out[idx]} ref {ref_out[idx]}")
     lerr = np.abs(lse[fin] - ref_lse[fin])
     assert lerr.size == 0 or lerr.max() <= LSE_ATOL, f"{what}: lse error {lerr.max()}"
+    margin = float((err / bound).max()) if err.size else 0.0
+    print(f"[parity] {what}: max|out-ref|={err.max() if err.size else 0:.3g} "
+          f"(max fraction of tolerance {margin:.3f}), max|lse-ref|="
+          f"{lerr.max() if lerr.size else 0:.3g}")
     return float(err.max()), float(lerr.max()) if lerr.size else 0.0
 
 
