@@ -483,7 +483,7 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
                                 static_cast<cuuint64_t>(num_blocks) * p->block_size};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kD) * 2};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kPanelCols),
-                               static_cast<cuuint32_t>(std::min(p->block_size, 32))};
+                               static_cast<cuuint32_t>(mla::kRowsPerBox)};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache),
                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -517,7 +517,6 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   dp.H = p->H;
   dp.block_size = p->block_size;
   dp.max_blocks = p->max_blocks;
-  dp.rows_per_box = std::min(p->block_size, 32);
   dp.num_blocks = num_blocks;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
 

@@ -13,15 +13,16 @@
 // Design (GB300-first; the pages' kernels are prior art, not the blueprint):
 // one 2-CTA cluster per work list, with split roles, because the fp32 output
 // accumulator of 128 heads x 512 columns fills a whole SM's tensor memory:
-//  * score CTA (cluster rank 0): streams 96-token KV tiles (all 576 columns)
-//    into two 108 KB shared-memory stages with TMA (one 32-row box per page
-//    slice and 64-column panel, block ids resolved from the block table),
-//    keeps Q [128 heads x 576] in tensor memory, issues S = Q.K^T with
-//    tcgen05 (M = 128 heads, N = 96 tokens, A from tensor memory), runs the
-//    fp32 online softmax (one thread per head row, lazy rescaling), and sends
-//    P (bf16) plus per-row rescale factors to the output CTA with st.async.
+//  * score CTA (cluster rank 0): streams 80-token KV tiles (all 576 columns)
+//    into two 90 KB shared-memory stages with TMA (16-row boxes per 64-column
+//    panel, block ids resolved from the block table), keeps Q [128 heads x
+//    576] in tensor memory, issues S = Q.K^T with tcgen05 (M = 128 heads,
+//    N = 80 tokens, A from tensor memory), runs the fp32 online softmax (one
+//    thread per head row, lazy rescaling), stages P (bf16) with the per-row
+//    rescale record in shared memory and ships each tile to the output CTA
+//    with one bulk copy into its shared memory (distributed shared memory).
 //  * output CTA (rank 1): holds O [128 x 512] fp32 in tensor memory, streams
-//    V half-tiles (256 columns) into a 3-slot ring with its own TMA loads
+//    V half-tiles (256 columns) into a 4-slot ring with its own TMA loads
 //    (L2 hits: the score CTA just read the same lines), issues O += P.V with
 //    tcgen05 (N = 256), applies the rescale when the softmax max moved, and
 //    writes the normalised output.
@@ -43,43 +44,32 @@ struct Ctrl {
   uint64_t s_full[2];             // score: S tile in tensor memory
   uint64_t s_free[2];             // score: softmax copied S out
   uint64_t q_ready;               // score: Q of the next item in tensor memory
-  uint64_t p_empty[kNumPBufs];    // score: peer finished P.V on P buffer k
+  uint64_t p_empty[kNumPBufs];    // score: peer finished P.V on its P buffer k
   uint64_t v_full[kNumVSlots];    // output: V half landed
   uint64_t v_empty[kNumVSlots];   // output: P.V done reading the V half
-  uint64_t p_full[kNumPBufs];     // output: P tile and row record landed (st.async bytes)
+  uint64_t p_full[kNumPBufs];     // output: P tile and row record landed (copy bytes)
   uint64_t o_ready[2];            // output: O rescaled / drained for tile g (alternating)
   uint64_t o_done[2];             // output: P.V of tile g complete (alternating)
   uint32_t tmem_base;
-  uint32_t pad;
+  int32_t abort_flag;             // score softmax warps: leave the loop together
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTile, 0, 0);   // K-major A and B
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);    // V is MN-major
 constexpr float kRescaleThreshold = 8.0f;                        // log2 units
-constexpr int kRowBytesSent = kTile * 2 + kRecFloats * 4;        // 204 per head row
+constexpr uint32_t kFullMask = 0xffffffffu;
 
 MLA_DEVI int tiles_of(const WorkItem& it) {
   return it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
 }
 
-// Row of the 2-D cache view holding token t of request b, or the first row
-// past the pool (a TMA box there reads zeros) for tokens at or past t_end and
-// for out-of-range block ids (which also raise MLA_DEVERR_BAD_BLOCK).
-MLA_DEVI int cache_row(const DecodeParams& p, int b, int t, int t_end, uint32_t& err) {
-  const int oob = static_cast<int>(p.num_blocks * p.block_size);
-  if (t >= t_end) return oob;
-  const int page = t / p.block_size;
-  const int blk = __ldg(&p.block_table[static_cast<int64_t>(b) * p.max_blocks + page]);
-  if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
-    err |= 1u;  // MLA_DEVERR_BAD_BLOCK
-    return oob;
-  }
-  return blk * p.block_size + (t % p.block_size);
-}
-
 MLA_DEVI void report(const DecodeParams& p, uint32_t bits) {
   if (bits) atomicOr(p.err, bits);
+}
+
+MLA_DEVI void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
 
 // Optional timeline instrumentation (compiled only with -DMLA_TRACE): each
@@ -101,52 +91,94 @@ MLA_DEVI void trace(int ev, int g) {
 #define MLA_TRACE_AT(ev, g) ((void)0)
 #endif
 
+// Block-table window of one producer warp: lane j holds the block id of page
+// base + j of the current request, so one coalesced load serves 32 pages.
+struct PageWindow {
+  int base = -1;
+  int val = 0;
+};
+
+// Row of the 2-D cache view holding token t (all lanes call this together),
+// or the first row past the pool (a TMA box there reads zeros) for tokens at
+// or past the item's end and for out-of-range block ids (MLA_DEVERR_BAD_BLOCK).
+MLA_DEVI int cache_row(const DecodeParams& p, const WorkItem& w, int t, PageWindow& win,
+                       int lane, uint32_t& err) {
+  const int oob = static_cast<int>(p.num_blocks * p.block_size);
+  if (t >= w.t1) return oob;
+  const int page = t / p.block_size;
+  if (win.base < 0 || page < win.base || page >= win.base + 32) {
+    win.base = page;
+    const int n_pages = (w.t1 + p.block_size - 1) / p.block_size;
+    win.val = (page + lane < n_pages)
+                  ? __ldg(&p.block_table[static_cast<int64_t>(w.b) * p.max_blocks + page + lane])
+                  : -1;
+  }
+  const int blk = __shfl_sync(kFullMask, win.val, page - win.base);
+  if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
+    err |= 1u;  // MLA_DEVERR_BAD_BLOCK
+    return oob;
+  }
+  return blk * p.block_size + (t % p.block_size);
+}
+
+// Lane 0 waits on a barrier; the whole warp learns the outcome.
+MLA_DEVI bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
+  bool ok = true;
+  if (lane == 0) ok = mbar_wait(bar, parity);
+  return __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+}
+
 // ------------------------------------------------------------ score CTA roles
 
-// TMA producer: all 9 panels of each 96-token tile into stage g % 2.
-MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int it0, int it1) {
+// TMA producer warp: all 9 panels of each 80-token tile into stage g % 2.
+MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int lane, int it0,
+                             int it1) {
   uint32_t err = 0;
   const uint64_t policy = policy_evict_normal();
-  const int R = p.rows_per_box;
-  const int nsub = kTile / R;
   int g = 0;
   bool ok = true;
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
-    if (__ldg(&p.seq_lens[w.b]) != w.seq_len) err |= 2u;  // MLA_DEVERR_SEQLEN_MISMATCH
-    // Warm L2 with the Q rows of the next non-empty item.
-    for (int nx = it + 1; nx < it1; ++nx) {
-      const WorkItem wn = p.items[nx];
-      if (tiles_of(wn) == 0) continue;
-      const uint16_t* qn = p.q_nope + static_cast<int64_t>(wn.b) * p.H * kDc;
-      const uint16_t* qp = p.q_pe + static_cast<int64_t>(wn.b) * p.H * kDr;
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qn), "r"(p.H * kDc * 2) : "memory");
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qp), "r"(p.H * kDr * 2) : "memory");
-      break;
+    if (lane == 0) {
+      if (__ldg(&p.seq_lens[w.b]) != w.seq_len) err |= 2u;  // MLA_DEVERR_SEQLEN_MISMATCH
+      // Warm L2 with the Q rows of the next non-empty item.
+      for (int nx = it + 1; nx < it1; ++nx) {
+        const WorkItem wn = p.items[nx];
+        if (tiles_of(wn) == 0) continue;
+        const uint16_t* qn = p.q_nope + static_cast<int64_t>(wn.b) * p.H * kDc;
+        const uint16_t* qp = p.q_pe + static_cast<int64_t>(wn.b) * p.H * kDr;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qn), "r"(p.H * kDc * 2) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qp), "r"(p.H * kDr * 2) : "memory");
+        break;
+      }
     }
+    PageWindow win;
     const int nt = tiles_of(w);
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
-      if (g >= kNumStages && !mbar_wait(smem_addr(&c->kv_empty[s]), ((g >> 1) - 1) & 1)) {
+      if (g >= kNumStages && !warp_wait(smem_addr(&c->kv_empty[s]), ((g >> 1) - 1) & 1, lane)) {
         ok = false;
         break;
       }
       MLA_TRACE_AT(0, g);
       const uint32_t full = smem_addr(&c->kv_full[s]);
-      mbar_arrive_expect_tx(full, kStageBytes);
+      if (lane == 0) mbar_arrive_expect_tx(full, kStageBytes);
       const uint32_t stage = smem_addr(data + s * kStageBytes);
       const int tile_t0 = w.t0 + i * kTile;
-      for (int sb = 0; sb < nsub; ++sb) {
-        const int y = cache_row(p, w.b, tile_t0 + sb * R, w.t1, err);
-        const uint32_t dst = stage + sb * R * 128;
+#pragma unroll 1
+      for (int sb = 0; sb < kSubBlocks; ++sb) {
+        const int y = cache_row(p, w, tile_t0 + sb * kRowsPerBox, win, lane, err);
+        if (lane == 0) {
+          const uint32_t dst = stage + sb * kRowsPerBox * 128;
 #pragma unroll
-        for (int pc = 0; pc < kNumPanels; ++pc)
-          tma_load_2d(dst + pc * kPanelBytes, &p.tmap_kv, pc * kPanelCols, y, full, policy);
+          for (int pc = 0; pc < kNumPanels; ++pc)
+            tma_load_2d(dst + pc * kPanelBytes, &p.tmap_kv, pc * kPanelCols, y, full, policy);
+        }
       }
     }
   }
   if (!ok) err |= 4u;
-  report(p, err);
+  if (lane == 0) report(p, err);
 }
 
 // MMA issuer: S[g%2] = Q . K^T over the 576 columns (36 k-steps of 16).
@@ -215,17 +247,21 @@ MLA_DEVI void load_q(const DecodeParams& p, int b, int row, uint32_t trow) {
   tmem_wait_st();
 }
 
-// Softmax warps: one thread per head row (TMEM lane).
-MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint32_t tmem, int warp, int lane,
-                            int it0, int it1) {
+// Softmax warps: one thread per head row (TMEM lane). The 128 threads stage
+// each P tile in shared memory; one elected thread ships it to the peer.
+MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem,
+                            int warp, int lane, int it0, int it1) {
   const int row = (warp & 3) * 32 + lane;
   const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const bool active = row < p.H;
+  const bool elected = (warp == 2 && lane == 0);
   const float sl2 = p.scale_log2;
-  // Peer (output CTA) addresses of the P buffers and their barriers.
-  const uint32_t pbuf0 = map_to_rank(smem_addr(reinterpret_cast<uint8_t*>(c) + kCtrlBytes +
-                                               kNumVSlots * kVHalfBytes), 1);
-  const uint32_t pfull0 = map_to_rank(smem_addr(&c->p_full[0]), 1);
+  uint8_t* staging = data + kNumStages * kStageBytes;
+  // Peer (output CTA) P buffers and their barriers, at the same offsets.
+  const uint32_t peer_pbuf0 = map_to_rank(smem_addr(data + kNumVSlots * kVHalfBytes), 1);
+  const uint32_t peer_pfull0 = map_to_rank(smem_addr(&c->p_full[0]), 1);
+  // Byte offset of this row inside a P tile (core-matrix row); chunk q adds 128*q.
+  const uint32_t prow_off = (row >> 3) * kPGroupBytes + (row & 7) * 16;
 
   auto next_nonempty = [&](int from) {
     for (int nx = from; nx < it1; ++nx)
@@ -248,140 +284,174 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint32_t tmem, int w
     float m_used = -INFINITY, l = 0.0f;
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&c->s_full[s]), (g >> 1) & 1))) {
-        ok = false;
-        break;
-      }
+      // A failed wait is recorded in the shared flag; every softmax thread
+      // still reaches the named barrier below and leaves the loop there.
+      const bool got_s = __all_sync(kFullMask, mbar_wait(smem_addr(&c->s_full[s]), (g >> 1) & 1));
+      if (!got_s && lane == 0) c->abort_flag = 1;
       if (row == 0) MLA_TRACE_AT(4, g);
-      tc_after_sync();
-      uint32_t ra[32], rb[32], rc[32];
-      tmem_ld32(trow + kTmemS0 + s * kTile + 0, ra);
-      tmem_ld32(trow + kTmemS0 + s * kTile + 32, rb);
-      tmem_ld32(trow + kTmemS0 + s * kTile + 64, rc);
-      tmem_wait_ld();
-      tc_before_sync();
-      mbar_arrive(smem_addr(&c->s_free[s]));
-      if (i == nt - 1 && nxt < it1) {
-        // All S MMAs of this item are complete: Q's columns are free.
-        load_q(p, p.items[nxt].b, row, trow);
+      uint32_t pk[kTile / 2];
+      float alpha = 1.0f;
+      if (got_s) {
+        uint32_t ra[32], rb[32], rc[16];
+        tc_after_sync();
+        tmem_ld32(trow + kTmemS0 + s * kTile + 0, ra);
+        tmem_ld32(trow + kTmemS0 + s * kTile + 32, rb);
+        tmem_ld16(trow + kTmemS0 + s * kTile + 64, rc);
+        tmem_wait_ld();
         tc_before_sync();
-        mbar_arrive(smem_addr(&c->q_ready));
+        mbar_arrive(smem_addr(&c->s_free[s]));
+        if (i == nt - 1 && nxt < it1) {
+          // All S MMAs of this item are complete: Q's columns are free.
+          load_q(p, p.items[nxt].b, row, trow);
+          tc_before_sync();
+          mbar_arrive(smem_addr(&c->q_ready));
+        }
+        if (active) {
+          float x[kTile];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            x[j] = __uint_as_float(ra[j]);
+            x[32 + j] = __uint_as_float(rb[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x[64 + j] = __uint_as_float(rc[j]);
+          const int valid = min(kTile, w.t1 - (w.t0 + i * kTile));
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < kTile; j += 4) {
+            if (j + 0 >= valid) x[j + 0] = -INFINITY;
+            if (j + 1 >= valid) x[j + 1] = -INFINITY;
+            if (j + 2 >= valid) x[j + 2] = -INFINITY;
+            if (j + 3 >= valid) x[j + 3] = -INFINITY;
+            mx0 = fmaxf(mx0, x[j + 0]);
+            mx1 = fmaxf(mx1, x[j + 1]);
+            mx2 = fmaxf(mx2, x[j + 2]);
+            mx3 = fmaxf(mx3, x[j + 3]);
+          }
+          const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+          if (m_tile > m_used + kRescaleThreshold) {
+            alpha = fast_exp2(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
+            l *= alpha;
+            m_used = m_tile;
+          }
+          float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+          for (int j = 0; j < kTile; j += 4) {
+            const float e0 = fast_exp2(fmaf(x[j + 0], sl2, -m_used));
+            const float e1 = fast_exp2(fmaf(x[j + 1], sl2, -m_used));
+            const float e2 = fast_exp2(fmaf(x[j + 2], sl2, -m_used));
+            const float e3 = fast_exp2(fmaf(x[j + 3], sl2, -m_used));
+            l0 += e0;
+            l1 += e1;
+            l2 += e2;
+            l3 += e3;
+            pk[j / 2] = pack_bf16x2(e0, e1);
+            pk[j / 2 + 1] = pack_bf16x2(e2, e3);
+          }
+          l += (l0 + l1) + (l2 + l3);
+        }
       }
+      // Stage P(g) in buffer k once the copy that last read it (tile g-2) is done.
       const int k = g & 1;
-      if (g >= kNumPBufs &&
-          !__all_sync(0xffffffffu, mbar_wait_cluster(smem_addr(&c->p_empty[k]), ((g >> 1) - 1) & 1))) {
+      if (elected && g >= kNumPBufs) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      named_barrier_sync(1, 128);
+      if (c->abort_flag) {
         ok = false;
         break;
       }
+      uint8_t* st = staging + k * kPBufBytes;
+      if (active) {
+#pragma unroll
+        for (int q = 0; q < kPCoreK; ++q)
+          *reinterpret_cast<uint4*>(st + prow_off + q * 128) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        float* rec = reinterpret_cast<float*>(st + kPBytes);
+        rec[row] = alpha;
+        rec[kMaxHeads + row] = l;
+        rec[2 * kMaxHeads + row] = m_used;
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 128);
       if (row == 0) MLA_TRACE_AT(5, g);
-      if (!active) continue;
-      float x[kTile];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        x[j] = __uint_as_float(ra[j]);
-        x[32 + j] = __uint_as_float(rb[j]);
-        x[64 + j] = __uint_as_float(rc[j]);
+      if (elected) {
+        if (g >= kNumPBufs &&
+            !mbar_wait_cluster(smem_addr(&c->p_empty[k]), ((g >> 1) - 1) & 1)) {
+          c->abort_flag = 1;   // seen by all at the next named barrier
+        } else {
+          asm volatile(
+              "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+              :: "r"(peer_pbuf0 + k * kPBufBytes), "r"(smem_addr(st)), "r"(kPMsgBytes),
+                 "r"(peer_pfull0 + k * 8)
+              : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        MLA_TRACE_AT(6, g);
       }
-      const int valid = min(kTile, w.t1 - (w.t0 + i * kTile));
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < kTile; j += 4) {
-        if (j + 0 >= valid) x[j + 0] = -INFINITY;
-        if (j + 1 >= valid) x[j + 1] = -INFINITY;
-        if (j + 2 >= valid) x[j + 2] = -INFINITY;
-        if (j + 3 >= valid) x[j + 3] = -INFINITY;
-        mx0 = fmaxf(mx0, x[j + 0]);
-        mx1 = fmaxf(mx1, x[j + 1]);
-        mx2 = fmaxf(mx2, x[j + 2]);
-        mx3 = fmaxf(mx3, x[j + 3]);
-      }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      float alpha = 1.0f;
-      if (m_tile > m_used + kRescaleThreshold) {
-        alpha = fast_exp2(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
-        l *= alpha;
-        m_used = m_tile;
-      }
-      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-      uint32_t pk[kTile / 2];
-#pragma unroll
-      for (int j = 0; j < kTile; j += 4) {
-        const float e0 = fast_exp2(fmaf(x[j + 0], sl2, -m_used));
-        const float e1 = fast_exp2(fmaf(x[j + 1], sl2, -m_used));
-        const float e2 = fast_exp2(fmaf(x[j + 2], sl2, -m_used));
-        const float e3 = fast_exp2(fmaf(x[j + 3], sl2, -m_used));
-        l0 += e0;
-        l1 += e1;
-        l2 += e2;
-        l3 += e3;
-        pk[j / 2] = pack_bf16x2(e0, e1);
-        pk[j / 2 + 1] = pack_bf16x2(e2, e3);
-      }
-      l += (l0 + l1) + (l2 + l3);
-      const uint32_t pb = pbuf0 + k * kPBufBytes;
-      const uint32_t bar = pfull0 + k * 8;
-#pragma unroll
-      for (int q = 0; q < kTile / 8; ++q) {
-        const uint32_t addr = pb + (q >> 3) * kPPanelBytes + row * 128 + (((q & 7) ^ (row & 7)) << 4);
-        st_async_v4(addr, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3], bar);
-      }
-      st_async_b32(pb + kPBytes + row * 4, __float_as_uint(alpha), bar);
-      st_async_b32(pb + kPBytes + 512 + row * 4, __float_as_uint(l), bar);
-      st_async_b32(pb + kPBytes + 1024 + row * 4, __float_as_uint(m_used), bar);
-      if (row == 0) MLA_TRACE_AT(6, g);
     }
     cur = nxt;
   }
-  // Drain: the peer's last commits arrive on p_empty; consume them so no
-  // remote arrival is still in flight when this CTA exits.
-  for (int gg = (g > 2 ? g - 2 : 0); gg < g && ok; ++gg)
-    if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_addr(&c->p_empty[gg & 1]), (gg >> 1) & 1)))
-      ok = false;
-  if (!ok) report(p, 4u);
+  // Drain: every copy has landed, and the peer's last commits (arriving on
+  // p_empty) are consumed, so nothing remote is in flight when we exit.
+  if (elected) {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (ok && !c->abort_flag)
+      for (int gg = (g > 2 ? g - 2 : 0); gg < g; ++gg)
+        if (!mbar_wait_cluster(smem_addr(&c->p_empty[gg & 1]), (gg >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+    if (!ok || c->abort_flag) report(p, 4u);
+  }
 }
 
 // ----------------------------------------------------------- output CTA roles
 
-// TMA producer: V half-tiles (4 panels = 256 columns) into a 3-slot ring.
-MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int it0, int it1) {
+// TMA producer warp: V half-tiles (4 panels = 256 columns) into a 4-slot ring.
+MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int lane, int it0,
+                           int it1) {
   uint32_t err = 0;
   const uint64_t policy = policy_evict_first();   // last use of these lines
-  const int R = p.rows_per_box;
-  const int nsub = kTile / R;
   int h = 0;
   bool ok = true;
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
     const int nt = tiles_of(w);
+    PageWindow win;
     for (int i = 0; i < nt && ok; ++i) {
       const int tile_t0 = w.t0 + i * kTile;
-      int ys[kTile / 16];
-      for (int sb = 0; sb < nsub; ++sb) ys[sb] = cache_row(p, w.b, tile_t0 + sb * R, w.t1, err);
+      int ys[kSubBlocks];
+#pragma unroll
+      for (int sb = 0; sb < kSubBlocks; ++sb)
+        ys[sb] = cache_row(p, w, tile_t0 + sb * kRowsPerBox, win, lane, err);
       for (int half = 0; half < 2; ++half, ++h) {
         const int v = h % kNumVSlots;
-        if (h >= kNumVSlots && !mbar_wait(smem_addr(&c->v_empty[v]), ((h / kNumVSlots) - 1) & 1)) {
+        if (h >= kNumVSlots &&
+            !warp_wait(smem_addr(&c->v_empty[v]), ((h / kNumVSlots) - 1) & 1, lane)) {
           ok = false;
           break;
         }
         MLA_TRACE_AT(8 + half, h >> 1);
-        const uint32_t full = smem_addr(&c->v_full[v]);
-        mbar_arrive_expect_tx(full, kVHalfBytes);
-        const uint32_t slot = smem_addr(data + v * kVHalfBytes);
-        for (int sb = 0; sb < nsub; ++sb) {
-          const uint32_t dst = slot + sb * R * 128;
+        if (lane == 0) {
+          const uint32_t full = smem_addr(&c->v_full[v]);
+          mbar_arrive_expect_tx(full, kVHalfBytes);
+          const uint32_t slot = smem_addr(data + v * kVHalfBytes);
 #pragma unroll
-          for (int pc = 0; pc < kVHalfPanels; ++pc)
-            tma_load_2d(dst + pc * kPanelBytes, &p.tmap_kv, (half * kVHalfPanels + pc) * kPanelCols,
-                        ys[sb], full, policy);
+          for (int sb = 0; sb < kSubBlocks; ++sb) {
+            const uint32_t dst = slot + sb * kRowsPerBox * 128;
+#pragma unroll
+            for (int pc = 0; pc < kVHalfPanels; ++pc)
+              tma_load_2d(dst + pc * kPanelBytes, &p.tmap_kv,
+                          (half * kVHalfPanels + pc) * kPanelCols, ys[sb], full, policy);
+          }
         }
       }
     }
   }
   if (!ok) err |= 4u;
-  report(p, err);
+  if (lane == 0) report(p, err);
 }
 
-// MMA issuer: O[:, 256*half ...] += P . V_half (6 k-steps of 16 tokens each).
+// MMA issuer: O[:, 256*half ...] += P . V_half (5 k-steps of 16 tokens each).
 MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
                       int it1) {
   int g = 0, h = 0;
@@ -395,7 +465,13 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
       if (!mbar_wait(smem_addr(&c->o_ready[g & 1]), (g >> 1) & 1)) { ok = false; break; }
       MLA_TRACE_AT(10, g);
       tc_after_sync();
-      const uint64_t a0 = smem_desc(smem_addr(pbufs + k * kPBufBytes), 16, 1024);
+      // P: no-swizzle K-major; K-adjacent core matrices 128 B apart, row
+      // groups kPGroupBytes apart (layout type 0 in bits 61-63).
+      const uint32_t pa = smem_addr(pbufs + k * kPBufBytes);
+      uint64_t a0 = static_cast<uint64_t>((pa >> 4) & 0x3FFFu);
+      a0 |= static_cast<uint64_t>(128 >> 4) << 16;
+      a0 |= static_cast<uint64_t>(kPGroupBytes >> 4) << 32;
+      a0 |= static_cast<uint64_t>(1) << 46;
       for (int half = 0; half < 2; ++half, ++h) {
         const int v = h % kNumVSlots;
         if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
@@ -404,7 +480,7 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
         const uint64_t b0 = smem_desc(smem_addr(data + v * kVHalfBytes), kPanelBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t ad = a0 + static_cast<uint64_t>(((kk >> 2) * kPPanelBytes + (kk & 3) * 32) >> 4);
+          const uint64_t ad = a0 + static_cast<uint64_t>((kk * 256) >> 4);
           const uint64_t bd = b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4);
           mma_ss(tmem + half * 256, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
@@ -412,8 +488,8 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
       }
       if (!ok) break;
       tc_commit(smem_addr(&c->o_done[g & 1]));
-      MLA_TRACE_AT(13, g);
       tc_commit_multicast(smem_addr(&c->p_empty[k]), static_cast<uint16_t>(0x1));
+      MLA_TRACE_AT(13, g);
     }
   }
   if (!ok) report(p, 4u);
@@ -444,19 +520,18 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
     float l_fin = 1.0f, m_fin = 0.0f;
     for (int i = 0; i < nt; ++i, ++g) {
       const int k = g & 1;
-      if (elected) mbar_arrive_expect_tx(smem_addr(&c->p_full[k]), p.H * kRowBytesSent);
-      if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_addr(&c->p_full[k]), (g >> 1) & 1))) {
+      if (elected) mbar_arrive_expect_tx(smem_addr(&c->p_full[k]), kPMsgBytes);
+      if (!__all_sync(kFullMask, mbar_wait_cluster(smem_addr(&c->p_full[k]), (g >> 1) & 1))) {
         ok = false;
         break;
       }
       if (row == 0) MLA_TRACE_AT(14, g);
       const float* rec = reinterpret_cast<const float*>(pbufs + k * kPBufBytes + kPBytes);
       const float alpha = active ? rec[row] : 1.0f;
-      const float lv = rec[128 + row];
-      const float mv = rec[256 + row];
-      fence_proxy_async_smem();
-      if (i > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
+      const float lv = rec[kMaxHeads + row];
+      const float mv = rec[2 * kMaxHeads + row];
+      if (i > 0 && __any_sync(kFullMask, alpha != 1.0f)) {
+        if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
           ok = false;
           break;
         }
@@ -482,7 +557,7 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
     }
     if (!ok) break;
     // Epilogue: O / l -> out (bf16) or the split partial (fp32).
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
+    if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
       ok = false;
       break;
     }
@@ -557,12 +632,15 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->v_full[v]), 1);
       mbar_init(smem_addr(&c->v_empty[v]), 1);
     }
+    c->abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) prefetch_tmap(&p.tmap_kv);
-  if (rank == 1) {
-    // Zero both P buffers once: rows >= H stay zero (padded heads).
-    uint4* pz = reinterpret_cast<uint4*>(data + kNumVSlots * kVHalfBytes);
+  {
+    // Zero the P staging buffers (score CTA) and P buffers (output CTA) once:
+    // rows >= H are never written and stay zero (padded heads).
+    uint4* pz = reinterpret_cast<uint4*>(
+        data + (rank == 0 ? kNumStages * kStageBytes : kNumVSlots * kVHalfBytes));
     for (int e = threadIdx.x; e < kNumPBufs * kPBufBytes / 16; e += kThreads)
       pz[e] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
@@ -578,15 +656,15 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
 
   if (rank == 0) {
     if (warp == 0) {
-      if (lane == 0) score_producer(p, c, data, it0, it1);
+      score_producer(p, c, data, lane, it0, it1);
     } else if (warp == 1) {
       if (lane == 0) score_mma(p, c, data, tmem, it0, it1);
     } else {
-      score_softmax(p, c, tmem, warp, lane, it0, it1);
+      score_softmax(p, c, data, tmem, warp, lane, it0, it1);
     }
   } else {
     if (warp == 0) {
-      if (lane == 0) out_producer(p, c, data, it0, it1);
+      out_producer(p, c, data, lane, it0, it1);
     } else if (warp == 1) {
       if (lane == 0) out_mma(p, c, data, tmem, it0, it1);
     } else {

@@ -13,20 +13,27 @@ constexpr int kDc = 512;                 // latent c_kv columns (= V width)
 constexpr int kDr = 64;                  // rope k_pe columns
 constexpr int kD = kDc + kDr;            // 576 bf16 per cached token row
 constexpr int kMaxHeads = 128;           // MMA M; fewer heads are padded inside the kernel
-constexpr int kTile = 96;                // tokens per KV tile (MMA N of the score product)
+constexpr int kTile = 80;                // tokens per KV tile (MMA N of the score product)
+constexpr int kRowsPerBox = 16;          // TMA box height: 16 tokens, always inside one page
+constexpr int kSubBlocks = kTile / kRowsPerBox;        // 5 boxes per panel per tile
 constexpr int kPanelCols = 64;           // bf16 columns of one 128-byte swizzle panel
 constexpr int kNumPanels = kD / kPanelCols;            // 9 panels per row
-constexpr int kPanelBytes = kTile * 128;               // one panel of one tile: 12 KB
-constexpr int kStageBytes = kNumPanels * kPanelBytes;  // full 576-wide tile: 108 KB
+constexpr int kPanelBytes = kTile * 128;               // one panel of one tile: 10 KB
+constexpr int kStageBytes = kNumPanels * kPanelBytes;  // full 576-wide tile: 90 KB
 constexpr int kVHalfPanels = 4;                        // V half = 256 columns
-constexpr int kVHalfBytes = kVHalfPanels * kPanelBytes;  // 48 KB
+constexpr int kVHalfBytes = kVHalfPanels * kPanelBytes;  // 40 KB
 constexpr int kNumStages = 2;            // score CTA: KV tiles in flight
-constexpr int kNumVSlots = 3;            // output CTA: V half-tiles in flight
-constexpr int kNumPBufs = 2;             // output CTA: P tiles in flight
-constexpr int kPPanelBytes = kMaxHeads * 128;          // 128 rows x 64 tokens (bf16)
-constexpr int kPBytes = 2 * kPPanelBytes;              // 96 tokens need two K panels
+constexpr int kNumVSlots = 4;            // output CTA: V half-tiles in flight
+constexpr int kNumPBufs = 2;             // P tiles in flight (staging and peer buffers)
+// P [128 rows x 80 tokens] bf16 in the no-swizzle K-major layout of 8-row x
+// 16-byte core matrices: [row/8][token/8][row%8][16 B]; K-adjacent cores are
+// 128 B apart, row groups 1280 B apart.
+constexpr int kPCoreK = kTile / 8;                     // 10 core matrices along K
+constexpr int kPGroupBytes = kPCoreK * 128;            // 1280
+constexpr int kPBytes = kMaxHeads / 8 * kPGroupBytes;  // 20 KB
 constexpr int kRecFloats = 3;                          // per row: alpha, l, m
-constexpr int kPBufBytes = kPBytes + 2048;             // P plus the per-row record
+constexpr int kPMsgBytes = kPBytes + kRecFloats * kMaxHeads * 4;  // 22016 B per tile
+constexpr int kPBufBytes = 22528;                      // message rounded to 512 B
 constexpr int kThreads = 192;            // 6 warps per CTA
 constexpr int kTmemCols = 512;
 // Score CTA TMEM columns: Q (576 bf16 packed in pairs) then two S buffers.
@@ -34,10 +41,11 @@ constexpr int kTmemQ = 0;
 constexpr int kTmemS0 = kD / 2;          // 288
 // Shared-memory data region (after the 1 KB control block).
 constexpr int kCtrlBytes = 1024;
-constexpr int kScoreDataBytes = kNumStages * kStageBytes;                         // 216 KB
-constexpr int kOutDataBytes = kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes;  // 212 KB
+constexpr int kScoreDataBytes = kNumStages * kStageBytes + kNumPBufs * kPBufBytes;  // 225 KB
+constexpr int kOutDataBytes = kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes;    // 204 KB
 constexpr int kDataBytes = kScoreDataBytes > kOutDataBytes ? kScoreDataBytes : kOutDataBytes;
 constexpr int kSmemBytes = kCtrlBytes + kDataBytes + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // One unit of work: tokens [t0, t1) of request b. slot >= 0 means the result
 // is a split partial written to the workspace; -1 writes out/lse directly.
@@ -75,7 +83,6 @@ struct DecodeParams {
   int H;
   int block_size;
   int max_blocks;
-  int rows_per_box;               // min(block_size, 32)
   int64_t num_blocks;
   float scale_log2;               // sm_scale * log2(e)
 };
