@@ -45,8 +45,9 @@ struct mla_plan_s {
   size_t h_cap = 0;
   cudaEvent_t upload_done = nullptr;
   size_t off_items = 0, off_offsets = 0, off_combine = 0, sched_bytes = 0;
-  // Cached TMA descriptor of the last cache seen.
-  CUtensorMap tmap;
+  // Cached TMA descriptors (16- and 32-row boxes) of the last cache seen.
+  CUtensorMap tmap16;
+  CUtensorMap tmap32;
   const void* tmap_ptr = nullptr;
   int64_t tmap_blocks = -1;
 };
@@ -482,16 +483,20 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kD),
                                 static_cast<cuuint64_t>(num_blocks) * p->block_size};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kD) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kPanelCols),
-                               static_cast<cuuint32_t>(mla::kRowsPerBox)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache),
-                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-      p->tmap_ptr = nullptr;
-      return MLA_ERR_INVALID_ARG;
+    CUtensorMap* maps[2] = {&p->tmap16, &p->tmap32};
+    const int heights[2] = {mla::kRowsSmallBox, std::min(p->block_size, mla::kRowsLargeBox)};
+    for (int i = 0; i < 2; ++i) {
+      const cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kPanelCols),
+                                 static_cast<cuuint32_t>(heights[i])};
+      CUresult r = enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache),
+                       dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) {
+        p->tmap_ptr = nullptr;
+        return MLA_ERR_INVALID_ARG;
+      }
     }
     p->tmap_ptr = kv_cache;
     p->tmap_blocks = num_blocks;
@@ -499,7 +504,8 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
 
   mla::DecodeParams dp;
   std::memset(&dp, 0, sizeof(dp));
-  dp.tmap_kv = p->tmap;
+  dp.tmap_kv16 = p->tmap16;
+  dp.tmap_kv32 = p->tmap32;
   dp.q_nope = static_cast<const uint16_t*>(q_nope);
   dp.q_pe = static_cast<const uint16_t*>(q_pe);
   dp.block_table = block_table;

@@ -39,8 +39,8 @@ namespace {
 // Control block: identical offsets in both CTAs of the pair, so a barrier can
 // be addressed in the peer by offset (mapa, multicast commit).
 struct Ctrl {
-  uint64_t kv_full[kNumStages];   // score: stage landed (TMA bytes)
-  uint64_t kv_empty[kNumStages];  // score: S MMAs done reading the stage
+  uint64_t kv_full[kNumStages * kNumPanels];   // score: panel slot landed (TMA bytes)
+  uint64_t kv_empty[kNumStages * kNumPanels];  // score: S MMAs done reading the panel slot
   uint64_t s_full[2];             // score: S tile in tensor memory
   uint64_t s_free[2];             // score: softmax copied S out
   uint64_t q_ready;               // score: Q of the next item in tensor memory
@@ -77,7 +77,7 @@ MLA_DEVI void named_barrier_sync(int id, int threads) {
 // fixed points of every tile. Records time only; skips no work.
 #ifdef MLA_TRACE
 __device__ uint64_t* g_mla_trace = nullptr;   // [pairs][2 ranks][kTraceEvents][kTraceTiles]
-constexpr int kTracePairs = 4, kTraceEvents = 16, kTraceTiles = 256;
+constexpr int kTracePairs = 4, kTraceEvents = 24, kTraceTiles = 256;
 MLA_DEVI void trace(int ev, int g) {
   uint64_t* t = g_mla_trace;
   const int pair = static_cast<int>(cluster_id_x());
@@ -121,6 +121,42 @@ MLA_DEVI int cache_row(const DecodeParams& p, const WorkItem& w, int t, PageWind
   return blk * p.block_size + (t % p.block_size);
 }
 
+// The TMA boxes that cover one 80-token tile of one 64-column panel: pieces of
+// 32 rows where a 32-row page-aligned run fits (block size >= 32), else 16.
+// A tile starts at a multiple of 80 tokens, so it starts at offset 0 or 16
+// modulo 32 and every piece stays inside one page.
+struct TilePieces {
+  int n;
+  int r0[kMaxPieces];     // first row of the piece inside the tile
+  int large[kMaxPieces];  // 1: 32-row box, 0: 16-row box
+  int y[kMaxPieces];      // cache row of the piece (or the zero-fill row past the pool)
+};
+
+MLA_DEVI void tile_pieces(const DecodeParams& p, const WorkItem& w, int tile_t0, PageWindow& win,
+                          int lane, uint32_t& err, TilePieces& tp) {
+  if (p.block_size >= kRowsLargeBox) {
+    if ((tile_t0 & 31) == 0) {
+      tp.n = 3;
+      tp.r0[0] = 0;  tp.large[0] = 1;
+      tp.r0[1] = 32; tp.large[1] = 1;
+      tp.r0[2] = 64; tp.large[2] = 0;
+    } else {
+      tp.n = 3;
+      tp.r0[0] = 0;  tp.large[0] = 0;
+      tp.r0[1] = 16; tp.large[1] = 1;
+      tp.r0[2] = 48; tp.large[2] = 1;
+    }
+  } else {
+    tp.n = kMaxPieces;
+#pragma unroll
+    for (int j = 0; j < kMaxPieces; ++j) {
+      tp.r0[j] = j * kRowsSmallBox;
+      tp.large[j] = 0;
+    }
+  }
+  for (int j = 0; j < tp.n; ++j) tp.y[j] = cache_row(p, w, tile_t0 + tp.r0[j], win, lane, err);
+}
+
 // Lane 0 waits on a barrier; the whole warp learns the outcome.
 MLA_DEVI bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
   bool ok = true;
@@ -154,25 +190,26 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
     }
     PageWindow win;
     const int nt = tiles_of(w);
-    for (int i = 0; i < nt; ++i, ++g) {
+    for (int i = 0; i < nt && ok; ++i, ++g) {
       const int s = g & 1;
-      if (g >= kNumStages && !warp_wait(smem_addr(&c->kv_empty[s]), ((g >> 1) - 1) & 1, lane)) {
-        ok = false;
-        break;
-      }
+      TilePieces tp;
+      tile_pieces(p, w, w.t0 + i * kTile, win, lane, err, tp);
       MLA_TRACE_AT(0, g);
-      const uint32_t full = smem_addr(&c->kv_full[s]);
-      if (lane == 0) mbar_arrive_expect_tx(full, kStageBytes);
       const uint32_t stage = smem_addr(data + s * kStageBytes);
-      const int tile_t0 = w.t0 + i * kTile;
-#pragma unroll 1
-      for (int sb = 0; sb < kSubBlocks; ++sb) {
-        const int y = cache_row(p, w, tile_t0 + sb * kRowsPerBox, win, lane, err);
+      for (int pc = 0; pc < kNumPanels; ++pc) {
+        const int slot = s * kNumPanels + pc;
+        if (g >= kNumStages &&
+            !warp_wait(smem_addr(&c->kv_empty[slot]), ((g >> 1) - 1) & 1, lane)) {
+          ok = false;
+          break;
+        }
         if (lane == 0) {
-          const uint32_t dst = stage + sb * kRowsPerBox * 128;
-#pragma unroll
-          for (int pc = 0; pc < kNumPanels; ++pc)
-            tma_load_2d(dst + pc * kPanelBytes, &p.tmap_kv, pc * kPanelCols, y, full, policy);
+          const uint32_t full = smem_addr(&c->kv_full[slot]);
+          mbar_arrive_expect_tx(full, kPanelBytes);
+          for (int j = 0; j < tp.n; ++j)
+            tma_load_2d(stage + pc * kPanelBytes + tp.r0[j] * 128,
+                        tp.large[j] ? &p.tmap_kv32 : &p.tmap_kv16, pc * kPanelCols, tp.y[j], full,
+                        policy);
         }
       }
     }
@@ -194,21 +231,27 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
     ++n_items;
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
-      if (!mbar_wait(smem_addr(&c->kv_full[s]), (g >> 1) & 1)) { ok = false; break; }
-      MLA_TRACE_AT(1, g);
       if (g >= 2 && !mbar_wait(smem_addr(&c->s_free[s]), ((g >> 1) - 1) & 1)) { ok = false; break; }
       MLA_TRACE_AT(2, g);
-      tc_after_sync();
       const uint32_t d = tmem + kTmemS0 + s * kTile;
       const uint64_t b0 = smem_desc(smem_addr(data + s * kStageBytes), 16, 1024);
 #pragma unroll
-      for (int k = 0; k < kD / 16; ++k) {
-        // panel k/4, 32 bytes per k-step inside the 128-byte swizzle row
-        const uint64_t bd = b0 + static_cast<uint64_t>(((k >> 2) * kPanelBytes + (k & 3) * 32) >> 4);
-        mma_ts(d, tmem + kTmemQ + k * 8, bd, kIdescS, k > 0 ? 1u : 0u);
+      for (int pc = 0; pc < kNumPanels; ++pc) {
+        const int slot = s * kNumPanels + pc;
+        if (!mbar_wait(smem_addr(&c->kv_full[slot]), (g >> 1) & 1)) { ok = false; break; }
+        if (pc == 0) MLA_TRACE_AT(1, g);
+        tc_after_sync();
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) {
+          // panel pc, 32 bytes per k-step inside the 128-byte swizzle row
+          const int k = pc * 4 + kq;
+          const uint64_t bd = b0 + static_cast<uint64_t>((pc * kPanelBytes + kq * 32) >> 4);
+          mma_ts(d, tmem + kTmemQ + k * 8, bd, kIdescS, k > 0 ? 1u : 0u);
+        }
+        tc_commit(smem_addr(&c->kv_empty[slot]));
       }
+      if (!ok) break;
       tc_commit(smem_addr(&c->s_full[s]));
-      tc_commit(smem_addr(&c->kv_empty[s]));
       MLA_TRACE_AT(3, g);
     }
   }
@@ -300,6 +343,7 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
         tmem_wait_ld();
         tc_before_sync();
         mbar_arrive(smem_addr(&c->s_free[s]));
+        if (row == 0) MLA_TRACE_AT(16, g);
         if (i == nt - 1 && nxt < it1) {
           // All S MMAs of this item are complete: Q's columns are free.
           load_q(p, p.items[nxt].b, row, trow);
@@ -353,8 +397,11 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       }
       // Stage P(g) in buffer k once the copy that last read it (tile g-2) is done.
       const int k = g & 1;
+      if (row == 0) MLA_TRACE_AT(17, g);
       if (elected && g >= kNumPBufs) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      if (elected) MLA_TRACE_AT(18, g);
       named_barrier_sync(1, 128);
+      if (row == 0) MLA_TRACE_AT(19, g);
       if (c->abort_flag) {
         ok = false;
         break;
@@ -370,7 +417,9 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
         rec[kMaxHeads + row] = l;
         rec[2 * kMaxHeads + row] = m_used;
       }
+      if (row == 0) MLA_TRACE_AT(20, g);
       fence_proxy_async_smem();
+      if (row == 0) MLA_TRACE_AT(21, g);
       named_barrier_sync(1, 128);
       if (row == 0) MLA_TRACE_AT(5, g);
       if (elected) {
@@ -418,11 +467,8 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
     const int nt = tiles_of(w);
     PageWindow win;
     for (int i = 0; i < nt && ok; ++i) {
-      const int tile_t0 = w.t0 + i * kTile;
-      int ys[kSubBlocks];
-#pragma unroll
-      for (int sb = 0; sb < kSubBlocks; ++sb)
-        ys[sb] = cache_row(p, w, tile_t0 + sb * kRowsPerBox, win, lane, err);
+      TilePieces tp;
+      tile_pieces(p, w, w.t0 + i * kTile, win, lane, err, tp);
       for (int half = 0; half < 2; ++half, ++h) {
         const int v = h % kNumVSlots;
         if (h >= kNumVSlots &&
@@ -435,13 +481,13 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
           const uint32_t full = smem_addr(&c->v_full[v]);
           mbar_arrive_expect_tx(full, kVHalfBytes);
           const uint32_t slot = smem_addr(data + v * kVHalfBytes);
-#pragma unroll
-          for (int sb = 0; sb < kSubBlocks; ++sb) {
-            const uint32_t dst = slot + sb * kRowsPerBox * 128;
+          for (int j = 0; j < tp.n; ++j) {
+            const uint32_t dst = slot + tp.r0[j] * 128;
+            const CUtensorMap* map = tp.large[j] ? &p.tmap_kv32 : &p.tmap_kv16;
 #pragma unroll
             for (int pc = 0; pc < kVHalfPanels; ++pc)
-              tma_load_2d(dst + pc * kPanelBytes, &p.tmap_kv,
-                          (half * kVHalfPanels + pc) * kPanelCols, ys[sb], full, policy);
+              tma_load_2d(dst + pc * kPanelBytes, map, (half * kVHalfPanels + pc) * kPanelCols,
+                          tp.y[j], full, policy);
           }
         }
       }
@@ -613,7 +659,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNumStages; ++s) {
+    for (int s = 0; s < kNumStages * kNumPanels; ++s) {
       mbar_init(smem_addr(&c->kv_full[s]), 1);
       mbar_init(smem_addr(&c->kv_empty[s]), 1);
     }
@@ -635,7 +681,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
     c->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&p.tmap_kv);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tmap_kv16);
+    prefetch_tmap(&p.tmap_kv32);
+  }
   {
     // Zero the P staging buffers (score CTA) and P buffers (output CTA) once:
     // rows >= H are never written and stay zero (padded heads).

@@ -14,8 +14,9 @@ constexpr int kDr = 64;                  // rope k_pe columns
 constexpr int kD = kDc + kDr;            // 576 bf16 per cached token row
 constexpr int kMaxHeads = 128;           // MMA M; fewer heads are padded inside the kernel
 constexpr int kTile = 80;                // tokens per KV tile (MMA N of the score product)
-constexpr int kRowsPerBox = 16;          // TMA box height: 16 tokens, always inside one page
-constexpr int kSubBlocks = kTile / kRowsPerBox;        // 5 boxes per panel per tile
+constexpr int kRowsSmallBox = 16;        // TMA box heights: 16 rows (any block size) and
+constexpr int kRowsLargeBox = 32;        // 32 rows (block sizes >= 32), never crossing a page
+constexpr int kMaxPieces = kTile / kRowsSmallBox;      // at most 5 boxes per panel per tile
 constexpr int kPanelCols = 64;           // bf16 columns of one 128-byte swizzle panel
 constexpr int kNumPanels = kD / kPanelCols;            // 9 panels per row
 constexpr int kPanelBytes = kTile * 128;               // one panel of one tile: 10 KB
@@ -68,7 +69,8 @@ struct CombineItem {
 };
 
 struct DecodeParams {
-  CUtensorMap tmap_kv;            // 2-D view [num_blocks*block_size rows][576] bf16
+  CUtensorMap tmap_kv16;          // 2-D view [num_blocks*block_size rows][576] bf16, 64x16 boxes
+  CUtensorMap tmap_kv32;          // the same view with 64x32 boxes (block_size >= 32)
   const uint16_t* q_nope;         // [B, H, 512]
   const uint16_t* q_pe;           // [B, H, 64]
   const int32_t* block_table;     // [B, max_blocks]
