@@ -506,6 +506,7 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   std::memset(&dp, 0, sizeof(dp));
   dp.tmap_kv16 = p->tmap16;
   dp.tmap_kv32 = p->tmap32;
+  dp.kv_cache = kv_cache;
   dp.q_nope = static_cast<const uint16_t*>(q_nope);
   dp.q_pe = static_cast<const uint16_t*>(q_pe);
   dp.block_table = block_table;

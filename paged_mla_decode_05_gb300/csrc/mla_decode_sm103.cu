@@ -52,6 +52,7 @@ struct Ctrl {
   uint64_t o_done[2];             // output: P.V of tile g complete (alternating)
   uint32_t tmem_base;
   int32_t abort_flag;             // score softmax warps: leave the loop together
+  int32_t p_seen;                 // output: P tiles received so far (paces the prefetcher)
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
@@ -59,6 +60,7 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTile, 0, 0);   // K-major A an
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);    // V is MN-major
 constexpr float kRescaleThreshold = 8.0f;                        // log2 units
 constexpr uint32_t kFullMask = 0xffffffffu;
+constexpr int kPrefetchTiles = 4;   // output prefetcher: distance ahead of received P (tiles)
 
 MLA_DEVI int tiles_of(const WorkItem& it) {
   return it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
@@ -77,14 +79,17 @@ MLA_DEVI void named_barrier_sync(int id, int threads) {
 // fixed points of every tile. Records time only; skips no work.
 #ifdef MLA_TRACE
 __device__ uint64_t* g_mla_trace = nullptr;   // [pairs][2 ranks][kTraceEvents][kTraceTiles]
-constexpr int kTracePairs = 4, kTraceEvents = 24, kTraceTiles = 256;
+constexpr int kTracePairs = 4, kTraceEvents = 64, kTraceTiles = 256;
+// Events 0..31 record %globaltimer; slot 32 + ev records clock64 of the same event.
 MLA_DEVI void trace(int ev, int g) {
   uint64_t* t = g_mla_trace;
   const int pair = static_cast<int>(cluster_id_x());
   if (t == nullptr || pair >= kTracePairs || g >= kTraceTiles) return;
   uint64_t now;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
-  t[((pair * 2 + cluster_rank()) * kTraceEvents + ev) * kTraceTiles + g] = now;
+  const int base = (pair * 2 + static_cast<int>(cluster_rank())) * kTraceEvents;
+  t[(base + ev) * kTraceTiles + g] = now;
+  t[(base + 32 + ev) * kTraceTiles + g] = static_cast<uint64_t>(clock64());
 }
 #define MLA_TRACE_AT(ev, g) trace(ev, g)
 #else
@@ -196,6 +201,7 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
       tile_pieces(p, w, w.t0 + i * kTile, win, lane, err, tp);
       MLA_TRACE_AT(0, g);
       const uint32_t stage = smem_addr(data + s * kStageBytes);
+#pragma unroll 1
       for (int pc = 0; pc < kNumPanels; ++pc) {
         const int slot = s * kNumPanels + pc;
         if (g >= kNumStages &&
@@ -235,7 +241,7 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
       MLA_TRACE_AT(2, g);
       const uint32_t d = tmem + kTmemS0 + s * kTile;
       const uint64_t b0 = smem_desc(smem_addr(data + s * kStageBytes), 16, 1024);
-#pragma unroll
+#pragma unroll 1
       for (int pc = 0; pc < kNumPanels; ++pc) {
         const int slot = s * kNumPanels + pc;
         if (!mbar_wait(smem_addr(&c->kv_full[slot]), (g >> 1) & 1)) { ok = false; break; }
@@ -260,7 +266,7 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
 
 // Load Q rows of request b into tensor memory columns [0, 288): lane = head,
 // two bf16 per column. Rows at or past H are zero (in-kernel head padding).
-MLA_DEVI void load_q(const DecodeParams& p, int b, int row, uint32_t trow) {
+__device__ __noinline__ void load_q(const DecodeParams& p, int b, int row, uint32_t trow) {
   const bool valid = row < p.H;
   const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<int64_t>(b) * p.H + row) * kDc);
   const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + (static_cast<int64_t>(b) * p.H + row) * kDr);
@@ -290,8 +296,11 @@ MLA_DEVI void load_q(const DecodeParams& p, int b, int row, uint32_t trow) {
   tmem_wait_st();
 }
 
-// Softmax warps: one thread per head row (TMEM lane). The 128 threads stage
-// each P tile in shared memory; one elected thread ships it to the peer.
+// Softmax warps: one thread per head row (TMEM lane). Two compact passes over
+// the S tile in 16-column chunks (row max, then exp/sum/pack) keep the code
+// small: several warp roles share each sub-partition's instruction cache.
+// P goes straight into a staging buffer; one elected thread ships the tile to
+// the peer with a bulk copy.
 MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem,
                             int warp, int lane, int it0, int it1) {
   const int row = (warp & 3) * 32 + lane;
@@ -303,18 +312,13 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
   // Peer (output CTA) P buffers and their barriers, at the same offsets.
   const uint32_t peer_pbuf0 = map_to_rank(smem_addr(data + kNumVSlots * kVHalfBytes), 1);
   const uint32_t peer_pfull0 = map_to_rank(smem_addr(&c->p_full[0]), 1);
-  // Byte offset of this row inside a P tile (core-matrix row); chunk q adds 128*q.
+  // Byte offset of this row inside a P tile (core-matrix row); core q adds 128*q.
   const uint32_t prow_off = (row >> 3) * kPGroupBytes + (row & 7) * 16;
-
-  auto next_nonempty = [&](int from) {
-    for (int nx = from; nx < it1; ++nx)
-      if (tiles_of(p.items[nx]) > 0) return nx;
-    return it1;
-  };
 
   int g = 0;
   bool ok = true;
-  int cur = next_nonempty(it0);
+  int cur = it0;
+  while (cur < it1 && tiles_of(p.items[cur]) == 0) ++cur;
   if (cur < it1) {
     load_q(p, p.items[cur].b, row, trow);
     tc_before_sync();
@@ -323,103 +327,87 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
   while (cur < it1 && ok) {
     const WorkItem w = p.items[cur];
     const int nt = tiles_of(w);
-    const int nxt = next_nonempty(cur + 1);
+    int nxt = cur + 1;
+    while (nxt < it1 && tiles_of(p.items[nxt]) == 0) ++nxt;
     float m_used = -INFINITY, l = 0.0f;
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
+      const int k = g & 1;
+      const uint32_t scol = trow + kTmemS0 + s * kTile;
+      const int valid = min(kTile, w.t1 - (w.t0 + i * kTile));
       // A failed wait is recorded in the shared flag; every softmax thread
       // still reaches the named barrier below and leaves the loop there.
       const bool got_s = __all_sync(kFullMask, mbar_wait(smem_addr(&c->s_full[s]), (g >> 1) & 1));
       if (!got_s && lane == 0) c->abort_flag = 1;
       if (row == 0) MLA_TRACE_AT(4, g);
-      uint32_t pk[kTile / 2];
       float alpha = 1.0f;
       if (got_s) {
-        uint32_t ra[32], rb[32], rc[16];
         tc_after_sync();
-        tmem_ld32(trow + kTmemS0 + s * kTile + 0, ra);
-        tmem_ld32(trow + kTmemS0 + s * kTile + 32, rb);
-        tmem_ld16(trow + kTmemS0 + s * kTile + 64, rc);
-        tmem_wait_ld();
-        tc_before_sync();
-        mbar_arrive(smem_addr(&c->s_free[s]));
-        if (row == 0) MLA_TRACE_AT(16, g);
-        if (i == nt - 1 && nxt < it1) {
-          // All S MMAs of this item are complete: Q's columns are free.
-          load_q(p, p.items[nxt].b, row, trow);
-          tc_before_sync();
-          mbar_arrive(smem_addr(&c->q_ready));
+        // Pass 1: row maximum of the valid columns.
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int cc = 0; cc < kTile / 16; ++cc) {
+          uint32_t r[16];
+          tmem_ld16(scol + cc * 16, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            mx = fmaxf(mx, cc * 16 + j < valid ? __uint_as_float(r[j]) : -INFINITY);
         }
-        if (active) {
-          float x[kTile];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            x[j] = __uint_as_float(ra[j]);
-            x[32 + j] = __uint_as_float(rb[j]);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) x[64 + j] = __uint_as_float(rc[j]);
-          const int valid = min(kTile, w.t1 - (w.t0 + i * kTile));
-          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < kTile; j += 4) {
-            if (j + 0 >= valid) x[j + 0] = -INFINITY;
-            if (j + 1 >= valid) x[j + 1] = -INFINITY;
-            if (j + 2 >= valid) x[j + 2] = -INFINITY;
-            if (j + 3 >= valid) x[j + 3] = -INFINITY;
-            mx0 = fmaxf(mx0, x[j + 0]);
-            mx1 = fmaxf(mx1, x[j + 1]);
-            mx2 = fmaxf(mx2, x[j + 2]);
-            mx3 = fmaxf(mx3, x[j + 3]);
-          }
-          const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-          if (m_tile > m_used + kRescaleThreshold) {
-            alpha = fast_exp2(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
-            l *= alpha;
-            m_used = m_tile;
-          }
-          float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-          for (int j = 0; j < kTile; j += 4) {
-            const float e0 = fast_exp2(fmaf(x[j + 0], sl2, -m_used));
-            const float e1 = fast_exp2(fmaf(x[j + 1], sl2, -m_used));
-            const float e2 = fast_exp2(fmaf(x[j + 2], sl2, -m_used));
-            const float e3 = fast_exp2(fmaf(x[j + 3], sl2, -m_used));
-            l0 += e0;
-            l1 += e1;
-            l2 += e2;
-            l3 += e3;
-            pk[j / 2] = pack_bf16x2(e0, e1);
-            pk[j / 2 + 1] = pack_bf16x2(e2, e3);
-          }
-          l += (l0 + l1) + (l2 + l3);
+        const float m_tile = mx * sl2;
+        if (m_tile > m_used + kRescaleThreshold) {
+          alpha = fast_exp2(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
+          l *= alpha;
+          m_used = m_tile;
         }
       }
+      if (row == 0) MLA_TRACE_AT(16, g);
       // Stage P(g) in buffer k once the copy that last read it (tile g-2) is done.
-      const int k = g & 1;
-      if (row == 0) MLA_TRACE_AT(17, g);
       if (elected && g >= kNumPBufs) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-      if (elected) MLA_TRACE_AT(18, g);
       named_barrier_sync(1, 128);
-      if (row == 0) MLA_TRACE_AT(19, g);
       if (c->abort_flag) {
         ok = false;
         break;
       }
       uint8_t* st = staging + k * kPBufBytes;
-      if (active) {
+      // Pass 2: p = 2^(s*scale*log2e - m), row sum, bf16 pack into the staging tile.
+      float lsum = 0.0f;
+#pragma unroll 1
+      for (int cc = 0; cc < kTile / 16; ++cc) {
+        uint32_t r[16];
+        tmem_ld16(scol + cc * 16, r);
+        tmem_wait_ld();
+        uint32_t pk[8];
 #pragma unroll
-        for (int q = 0; q < kPCoreK; ++q)
-          *reinterpret_cast<uint4*>(st + prow_off + q * 128) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int j = 0; j < 16; j += 2) {
+          const float e0 = cc * 16 + j < valid ? fast_exp2(fmaf(__uint_as_float(r[j]), sl2, -m_used)) : 0.0f;
+          const float e1 = cc * 16 + j + 1 < valid ? fast_exp2(fmaf(__uint_as_float(r[j + 1]), sl2, -m_used)) : 0.0f;
+          lsum += e0 + e1;
+          pk[j / 2] = pack_bf16x2(e0, e1);
+        }
+        if (active) {
+          *reinterpret_cast<uint4*>(st + prow_off + (2 * cc) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(st + prow_off + (2 * cc + 1) * 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      // S is no longer needed: its buffer may take tile g + 2.
+      tc_before_sync();
+      mbar_arrive(smem_addr(&c->s_free[s]));
+      if (row == 0) MLA_TRACE_AT(17, g);
+      if (active) {
+        l += lsum;
         float* rec = reinterpret_cast<float*>(st + kPBytes);
         rec[row] = alpha;
         rec[kMaxHeads + row] = l;
         rec[2 * kMaxHeads + row] = m_used;
       }
-      if (row == 0) MLA_TRACE_AT(20, g);
+      if (i == nt - 1 && nxt < it1) {
+        // All S MMAs of this item are complete: Q's columns are free.
+        load_q(p, p.items[nxt].b, row, trow);
+        tc_before_sync();
+        mbar_arrive(smem_addr(&c->q_ready));
+      }
       fence_proxy_async_smem();
-      if (row == 0) MLA_TRACE_AT(21, g);
       named_barrier_sync(1, 128);
       if (row == 0) MLA_TRACE_AT(5, g);
       if (elected) {
@@ -497,6 +485,52 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
   if (lane == 0) report(p, err);
 }
 
+// Prefetch warp of the output CTA: walks the pair's tiles kPrefetchTiles
+// ahead of the P tiles received so far and issues per-line L2 prefetches
+// (load/store path) for the cache pages of those tiles, so the score CTA's
+// TMA loads find them in L2. Pages are contiguous blocks of block_size x
+// 1152 bytes; each page is prefetched once per item.
+MLA_DEVI void out_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0, int it1) {
+  const char* cache = reinterpret_cast<const char*>(p.kv_cache);
+  const int lines = p.block_size * (kD * 2 / 128);
+  volatile int32_t* seen = &c->p_seen;
+  int g = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem w = p.items[it];
+    const int nt = tiles_of(w);
+    const int n_pages = (w.t1 + p.block_size - 1) / p.block_size;
+    PageWindow win;
+    int next_page = w.t0 / p.block_size;
+    for (int i = 0; i < nt; ++i, ++g) {
+      // Stay at most kPrefetchTiles ahead (bounded wait: about 1 s).
+      int ahead_ok = 1;
+      if (lane == 0) {
+        const long long t0 = clock64();
+        while (*seen < g - kPrefetchTiles) {
+          if (clock64() - t0 > kWaitLimitCycles) { ahead_ok = 0; break; }
+          __nanosleep(200);
+        }
+      }
+      if (!__shfl_sync(kFullMask, ahead_ok, 0)) return;
+      const int hi = min(n_pages, (min(w.t1, w.t0 + (i + 1) * kTile) + p.block_size - 1) / p.block_size);
+      for (; next_page < hi; ++next_page) {
+        const int page = next_page;
+        if (win.base < 0 || page < win.base || page >= win.base + 32) {
+          win.base = page;
+          win.val = (page + lane < n_pages)
+                        ? __ldg(&p.block_table[static_cast<int64_t>(w.b) * p.max_blocks + page + lane])
+                        : -1;
+        }
+        const int blk = __shfl_sync(kFullMask, win.val, page - win.base);
+        if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) continue;
+        const char* base = cache + static_cast<int64_t>(blk) * p.block_size * (kD * 2);
+        for (int ln = lane; ln < lines; ln += 32)
+          asm volatile("prefetch.global.L2 [%0];" :: "l"(base + ln * 128));
+      }
+    }
+  }
+}
+
 // MMA issuer: O[:, 256*half ...] += P . V_half (5 k-steps of 16 tokens each).
 MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
                       int it1) {
@@ -571,7 +605,10 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
         ok = false;
         break;
       }
-      if (row == 0) MLA_TRACE_AT(14, g);
+      if (row == 0) {
+        MLA_TRACE_AT(14, g);
+        atomicAdd(&c->p_seen, 1);
+      }
       const float* rec = reinterpret_cast<const float*>(pbufs + k * kPBufBytes + kPBytes);
       const float alpha = active ? rec[row] : 1.0f;
       const float lv = rec[kMaxHeads + row];
@@ -679,6 +716,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->v_empty[v]), 1);
     }
     c->abort_flag = 0;
+    c->p_seen = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -708,7 +746,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       score_producer(p, c, data, lane, it0, it1);
     } else if (warp == 1) {
       if (lane == 0) score_mma(p, c, data, tmem, it0, it1);
-    } else {
+    } else if (warp < 6) {
       score_softmax(p, c, data, tmem, warp, lane, it0, it1);
     }
   } else {
@@ -716,8 +754,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       out_producer(p, c, data, lane, it0, it1);
     } else if (warp == 1) {
       if (lane == 0) out_mma(p, c, data, tmem, it0, it1);
-    } else {
+    } else if (warp < 6) {
       out_correct(p, c, data, tmem, warp, lane, it0, it1);
+    } else {
+      out_prefetcher(p, c, lane, it0, it1);
     }
   }
   __syncwarp();

@@ -35,7 +35,7 @@ constexpr int kPBytes = kMaxHeads / 8 * kPGroupBytes;  // 20 KB
 constexpr int kRecFloats = 3;                          // per row: alpha, l, m
 constexpr int kPMsgBytes = kPBytes + kRecFloats * kMaxHeads * 4;  // 22016 B per tile
 constexpr int kPBufBytes = 22528;                      // message rounded to 512 B
-constexpr int kThreads = 192;            // 6 warps per CTA
+constexpr int kThreads = 224;            // 7 warps per CTA
 constexpr int kTmemCols = 512;
 // Score CTA TMEM columns: Q (576 bf16 packed in pairs) then two S buffers.
 constexpr int kTmemQ = 0;
@@ -71,6 +71,7 @@ struct CombineItem {
 struct DecodeParams {
   CUtensorMap tmap_kv16;          // 2-D view [num_blocks*block_size rows][576] bf16, 64x16 boxes
   CUtensorMap tmap_kv32;          // the same view with 64x32 boxes (block_size >= 32)
+  const void* kv_cache;           // the cache itself, for L2 line prefetches
   const uint16_t* q_nope;         // [B, H, 512]
   const uint16_t* q_pe;           // [B, H, 64]
   const int32_t* block_table;     // [B, max_blocks]

@@ -57,20 +57,25 @@ MLA_DEVI void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
                :: "r"(bar), "r"(bytes) : "memory");
 }
+// try_wait with a suspend-time hint: a waiting thread sleeps in hardware
+// until the phase completes (or the hint, in ns, expires) instead of
+// spinning and taking issue slots from the warps doing the work.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 MLA_DEVI bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile("{\n\t.reg .pred p;\n\t"
-               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                "selp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+               : "=r"(ok) : "r"(bar), "r"(parity), "r"(kSuspendHintNs) : "memory");
   return ok != 0;
 }
 MLA_DEVI bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile("{\n\t.reg .pred p;\n\t"
-               "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+               "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
                "selp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+               : "=r"(ok) : "r"(bar), "r"(parity), "r"(kSuspendHintNs) : "memory");
   return ok != 0;
 }
 // Wait for the completion of the phase with the given parity. Returns false
@@ -133,6 +138,19 @@ MLA_DEVI void st_async_v4(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t
 MLA_DEVI void st_async_b32(uint32_t remote_addr, uint32_t a, uint32_t remote_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                :: "r"(remote_addr), "r"(a), "r"(remote_bar) : "memory");
+}
+
+// ------------------------------------------------ cp.async (load/store path)
+// 16-byte global -> shared copy through L2 (bypassing L1); src_bytes = 0
+// writes 16 zero bytes and reads nothing.
+MLA_DEVI void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+               :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes this arrival).
+MLA_DEVI void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
