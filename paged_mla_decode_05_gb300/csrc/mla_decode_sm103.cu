@@ -36,11 +36,14 @@
 namespace mla {
 namespace {
 
+constexpr int kPanelGroups = 3;                    // a stage's 9 panels in 3 groups of 3
+constexpr int kGroupPanels = kNumPanels / kPanelGroups;
+
 // Control block: identical offsets in both CTAs of the pair, so a barrier can
 // be addressed in the peer by offset (mapa, multicast commit).
 struct Ctrl {
-  uint64_t kv_full[kNumStages * kNumPanels];   // score: panel slot landed (TMA bytes)
-  uint64_t kv_empty[kNumStages * kNumPanels];  // score: S MMAs done reading the panel slot
+  uint64_t kv_full[kNumStages * kPanelGroups];   // score: group of 3 panels landed (TMA bytes)
+  uint64_t kv_empty[kNumStages * kPanelGroups];  // score: S MMAs done reading the group
   uint64_t s_full[2];             // score: S tile in tensor memory
   uint64_t s_free[2];             // score: softmax copied S out
   uint64_t q_ready;               // score: Q of the next item in tensor memory
@@ -201,22 +204,37 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
       tile_pieces(p, w, w.t0 + i * kTile, win, lane, err, tp);
       MLA_TRACE_AT(0, g);
       const uint32_t stage = smem_addr(data + s * kStageBytes);
+      // One warp instruction issues a whole group: lane j loads box (panel
+      // grp*3 + j / n, piece j % n) of the tile.
+      const int boxes = kGroupPanels * tp.n;
+      int my_piece = lane % tp.n;
+      int my_r0 = 0, my_large = 0, my_y = 0;
+#pragma unroll
+      for (int jj = 0; jj < kMaxPieces; ++jj)
+        if (jj == my_piece) {
+          my_r0 = tp.r0[jj];
+          my_large = tp.large[jj];
+          my_y = tp.y[jj];
+        }
+      const void* my_map = my_large ? static_cast<const void*>(&p.tmap_kv32)
+                                    : static_cast<const void*>(&p.tmap_kv16);
 #pragma unroll 1
-      for (int pc = 0; pc < kNumPanels; ++pc) {
-        const int slot = s * kNumPanels + pc;
+      for (int grp = 0; grp < kPanelGroups; ++grp) {
+        const int slot = s * kPanelGroups + grp;
         if (g >= kNumStages &&
             !warp_wait(smem_addr(&c->kv_empty[slot]), ((g >> 1) - 1) & 1, lane)) {
           ok = false;
           break;
         }
-        if (lane == 0) {
-          const uint32_t full = smem_addr(&c->kv_full[slot]);
-          mbar_arrive_expect_tx(full, kPanelBytes);
-          for (int j = 0; j < tp.n; ++j)
-            tma_load_2d(stage + pc * kPanelBytes + tp.r0[j] * 128,
-                        tp.large[j] ? &p.tmap_kv32 : &p.tmap_kv16, pc * kPanelCols, tp.y[j], full,
-                        policy);
+        const uint32_t full = smem_addr(&c->kv_full[slot]);
+        if (lane == 0) mbar_arrive_expect_tx(full, kGroupPanels * kPanelBytes);
+        if (lane < boxes) {
+          const int pc = grp * kGroupPanels + lane / tp.n;
+          tma_load_2d(stage + pc * kPanelBytes + my_r0 * 128, my_map, pc * kPanelCols, my_y, full,
+                      policy);
         }
+        if (grp == 0 && lane == 0) MLA_TRACE_AT(26, g);
+        if (grp == 2 && lane == 0) MLA_TRACE_AT(27, g);
       }
     }
   }
@@ -242,17 +260,19 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
       const uint32_t d = tmem + kTmemS0 + s * kTile;
       const uint64_t b0 = smem_desc(smem_addr(data + s * kStageBytes), 16, 1024);
 #pragma unroll 1
-      for (int pc = 0; pc < kNumPanels; ++pc) {
-        const int slot = s * kNumPanels + pc;
+      for (int grp = 0; grp < kPanelGroups; ++grp) {
+        const int slot = s * kPanelGroups + grp;
         if (!mbar_wait(smem_addr(&c->kv_full[slot]), (g >> 1) & 1)) { ok = false; break; }
-        if (pc == 0) MLA_TRACE_AT(1, g);
+        if (grp == 0) MLA_TRACE_AT(1, g);
+        if (grp == 2) MLA_TRACE_AT(28, g);
         tc_after_sync();
+        const uint64_t bg = b0 + static_cast<uint64_t>((grp * kGroupPanels * kPanelBytes) >> 4);
+        const uint32_t ag = tmem + kTmemQ + grp * (kGroupPanels * 4 * 8);
 #pragma unroll
-        for (int kq = 0; kq < 4; ++kq) {
-          // panel pc, 32 bytes per k-step inside the 128-byte swizzle row
-          const int k = pc * 4 + kq;
-          const uint64_t bd = b0 + static_cast<uint64_t>((pc * kPanelBytes + kq * 32) >> 4);
-          mma_ts(d, tmem + kTmemQ + k * 8, bd, kIdescS, k > 0 ? 1u : 0u);
+        for (int kq = 0; kq < kGroupPanels * 4; ++kq) {
+          // panel kq/4 of the group, 32 bytes per k-step inside the 128-byte swizzle row
+          const uint64_t bd = bg + static_cast<uint64_t>(((kq >> 2) * kPanelBytes + (kq & 3) * 32) >> 4);
+          mma_ts(d, ag + kq * 8, bd, kIdescS, (grp > 0 || kq > 0) ? 1u : 0u);
         }
         tc_commit(smem_addr(&c->kv_empty[slot]));
       }
@@ -465,18 +485,24 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
           break;
         }
         MLA_TRACE_AT(8 + half, h >> 1);
-        if (lane == 0) {
-          const uint32_t full = smem_addr(&c->v_full[v]);
-          mbar_arrive_expect_tx(full, kVHalfBytes);
-          const uint32_t slot = smem_addr(data + v * kVHalfBytes);
-          for (int j = 0; j < tp.n; ++j) {
-            const uint32_t dst = slot + tp.r0[j] * 128;
-            const CUtensorMap* map = tp.large[j] ? &p.tmap_kv32 : &p.tmap_kv16;
+        const uint32_t full = smem_addr(&c->v_full[v]);
+        if (lane == 0) mbar_arrive_expect_tx(full, kVHalfBytes);
+        // One warp instruction: lane j loads panel j % 4 of piece j / 4.
+        if (lane < kVHalfPanels * tp.n) {
+          const int pc = lane & 3;
+          const int piece = lane >> 2;
+          int r0 = 0, large = 0, y = 0;
 #pragma unroll
-            for (int pc = 0; pc < kVHalfPanels; ++pc)
-              tma_load_2d(dst + pc * kPanelBytes, map, (half * kVHalfPanels + pc) * kPanelCols,
-                          tp.y[j], full, policy);
-          }
+          for (int jj = 0; jj < kMaxPieces; ++jj)
+            if (jj == piece) {
+              r0 = tp.r0[jj];
+              large = tp.large[jj];
+              y = tp.y[jj];
+            }
+          const void* map = large ? static_cast<const void*>(&p.tmap_kv32)
+                                  : static_cast<const void*>(&p.tmap_kv16);
+          tma_load_2d(smem_addr(data + v * kVHalfBytes) + pc * kPanelBytes + r0 * 128, map,
+                      (half * kVHalfPanels + pc) * kPanelCols, y, full, policy);
         }
       }
     }
@@ -696,7 +722,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNumStages * kNumPanels; ++s) {
+    for (int s = 0; s < kNumStages * kPanelGroups; ++s) {
       mbar_init(smem_addr(&c->kv_full[s]), 1);
       mbar_init(smem_addr(&c->kv_empty[s]), 1);
     }
