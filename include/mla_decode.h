@@ -147,6 +147,51 @@ mla_status_t mla_decode(mla_plan_t plan, const void* q_nope, const void* q_pe,
                         const int32_t* seq_lens, float sm_scale, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of device memory behind mla_decode_no_alloc (32 MiB). */
+#define MLA_NO_ALLOC_SCRATCH_BYTES (((size_t)32) << 20)
+
+/*
+ * mla_decode_no_alloc — mla_decode for callers that cannot allocate device
+ * memory at decode time. The method's sources have no counterpart: it exists
+ * for serving engines whose caching allocator already holds nearly all of
+ * HBM, so that a cudaMalloc outside the pool fails or fragments it, and for
+ * host threads that must not wait on the device-wide synchronisation that
+ * cudaMalloc and cudaFree can bring.
+ *
+ * Same computation, kernels and argument rules as mla_decode, with three
+ * differences:
+ *  - No workspace argument. The split partials, a copy of the plan's work
+ *    list and the device error word live in one fixed array of
+ *    MLA_NO_ALLOC_SCRATCH_BYTES inside the library's device image. Every GPU
+ *    that loads the library holds it until the process exits.
+ *  - The plan may be host-only (mla_decode_plan_ex with host_only = 1, so
+ *    that planning allocates no device memory either). Each call copies the
+ *    plan's work list from host memory into the scratch on `stream`.
+ *  - err_bits (device uint32, may be NULL) receives this call's
+ *    MLA_DEVERR_* bits: the call zeroes it, then the kernels OR into it. With
+ *    NULL the bits go to a word in the scratch that the call zeroes and
+ *    nobody reads. mla_check_device_error does not see this call's errors.
+ *
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no pinned memory.
+ * Its first call on each device looks up the scratch's device address (and
+ * sets the kernel attributes mla_decode also needs); make that first call
+ * before any stream capture on that device.
+ *
+ * Every call on a device shares the one scratch array, which keeps what the
+ * last call left there. Calls whose work may overlap on the GPU (different
+ * streams, or several threads) race on it and corrupt each other's results:
+ * order them on one stream or synchronise between them.
+ *
+ * Errors: those of mla_decode, and MLA_ERR_WORKSPACE_TOO_SMALL when the
+ * plan's work list plus its split partials (mla_plan_workspace_bytes) need
+ * more than MLA_NO_ALLOC_SCRATCH_BYTES; such a plan must use mla_decode.
+ */
+mla_status_t mla_decode_no_alloc(mla_plan_t plan, const void* q_nope, const void* q_pe,
+                                 const void* kv_cache, int64_t num_blocks,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 float sm_scale, void* out, float* lse, uint32_t* err_bits,
+                                 void* stream);
+
 /*
  * mla_check_device_error — synchronise `stream`, read and clear the plan's
  * device error word (sticky across decodes since the last check). Writes the

@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
         "mla_plan_num_clusters": (i32, [p]),
         "mla_plan_work_item": (i32, [p, i32, p, p, p, p, p]),
         "mla_decode": (i32, [p, p, p, p, i64, p, p, ctypes.c_float, p, p, p, sz, p]),
+        "mla_decode_no_alloc": (i32, [p, p, p, p, i64, p, p, ctypes.c_float, p, p, p, p]),
         "mla_check_device_error": (i32, [p, p, ctypes.POINTER(u32)]),
         "mla_plan_destroy": (None, [p]),
         "mla_status_string": (ctypes.c_char_p, [i32]),
@@ -223,6 +224,38 @@ def mla_decode(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, sm_sca
     _check(LIB.mla_decode(plan.handle, args[0], args[1], args[2], nb, bt, sl,
                           ctypes.c_float(sm_scale), o, l, ws, ws_bytes, _stream_ptr(stream)),
            "mla_decode")
+
+
+def mla_decode_no_alloc(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens,
+                        sm_scale: float, out, lse, err_bits=None, stream=None):
+    """Enqueue one decode that allocates nothing (see mla_decode_no_alloc in
+    include/mla_decode.h): for callers whose device memory all belongs to a
+    caching allocator, or who must not stall on cudaMalloc's synchronisation.
+
+    Same tensors as ``mla_decode`` but no workspace: the split partials live in
+    the library's fixed device scratch, shared by every call on the device, so
+    calls that may overlap on the GPU race. ``plan`` may be host-only.
+    ``err_bits`` is an optional CUDA int32 tensor of one element that receives
+    this call's device error bits.
+    """
+    import torch
+    B, H = plan.B, plan.H
+    if kv_cache.dim() != 3 or kv_cache.shape[1] != plan.block_size or kv_cache.shape[2] != D:
+        raise ValueError(f"kv_cache must have shape [num_blocks, {plan.block_size}, {D}]")
+    nb = int(kv_cache.shape[0])
+    args = [
+        _tensor(q_nope, torch.bfloat16, (B, H, D_C), "q_nope"),
+        _tensor(q_pe, torch.bfloat16, (B, H, D_R), "q_pe"),
+        _tensor(kv_cache, torch.bfloat16, (nb, plan.block_size, D), "kv_cache"),
+    ]
+    bt = _tensor(block_table, torch.int32, (B, plan.max_blocks), "block_table")
+    sl = _tensor(seq_lens, torch.int32, (B,), "seq_lens")
+    o = _tensor(out, torch.bfloat16, (B, H, D_C), "out")
+    l = _tensor(lse, torch.float32, (B, H), "lse")
+    eb = ctypes.c_void_p(0) if err_bits is None else _tensor(err_bits, torch.int32, (1,), "err_bits")
+    _check(LIB.mla_decode_no_alloc(plan.handle, args[0], args[1], args[2], nb, bt, sl,
+                                   ctypes.c_float(sm_scale), o, l, eb, _stream_ptr(stream)),
+           "mla_decode_no_alloc")
 
 
 def mla_check_device_error(plan: Plan, stream=None) -> int:

@@ -362,6 +362,33 @@ void free_plan(mla_plan_s* p) {
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
+// Tensor maps (16-row and block-height boxes) of the cache at kv_cache, kept
+// in the plan until the cache pointer or pool size changes.
+mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_blocks) {
+  if (p->tmap_ptr == kv_cache && p->tmap_blocks == num_blocks) return MLA_OK;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return MLA_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kD),
+                              static_cast<cuuint64_t>(num_blocks) * p->block_size};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kD) * 2};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap* maps[2] = {&p->tmap16, &p->tmap32};
+  const int heights[2] = {mla::kRowsSmallBox, std::min(p->block_size, mla::kRowsLargeBox)};
+  for (int i = 0; i < 2; ++i) {
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kPanelCols),
+                               static_cast<cuuint32_t>(heights[i])};
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      p->tmap_ptr = nullptr;
+      return MLA_ERR_INVALID_ARG;
+    }
+  }
+  p->tmap_ptr = kv_cache;
+  p->tmap_blocks = num_blocks;
+  return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -532,6 +559,99 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   if (!p->combine.empty()) {
     mla::CombineParams cp;
     cp.items = reinterpret_cast<const CombineItem*>(p->d_buf + p->off_combine);
+    cp.part_o = dp.part_o;
+    cp.part_lse = dp.part_lse;
+    cp.out = dp.out;
+    cp.lse = lse;
+    cp.H = p->H;
+    if (mla::launch_combine(cp, static_cast<int>(p->combine.size()), s) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+// The allocation-free variant: the workspace, the device copy of the work
+// list and the error word are carved from the library's fixed device scratch
+// (mla_no_alloc_sm103.cu) instead of caller or plan memory. Layout of the
+// scratch per call: [error word | work list as laid out by build_schedule |
+// split partials o | split partials lse].
+mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q_pe,
+                                 const void* kv_cache, int64_t num_blocks,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 float sm_scale, void* out, float* lse, uint32_t* err_bits,
+                                 void* stream) {
+  if (!p) return MLA_ERR_INVALID_ARG;
+  if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(err_bits, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || num_blocks * p->block_size + 64 >= (int64_t{1} << 31))
+    return MLA_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+  // Schedule and partials must fit the fixed scratch; checked before any
+  // device call so that an oversize plan is refused the same way everywhere.
+  const size_t o_bytes = static_cast<size_t>(p->num_slots) * p->H * mla::kDc * 4;
+  if (p->sched_bytes + p->workspace_bytes > mla::kNoAllocScratchBytes)
+    return MLA_ERR_WORKSPACE_TOO_SMALL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_UNSUPPORTED_DEVICE;
+  if (p->device >= 0 && dev != p->device) return MLA_ERR_INVALID_ARG;
+  mla_status_t st = prepare_device(dev, nullptr);
+  if (st != MLA_OK) return st;
+  uint8_t* scratch = nullptr;
+  if (mla::no_alloc_scratch(dev, &scratch) != cudaSuccess) return MLA_ERR_CUDA;
+  st = refresh_kv_maps(p, kv_cache, num_blocks);
+  if (st != MLA_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The error word is the only state that must start at zero: the work list
+  // is rewritten below, and every partial slot is written in full by its work
+  // item before the combine kernel reads it.
+  uint32_t* err = err_bits ? err_bits : reinterpret_cast<uint32_t*>(scratch);
+  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MLA_ERR_CUDA;
+  // The plan's host vectors are the source; a copy from pageable memory has
+  // been staged by the time cudaMemcpyAsync returns, so a later
+  // mla_plan_update cannot change what this call reads.
+  if (cudaMemcpyAsync(scratch + p->off_items, p->items.data(), p->items.size() * sizeof(WorkItem),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(scratch + p->off_offsets, p->cluster_offsets.data(),
+                      p->cluster_offsets.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                      s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (!p->combine.empty() &&
+      cudaMemcpyAsync(scratch + p->off_combine, p->combine.data(),
+                      p->combine.size() * sizeof(CombineItem), cudaMemcpyHostToDevice,
+                      s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+
+  uint8_t* ws = scratch + p->sched_bytes;  // sched_bytes is a multiple of 256
+  mla::DecodeParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.tmap_kv16 = p->tmap16;
+  dp.tmap_kv32 = p->tmap32;
+  dp.kv_cache = kv_cache;
+  dp.q_nope = static_cast<const uint16_t*>(q_nope);
+  dp.q_pe = static_cast<const uint16_t*>(q_pe);
+  dp.block_table = block_table;
+  dp.seq_lens = seq_lens;
+  dp.out = static_cast<uint16_t*>(out);
+  dp.lse = lse;
+  dp.part_o = p->num_slots ? reinterpret_cast<float*>(ws) : nullptr;
+  dp.part_lse = p->num_slots ? reinterpret_cast<float*>(ws + align_up(o_bytes, 256)) : nullptr;
+  dp.items = reinterpret_cast<const WorkItem*>(scratch + p->off_items);
+  dp.cluster_offsets = reinterpret_cast<const int32_t*>(scratch + p->off_offsets);
+  dp.err = err;
+  dp.H = p->H;
+  dp.block_size = p->block_size;
+  dp.max_blocks = p->max_blocks;
+  dp.num_blocks = num_blocks;
+  dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  if (mla::launch_decode(dp, p->num_clusters, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (!p->combine.empty()) {
+    mla::CombineParams cp;
+    cp.items = reinterpret_cast<const CombineItem*>(scratch + p->off_combine);
     cp.part_o = dp.part_o;
     cp.part_lse = dp.part_lse;
     cp.out = dp.out;

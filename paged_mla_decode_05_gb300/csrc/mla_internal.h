@@ -105,4 +105,10 @@ cudaError_t launch_combine(const CombineParams& p, int num_items, cudaStream_t s
 cudaError_t decode_max_clusters(int* num_clusters);
 cudaError_t decode_prepare_device();
 
+// Bytes of the fixed device scratch behind mla_decode_no_alloc.
+constexpr size_t kNoAllocScratchBytes = size_t{32} << 20;
+// Device address of that scratch on `device`, which must be current; looked
+// up on the first call per device and cached (mla_no_alloc_sm103.cu).
+cudaError_t no_alloc_scratch(int device, uint8_t** ptr);
+
 }  // namespace mla
