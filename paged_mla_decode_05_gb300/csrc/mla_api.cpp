@@ -45,9 +45,11 @@ struct mla_plan_s {
   size_t h_cap = 0;
   cudaEvent_t upload_done = nullptr;
   size_t off_items = 0, off_offsets = 0, off_combine = 0, sched_bytes = 0;
-  // Cached TMA descriptors (16- and 32-row boxes) of the last cache seen.
-  CUtensorMap tmap16;
-  CUtensorMap tmap32;
+  // Cached TMA descriptors (K and V boxes, 16- and 32-row) of the last cache seen.
+  CUtensorMap tmap_k16;
+  CUtensorMap tmap_k32;
+  CUtensorMap tmap_v16;
+  CUtensorMap tmap_v32;
   const void* tmap_ptr = nullptr;
   int64_t tmap_blocks = -1;
 };
@@ -362,22 +364,32 @@ void free_plan(mla_plan_s* p) {
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-// Tensor maps (16-row and block-height boxes) of the cache at kv_cache, kept
-// in the plan until the cache pointer or pool size changes.
+// Tensor maps of the cache at kv_cache, kept in the plan until the cache
+// pointer or pool size changes. The cache is viewed as a 3-D tensor
+// {64 columns, rows, 9 panels} with a row stride of 1152 B and a panel stride
+// of 128 B, so one box brings a run of rows across several panels and lands
+// as [panel][row][128 B] (128-byte swizzle, zero fill outside the pool).
+// Boxes: 16 or min(block_size, 32) rows; 9 panels (K: all 576 columns) or 4
+// panels (one half of V).
 mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_blocks) {
   if (p->tmap_ptr == kv_cache && p->tmap_blocks == num_blocks) return MLA_OK;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return MLA_ERR_CUDA;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kD),
-                              static_cast<cuuint64_t>(num_blocks) * p->block_size};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kD) * 2};
-  const cuuint32_t estr[2] = {1, 1};
-  CUtensorMap* maps[2] = {&p->tmap16, &p->tmap32};
-  const int heights[2] = {mla::kRowsSmallBox, std::min(p->block_size, mla::kRowsLargeBox)};
-  for (int i = 0; i < 2; ++i) {
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kPanelCols),
-                               static_cast<cuuint32_t>(heights[i])};
-    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache), dims,
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(mla::kPanelCols),
+                              static_cast<cuuint64_t>(num_blocks) * p->block_size,
+                              static_cast<cuuint64_t>(mla::kNumPanels)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(mla::kD) * 2,
+                                 static_cast<cuuint64_t>(mla::kPanelCols) * 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMap* maps[4] = {&p->tmap_k16, &p->tmap_k32, &p->tmap_v16, &p->tmap_v32};
+  const int large = std::min(p->block_size, mla::kRowsLargeBox);
+  const int heights[4] = {mla::kRowsSmallBox, large, mla::kRowsSmallBox, large};
+  const int panels[4] = {mla::kNumPanels, mla::kNumPanels, mla::kVHalfPanels, mla::kVHalfPanels};
+  for (int i = 0; i < 4; ++i) {
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(mla::kPanelCols),
+                               static_cast<cuuint32_t>(heights[i]),
+                               static_cast<cuuint32_t>(panels[i])};
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv_cache), dims,
             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       p->tmap_ptr = nullptr;
@@ -504,35 +516,15 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   mla_status_t st = prepare_device(dev, nullptr);
   if (st != MLA_OK) return st;
 
-  if (p->tmap_ptr != kv_cache || p->tmap_blocks != num_blocks) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return MLA_ERR_CUDA;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kD),
-                                static_cast<cuuint64_t>(num_blocks) * p->block_size};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kD) * 2};
-    const cuuint32_t estr[2] = {1, 1};
-    CUtensorMap* maps[2] = {&p->tmap16, &p->tmap32};
-    const int heights[2] = {mla::kRowsSmallBox, std::min(p->block_size, mla::kRowsLargeBox)};
-    for (int i = 0; i < 2; ++i) {
-      const cuuint32_t box[2] = {static_cast<cuuint32_t>(mla::kPanelCols),
-                                 static_cast<cuuint32_t>(heights[i])};
-      CUresult r = enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache),
-                       dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-      if (r != CUDA_SUCCESS) {
-        p->tmap_ptr = nullptr;
-        return MLA_ERR_INVALID_ARG;
-      }
-    }
-    p->tmap_ptr = kv_cache;
-    p->tmap_blocks = num_blocks;
-  }
+  st = refresh_kv_maps(p, kv_cache, num_blocks);
+  if (st != MLA_OK) return st;
 
   mla::DecodeParams dp;
   std::memset(&dp, 0, sizeof(dp));
-  dp.tmap_kv16 = p->tmap16;
-  dp.tmap_kv32 = p->tmap32;
+  dp.tmap_k16 = p->tmap_k16;
+  dp.tmap_k32 = p->tmap_k32;
+  dp.tmap_v16 = p->tmap_v16;
+  dp.tmap_v32 = p->tmap_v32;
   dp.kv_cache = kv_cache;
   dp.q_nope = static_cast<const uint16_t*>(q_nope);
   dp.q_pe = static_cast<const uint16_t*>(q_pe);
@@ -629,8 +621,10 @@ mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q
   uint8_t* ws = scratch + p->sched_bytes;  // sched_bytes is a multiple of 256
   mla::DecodeParams dp;
   std::memset(&dp, 0, sizeof(dp));
-  dp.tmap_kv16 = p->tmap16;
-  dp.tmap_kv32 = p->tmap32;
+  dp.tmap_k16 = p->tmap_k16;
+  dp.tmap_k32 = p->tmap_k32;
+  dp.tmap_v16 = p->tmap_v16;
+  dp.tmap_v32 = p->tmap_v32;
   dp.kv_cache = kv_cache;
   dp.q_nope = static_cast<const uint16_t*>(q_nope);
   dp.q_pe = static_cast<const uint16_t*>(q_pe);

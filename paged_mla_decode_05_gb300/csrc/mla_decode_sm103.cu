@@ -14,16 +14,18 @@
 // one 2-CTA cluster per work list, with split roles, because the fp32 output
 // accumulator of 128 heads x 512 columns fills a whole SM's tensor memory:
 //  * score CTA (cluster rank 0): streams 80-token KV tiles (all 576 columns)
-//    into two 90 KB shared-memory stages with TMA (16-row boxes per 64-column
-//    panel, block ids resolved from the block table), keeps Q [128 heads x
-//    576] in tensor memory, issues S = Q.K^T with tcgen05 (M = 128 heads,
-//    N = 80 tokens, A from tensor memory), runs the fp32 online softmax (one
-//    thread per head row, lazy rescaling), stages P (bf16) with the per-row
-//    rescale record in shared memory and ships each tile to the output CTA
-//    with one bulk copy into its shared memory (distributed shared memory).
+//    into two 90 KB shared-memory stages, one 3-D TMA box per page piece (a
+//    page-aligned run of 32 or 16 rows across all 9 panels; per-SM TMA cost
+//    is per box, so few large boxes keep up with HBM), keeps Q [128 heads x
+//    576] in tensor memory, and computes S = Q.K^T with tcgen05 (M = 128
+//    heads, N = the piece's rows, A from tensor memory) from three issuer
+//    threads, one per piece. The fp32 online softmax (one thread per head
+//    row, one pass per tile with a lazy rescale) stages P (bf16) and the
+//    per-row rescale record in shared memory and ships each tile to the
+//    output CTA with one bulk copy into its shared memory.
 //  * output CTA (rank 1): holds O [128 x 512] fp32 in tensor memory, streams
-//    V half-tiles (256 columns) into a 4-slot ring with its own TMA loads
-//    (L2 hits: the score CTA just read the same lines), issues O += P.V with
+//    V half-tiles (256 columns) into a 4-slot ring with 3-D TMA boxes (L2
+//    hits: the score CTA just read the same lines), issues O += P.V with
 //    tcgen05 (N = 256), applies the rescale when the softmax max moved, and
 //    writes the normalised output.
 // Heads below 128 are padded inside the kernel: zero Q rows in tensor memory
@@ -36,14 +38,13 @@
 namespace mla {
 namespace {
 
-constexpr int kPanelGroups = 3;                    // a stage's 9 panels in 3 groups of 3
-constexpr int kGroupPanels = kNumPanels / kPanelGroups;
+constexpr int kScoreIssuers = 3;   // score MMA issuer threads (warps 1, 6, 7 of the score CTA)
 
 // Control block: identical offsets in both CTAs of the pair, so a barrier can
 // be addressed in the peer by offset (mapa, multicast commit).
 struct Ctrl {
-  uint64_t kv_full[kNumStages * kPanelGroups];   // score: group of 3 panels landed (TMA bytes)
-  uint64_t kv_empty[kNumStages * kPanelGroups];  // score: S MMAs done reading the group
+  uint64_t kv_full[kNumStages * kMaxPieces];    // score: piece of a stage landed (TMA bytes)
+  uint64_t kv_empty[kNumStages * kMaxPieces];   // score: S MMAs done reading the piece
   uint64_t s_full[2];             // score: S tile in tensor memory
   uint64_t s_free[2];             // score: softmax copied S out
   uint64_t q_ready;               // score: Q of the next item in tensor memory
@@ -59,7 +60,8 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTile, 0, 0);   // K-major A and B
+constexpr uint32_t kIdescS32 = idesc_bf16_f32(128, kRowsLargeBox, 0, 0);  // K-major A and B
+constexpr uint32_t kIdescS16 = idesc_bf16_f32(128, kRowsSmallBox, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);    // V is MN-major
 constexpr float kRescaleThreshold = 8.0f;                        // log2 units
 constexpr uint32_t kFullMask = 0xffffffffu;
@@ -106,63 +108,79 @@ struct PageWindow {
   int val = 0;
 };
 
-// Row of the 2-D cache view holding token t (all lanes call this together),
-// or the first row past the pool (a TMA box there reads zeros) for tokens at
-// or past the item's end and for out-of-range block ids (MLA_DEVERR_BAD_BLOCK).
-MLA_DEVI int cache_row(const DecodeParams& p, const WorkItem& w, int t, PageWindow& win,
-                       int lane, uint32_t& err) {
-  const int oob = static_cast<int>(p.num_blocks * p.block_size);
-  if (t >= w.t1) return oob;
-  const int page = t / p.block_size;
-  if (win.base < 0 || page < win.base || page >= win.base + 32) {
-    win.base = page;
-    const int n_pages = (w.t1 + p.block_size - 1) / p.block_size;
-    win.val = (page + lane < n_pages)
-                  ? __ldg(&p.block_table[static_cast<int64_t>(w.b) * p.max_blocks + page + lane])
+// The pieces of one 80-token tile: page-aligned runs of 32 rows where they fit
+// (block size >= 32), else 16. A tile starts at a multiple of 80 tokens, so at
+// offset 0 or 16 modulo 32, and every piece stays inside one page.
+MLA_DEVI int pieces_per_tile(int block_size) {
+  return block_size >= kRowsLargeBox ? 3 : kMaxPieces;
+}
+// Piece j of the tile starting at token tile_t0: first row inside the tile
+// and whether it is a 32-row box.
+MLA_DEVI void piece_shape(int block_size, int tile_t0, int j, int& r0, int& large) {
+  if (block_size < kRowsLargeBox) {
+    r0 = j * kRowsSmallBox;
+    large = 0;
+  } else if ((tile_t0 & 31) == 0) {
+    r0 = j * kRowsLargeBox;
+    large = j < 2;
+  } else {
+    r0 = j == 0 ? 0 : kRowsSmallBox + (j - 1) * kRowsLargeBox;
+    large = j > 0;
+  }
+}
+
+// Make the warp's block-table window cover the pages of the tile starting at
+// tile_t0 (all lanes call this together; lane i holds page base + i).
+MLA_DEVI void window_cover(const DecodeParams& p, const WorkItem& w, int tile_t0,
+                           PageWindow& win, int lane) {
+  const int sh = __ffs(p.block_size) - 1;   // block sizes are powers of two
+  const int first = tile_t0 >> sh;
+  const int last = (min(tile_t0 + kTile, w.t1) - 1) >> sh;
+  if (win.base < 0 || first < win.base || last >= win.base + 32) {
+    win.base = first;
+    const int n_pages = (w.t1 + p.block_size - 1) >> sh;
+    win.val = (first + lane < n_pages)
+                  ? __ldg(&p.block_table[static_cast<int64_t>(w.b) * p.max_blocks + first + lane])
                   : -1;
   }
-  const int blk = __shfl_sync(kFullMask, win.val, page - win.base);
+}
+
+// Cache row of token t through the window (all lanes call this together,
+// each for its own t), or the first row past the pool (a TMA box there reads
+// zeros) for tokens at or past the item's end and for out-of-range block ids
+// (MLA_DEVERR_BAD_BLOCK).
+MLA_DEVI int cache_row(const DecodeParams& p, const WorkItem& w, int t, const PageWindow& win,
+                       uint32_t& err) {
+  const int sh = __ffs(p.block_size) - 1;
+  const int blk = __shfl_sync(kFullMask, win.val, ((t >> sh) - win.base) & 31);
+  const int oob = static_cast<int>(p.num_blocks * p.block_size);
+  if (t >= w.t1) return oob;
   if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
     err |= 1u;  // MLA_DEVERR_BAD_BLOCK
     return oob;
   }
-  return blk * p.block_size + (t % p.block_size);
+  return (blk << sh) + (t & (p.block_size - 1));
 }
 
-// The TMA boxes that cover one 80-token tile of one 64-column panel: pieces of
-// 32 rows where a 32-row page-aligned run fits (block size >= 32), else 16.
-// A tile starts at a multiple of 80 tokens, so it starts at offset 0 or 16
-// modulo 32 and every piece stays inside one page.
-struct TilePieces {
-  int n;
-  int r0[kMaxPieces];     // first row of the piece inside the tile
-  int large[kMaxPieces];  // 1: 32-row box, 0: 16-row box
-  int y[kMaxPieces];      // cache row of the piece (or the zero-fill row past the pool)
-};
-
-MLA_DEVI void tile_pieces(const DecodeParams& p, const WorkItem& w, int tile_t0, PageWindow& win,
-                          int lane, uint32_t& err, TilePieces& tp) {
-  if (p.block_size >= kRowsLargeBox) {
-    if ((tile_t0 & 31) == 0) {
-      tp.n = 3;
-      tp.r0[0] = 0;  tp.large[0] = 1;
-      tp.r0[1] = 32; tp.large[1] = 1;
-      tp.r0[2] = 64; tp.large[2] = 0;
-    } else {
-      tp.n = 3;
-      tp.r0[0] = 0;  tp.large[0] = 0;
-      tp.r0[1] = 16; tp.large[1] = 1;
-      tp.r0[2] = 48; tp.large[2] = 1;
-    }
+// The piece holding tile row kr (a multiple of 16): its first row and height.
+MLA_DEVI void piece_of_row(int block_size, int tile_t0, int kr, int& r0, int& rows) {
+  if (block_size < kRowsLargeBox) {
+    r0 = kr & ~15;
+    rows = kRowsSmallBox;
+  } else if ((tile_t0 & 31) == 0) {
+    r0 = kr < 64 ? (kr & ~31) : 64;
+    rows = kr < 64 ? kRowsLargeBox : kRowsSmallBox;
   } else {
-    tp.n = kMaxPieces;
-#pragma unroll
-    for (int j = 0; j < kMaxPieces; ++j) {
-      tp.r0[j] = j * kRowsSmallBox;
-      tp.large[j] = 0;
-    }
+    r0 = kr < 16 ? 0 : 16 + ((kr - 16) & ~31);
+    rows = kr < 16 ? kRowsSmallBox : kRowsLargeBox;
   }
-  for (int j = 0; j < tp.n; ++j) tp.y[j] = cache_row(p, w, tile_t0 + tp.r0[j], win, lane, err);
+}
+
+// Index of the piece holding tile row kr (any row) in the tile starting at tile_t0.
+MLA_DEVI int piece_index_of_row(int block_size, int tile_t0, int kr) {
+  if (block_size < kRowsLargeBox) return kr >> 4;
+  if ((tile_t0 & 31) == 0) return kr < 64 ? (kr >> 5) : 2;
+  return kr < 16 ? 0 : 1 + ((kr - 16) >> 5);
 }
 
 // Lane 0 waits on a barrier; the whole warp learns the outcome.
@@ -174,13 +192,22 @@ MLA_DEVI bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
 
 // ------------------------------------------------------------ score CTA roles
 
-// TMA producer warp: all 9 panels of each 80-token tile into stage g % 2.
+// TMA producer warp: each 80-token tile into stage g % 2 as one 3-D box per
+// piece (all 9 panels), lane j loading piece j, each piece on its own
+// barrier. A stage holds piece j of the tile at r0_j * 1152 B as
+// [panel][rows][128 B]; consecutive tiles may be cut into pieces differently
+// (a tile's cut depends on its first token modulo 32), so before a piece
+// overwrites its rows the lane waits until the S MMAs are done with the old
+// piece holding the new piece's last row (they finish pieces in order).
 MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int lane, int it0,
                              int it1) {
   uint32_t err = 0;
   const uint64_t policy = policy_evict_normal();
   int g = 0;
   bool ok = true;
+  int prev_t0_even = 0, prev_t0_odd = 0;   // first token of the tile each stage last held
+  static_assert(kNumStages == 2, "one previous-tile record per stage");
+  const int n = pieces_per_tile(p.block_size);
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
     if (lane == 0) {
@@ -200,53 +227,52 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
     const int nt = tiles_of(w);
     for (int i = 0; i < nt && ok; ++i, ++g) {
       const int s = g & 1;
-      TilePieces tp;
-      tile_pieces(p, w, w.t0 + i * kTile, win, lane, err, tp);
+      const int tile_t0 = w.t0 + i * kTile;
+      int r0, large;
+      piece_shape(p.block_size, tile_t0, lane < n ? lane : 0, r0, large);
+      window_cover(p, w, tile_t0, win, lane);
+      const int y = cache_row(p, w, tile_t0 + r0, win, err);
+      const int rows = large ? kRowsLargeBox : kRowsSmallBox;
       MLA_TRACE_AT(0, g);
-      const uint32_t stage = smem_addr(data + s * kStageBytes);
-      // One warp instruction issues a whole group: lane j loads box (panel
-      // grp*3 + j / n, piece j % n) of the tile.
-      const int boxes = kGroupPanels * tp.n;
-      int my_piece = lane % tp.n;
-      int my_r0 = 0, my_large = 0, my_y = 0;
-#pragma unroll
-      for (int jj = 0; jj < kMaxPieces; ++jj)
-        if (jj == my_piece) {
-          my_r0 = tp.r0[jj];
-          my_large = tp.large[jj];
-          my_y = tp.y[jj];
+      bool good = true;
+      if (lane < n) {
+        if (g >= kNumStages) {
+          const int jw = piece_index_of_row(p.block_size, s ? prev_t0_odd : prev_t0_even,
+                                            r0 + rows - 1);
+          good = mbar_wait(smem_addr(&c->kv_empty[s * kMaxPieces + jw]), ((g >> 1) - 1) & 1);
         }
-      const void* my_map = my_large ? static_cast<const void*>(&p.tmap_kv32)
-                                    : static_cast<const void*>(&p.tmap_kv16);
-#pragma unroll 1
-      for (int grp = 0; grp < kPanelGroups; ++grp) {
-        const int slot = s * kPanelGroups + grp;
-        if (g >= kNumStages &&
-            !warp_wait(smem_addr(&c->kv_empty[slot]), ((g >> 1) - 1) & 1, lane)) {
-          ok = false;
-          break;
+        if (good) {
+          const uint32_t full = smem_addr(&c->kv_full[s * kMaxPieces + lane]);
+          mbar_arrive_expect_tx(full, rows * kD * 2);
+          tma_load_3d(smem_addr(data + s * kStageBytes + r0 * (kD * 2)),
+                      large ? static_cast<const void*>(&p.tmap_k32)
+                            : static_cast<const void*>(&p.tmap_k16),
+                      0, y, 0, full, policy);
         }
-        const uint32_t full = smem_addr(&c->kv_full[slot]);
-        if (lane == 0) mbar_arrive_expect_tx(full, kGroupPanels * kPanelBytes);
-        if (lane < boxes) {
-          const int pc = grp * kGroupPanels + lane / tp.n;
-          tma_load_2d(stage + pc * kPanelBytes + my_r0 * 128, my_map, pc * kPanelCols, my_y, full,
-                      policy);
-        }
-        if (grp == 0 && lane == 0) MLA_TRACE_AT(26, g);
-        if (grp == 2 && lane == 0) MLA_TRACE_AT(27, g);
+        if (lane == 0) MLA_TRACE_AT(26, g);
       }
+      if (s) prev_t0_odd = tile_t0;
+      else prev_t0_even = tile_t0;
+      if (!__all_sync(kFullMask, good)) ok = false;
     }
   }
   if (!ok) err |= 4u;
+  err = __reduce_or_sync(kFullMask, err);
   if (lane == 0) report(p, err);
 }
 
-// MMA issuer: S[g%2] = Q . K^T over the 576 columns (36 k-steps of 16).
+// S MMA issuers: S[g%2] = Q . K^T over the 576 columns, per piece (N = the
+// piece's 16 or 32 rows, written to the piece's own S columns; 36 k-steps of
+// 16). kScoreIssuers threads in different warps each take the pieces j with
+// j % kScoreIssuers == m: one thread issues at most one MMA every ~50 cycles,
+// so small-N MMAs from a single thread would leave the tensor pipe idle. Each
+// issuer commits its own MMAs: kv_empty of its pieces, then s_full (which
+// counts one arrival per issuer).
 MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
-                        int it1) {
+                        int it1, int m) {
   int g = 0, n_items = 0;
   bool ok = true;
+  const int n = pieces_per_tile(p.block_size);
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
     const int nt = tiles_of(w);
@@ -256,29 +282,41 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
       if (g >= 2 && !mbar_wait(smem_addr(&c->s_free[s]), ((g >> 1) - 1) & 1)) { ok = false; break; }
-      MLA_TRACE_AT(2, g);
-      const uint32_t d = tmem + kTmemS0 + s * kTile;
-      const uint64_t b0 = smem_desc(smem_addr(data + s * kStageBytes), 16, 1024);
+      if (m == 0) MLA_TRACE_AT(2, g);
+      const int tile_t0 = w.t0 + i * kTile;
+      const uint32_t stage = smem_addr(data + s * kStageBytes);
 #pragma unroll 1
-      for (int grp = 0; grp < kPanelGroups; ++grp) {
-        const int slot = s * kPanelGroups + grp;
+      for (int j = m; j < n; j += kScoreIssuers) {
+        int r0, large;
+        piece_shape(p.block_size, tile_t0, j, r0, large);
+        const int slot = s * kMaxPieces + j;
         if (!mbar_wait(smem_addr(&c->kv_full[slot]), (g >> 1) & 1)) { ok = false; break; }
-        if (grp == 0) MLA_TRACE_AT(1, g);
-        if (grp == 2) MLA_TRACE_AT(28, g);
+        if (m == 0 && j == 0) MLA_TRACE_AT(1, g);
+        if (m > 0 && j < kScoreIssuers) MLA_TRACE_AT(26 + 2 * m, g);
         tc_after_sync();
-        const uint64_t bg = b0 + static_cast<uint64_t>((grp * kGroupPanels * kPanelBytes) >> 4);
-        const uint32_t ag = tmem + kTmemQ + grp * (kGroupPanels * 4 * 8);
+        const uint32_t d = tmem + kTmemS0 + s * kTile + r0;
+        const uint32_t idesc = large ? kIdescS32 : kIdescS16;
+        // Descriptor of the piece's first panel; later k-steps only move the
+        // start-address field (low word, 16-byte units, never carries out).
+        const uint64_t bp = smem_desc(stage + r0 * (kD * 2), 16, 1024);
+        const uint32_t lo = static_cast<uint32_t>(bp);
+        const uint32_t hi = static_cast<uint32_t>(bp >> 32);
+        const uint32_t panel_step = (large ? kRowsLargeBox : kRowsSmallBox) * 128 / 16;
+        uint32_t a = tmem + kTmemQ;
+        uint32_t blo = lo;
+#pragma unroll 1
+        for (int pc = 0; pc < kNumPanels; ++pc, a += 32, blo += panel_step) {
 #pragma unroll
-        for (int kq = 0; kq < kGroupPanels * 4; ++kq) {
-          // panel kq/4 of the group, 32 bytes per k-step inside the 128-byte swizzle row
-          const uint64_t bd = bg + static_cast<uint64_t>(((kq >> 2) * kPanelBytes + (kq & 3) * 32) >> 4);
-          mma_ts(d, ag + kq * 8, bd, kIdescS, (grp > 0 || kq > 0) ? 1u : 0u);
+          for (int q = 0; q < 4; ++q)   // 32 bytes per k-step inside the 128-byte swizzle row
+            mma_ts(d, a + q * 8, (static_cast<uint64_t>(hi) << 32) | (blo + q * 2), idesc,
+                   (pc > 0 || q > 0) ? 1u : 0u);
         }
+        if (j < kScoreIssuers) MLA_TRACE_AT(m == 0 ? 24 : 27 + 2 * m, g);
         tc_commit(smem_addr(&c->kv_empty[slot]));
       }
       if (!ok) break;
       tc_commit(smem_addr(&c->s_full[s]));
-      MLA_TRACE_AT(3, g);
+      if (m == 0) MLA_TRACE_AT(3, g);
     }
   }
   if (!ok) report(p, 4u);
@@ -361,26 +399,6 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       if (!got_s && lane == 0) c->abort_flag = 1;
       if (row == 0) MLA_TRACE_AT(4, g);
       float alpha = 1.0f;
-      if (got_s) {
-        tc_after_sync();
-        // Pass 1: row maximum of the valid columns.
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int cc = 0; cc < kTile / 16; ++cc) {
-          uint32_t r[16];
-          tmem_ld16(scol + cc * 16, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            mx = fmaxf(mx, cc * 16 + j < valid ? __uint_as_float(r[j]) : -INFINITY);
-        }
-        const float m_tile = mx * sl2;
-        if (m_tile > m_used + kRescaleThreshold) {
-          alpha = fast_exp2(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
-          l *= alpha;
-          m_used = m_tile;
-        }
-      }
       if (row == 0) MLA_TRACE_AT(16, g);
       // Stage P(g) in buffer k once the copy that last read it (tile g-2) is done.
       if (elected && g >= kNumPBufs) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -389,27 +407,64 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
         ok = false;
         break;
       }
+      tc_after_sync();
       uint8_t* st = staging + k * kPBufBytes;
-      // Pass 2: p = 2^(s*scale*log2e - m), row sum, bf16 pack into the staging tile.
-      float lsum = 0.0f;
+      // p = 2^(s*scale*log2e - m) with the running maximum m, row sum, bf16
+      // pack into the staging tile (one 16-byte core-matrix row per 8
+      // columns); the tile's own maximum is tracked on the way. If it lies
+      // more than kRescaleThreshold above m for some row (always on an
+      // item's first tile, rarely after), the warp redoes the tile with the
+      // new maximum. S is read in two halves of 40 columns, one batched load
+      // and one wait each, in rolled loops: compact code.
+      float ls0, ls1;
 #pragma unroll 1
-      for (int cc = 0; cc < kTile / 16; ++cc) {
-        uint32_t r[16];
-        tmem_ld16(scol + cc * 16, r);
-        tmem_wait_ld();
-        uint32_t pk[8];
+      while (true) {
+        ls0 = 0.0f;
+        ls1 = 0.0f;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t r[40];
+          tmem_ld32(scol + hh * 40, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld8(scol + hh * 40 + 32, &r[32]);
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const float e0 = cc * 16 + j < valid ? fast_exp2(fmaf(__uint_as_float(r[j]), sl2, -m_used)) : 0.0f;
-          const float e1 = cc * 16 + j + 1 < valid ? fast_exp2(fmaf(__uint_as_float(r[j + 1]), sl2, -m_used)) : 0.0f;
-          lsum += e0 + e1;
-          pk[j / 2] = pack_bf16x2(e0, e1);
+          for (int j = 0; j < 40; j += 8) reg_fence8(&r[j]);
+          if (row == 0) MLA_TRACE_AT(18 + 2 * hh, g);
+          const int vh = valid - hh * 40;
+#pragma unroll
+          for (int q = 0; q < 5; ++q) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+              const int cc = 8 * q + j;
+              const float s0 = cc < vh ? __uint_as_float(r[cc]) : -INFINITY;
+              const float s1 = cc + 1 < vh ? __uint_as_float(r[cc + 1]) : -INFINITY;
+              mx0 = fmaxf(mx0, s0);
+              mx1 = fmaxf(mx1, s1);
+              const float e0 = fast_exp2(fmaf(s0, sl2, -m_used));
+              const float e1 = fast_exp2(fmaf(s1, sl2, -m_used));
+              ls0 += e0;
+              ls1 += e1;
+              pk[j / 2] = pack_bf16x2(e0, e1);
+            }
+            if (active)
+              *reinterpret_cast<uint4*>(st + prow_off + (hh * 5 + q) * 128) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          if (row == 0) MLA_TRACE_AT(19 + 2 * hh, g);
         }
-        if (active) {
-          *reinterpret_cast<uint4*>(st + prow_off + (2 * cc) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(st + prow_off + (2 * cc + 1) * 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        const float m_tile = fmaxf(mx0, mx1) * sl2;
+        const bool need = m_tile > m_used + kRescaleThreshold;
+        if (!__any_sync(kFullMask, need)) break;
+        if (need) {
+          const float a = fast_exp2(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
+          alpha *= a;
+          l *= a;
+          m_used = m_tile;
         }
       }
+      const float lsum = ls0 + ls1;
       // S is no longer needed: its buffer may take tile g + 2.
       tc_before_sync();
       mbar_arrive(smem_addr(&c->s_free[s]));
@@ -475,8 +530,12 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
     const int nt = tiles_of(w);
     PageWindow win;
     for (int i = 0; i < nt && ok; ++i) {
-      TilePieces tp;
-      tile_pieces(p, w, w.t0 + i * kTile, win, lane, err, tp);
+      const int tile_t0 = w.t0 + i * kTile;
+      const int n = pieces_per_tile(p.block_size);
+      int r0, large;
+      piece_shape(p.block_size, tile_t0, lane < n ? lane : 0, r0, large);
+      window_cover(p, w, tile_t0, win, lane);
+      const int y = cache_row(p, w, tile_t0 + r0, win, err);
       for (int half = 0; half < 2; ++half, ++h) {
         const int v = h % kNumVSlots;
         if (h >= kNumVSlots &&
@@ -487,27 +546,19 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
         MLA_TRACE_AT(8 + half, h >> 1);
         const uint32_t full = smem_addr(&c->v_full[v]);
         if (lane == 0) mbar_arrive_expect_tx(full, kVHalfBytes);
-        // One warp instruction: lane j loads panel j % 4 of piece j / 4.
-        if (lane < kVHalfPanels * tp.n) {
-          const int pc = lane & 3;
-          const int piece = lane >> 2;
-          int r0 = 0, large = 0, y = 0;
-#pragma unroll
-          for (int jj = 0; jj < kMaxPieces; ++jj)
-            if (jj == piece) {
-              r0 = tp.r0[jj];
-              large = tp.large[jj];
-              y = tp.y[jj];
-            }
-          const void* map = large ? static_cast<const void*>(&p.tmap_kv32)
-                                  : static_cast<const void*>(&p.tmap_kv16);
-          tma_load_2d(smem_addr(data + v * kVHalfBytes) + pc * kPanelBytes + r0 * 128, map,
-                      (half * kVHalfPanels + pc) * kPanelCols, y, full, policy);
+        __syncwarp();
+        // One warp instruction: lane j loads piece j (4 panels of this half).
+        if (lane < n) {
+          tma_load_3d(smem_addr(data + v * kVHalfBytes) + r0 * (kVHalfPanels * 128),
+                      large ? static_cast<const void*>(&p.tmap_v32)
+                            : static_cast<const void*>(&p.tmap_v16),
+                      0, y, half * kVHalfPanels, full, policy);
         }
       }
     }
   }
   if (!ok) err |= 4u;
+  err = __reduce_or_sync(kFullMask, err);
   if (lane == 0) report(p, err);
 }
 
@@ -568,6 +619,7 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
     const int nt = tiles_of(w);
     for (int i = 0; i < nt; ++i, ++g) {
       const int k = g & 1;
+      const int tile_t0 = w.t0 + i * kTile;
       if (!mbar_wait(smem_addr(&c->o_ready[g & 1]), (g >> 1) & 1)) { ok = false; break; }
       MLA_TRACE_AT(10, g);
       tc_after_sync();
@@ -583,11 +635,16 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
         if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
         MLA_TRACE_AT(11 + half, g);
         tc_after_sync();
-        const uint64_t b0 = smem_desc(smem_addr(data + v * kVHalfBytes), kPanelBytes, 1024);
+        // V half: MN-major, 128-byte swizzle; the 16 tokens of k-step kk lie
+        // in one piece, whose panels are (piece rows x 128 B) apart.
+        const uint32_t vs = smem_addr(data + v * kVHalfBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
+          int r0, rows;
+          piece_of_row(p.block_size, tile_t0, kk * 16, r0, rows);
           const uint64_t ad = a0 + static_cast<uint64_t>((kk * 256) >> 4);
-          const uint64_t bd = b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+          const uint64_t bd = smem_desc(vs + r0 * (kVHalfPanels * 128) + (kk * 16 - r0) * 128,
+                                        rows * 128, 1024);
           mma_ss(tmem + half * 256, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_addr(&c->v_empty[v]));
@@ -722,12 +779,12 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNumStages * kPanelGroups; ++s) {
+    for (int s = 0; s < kNumStages * kMaxPieces; ++s) {
       mbar_init(smem_addr(&c->kv_full[s]), 1);
       mbar_init(smem_addr(&c->kv_empty[s]), 1);
     }
     for (int j = 0; j < 2; ++j) {
-      mbar_init(smem_addr(&c->s_full[j]), 1);
+      mbar_init(smem_addr(&c->s_full[j]), kScoreIssuers);
       mbar_init(smem_addr(&c->s_free[j]), 128);
       mbar_init(smem_addr(&c->o_ready[j]), 128);
       mbar_init(smem_addr(&c->o_done[j]), 1);
@@ -746,8 +803,11 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&p.tmap_kv16);
-    prefetch_tmap(&p.tmap_kv32);
+    prefetch_tmap(&p.tmap_k16);
+    prefetch_tmap(&p.tmap_k32);
+  } else if (warp == 0 && lane == 1) {
+    prefetch_tmap(&p.tmap_v16);
+    prefetch_tmap(&p.tmap_v32);
   }
   {
     // Zero the P staging buffers (score CTA) and P buffers (output CTA) once:
@@ -770,9 +830,9 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   if (rank == 0) {
     if (warp == 0) {
       score_producer(p, c, data, lane, it0, it1);
-    } else if (warp == 1) {
-      if (lane == 0) score_mma(p, c, data, tmem, it0, it1);
-    } else if (warp < 6) {
+    } else if (warp == 1 || warp >= 6) {
+      if (lane == 0) score_mma(p, c, data, tmem, it0, it1, warp == 1 ? 0 : warp - 5);
+    } else {
       score_softmax(p, c, data, tmem, warp, lane, it0, it1);
     }
   } else {
@@ -782,7 +842,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       if (lane == 0) out_mma(p, c, data, tmem, it0, it1);
     } else if (warp < 6) {
       out_correct(p, c, data, tmem, warp, lane, it0, it1);
-    } else {
+    } else if (warp == 6) {
       out_prefetcher(p, c, lane, it0, it1);
     }
   }

@@ -20,8 +20,12 @@ constexpr int kMaxPieces = kTile / kRowsSmallBox;      // at most 5 boxes per pa
 constexpr int kPanelCols = 64;           // bf16 columns of one 128-byte swizzle panel
 constexpr int kNumPanels = kD / kPanelCols;            // 9 panels per row
 constexpr int kPanelBytes = kTile * 128;               // one panel of one tile: 10 KB
+// Score stage: the piece of rows r0.. of the tile at r0 * 1152 B, laid out as
+// [9 panels][rows of the piece][128 B].
 constexpr int kStageBytes = kNumPanels * kPanelBytes;  // full 576-wide tile: 90 KB
 constexpr int kVHalfPanels = 4;                        // V half = 256 columns
+// V half slot: the piece of rows r0.. of the tile at r0 * 512 B, laid out as
+// [4 panels][rows of the piece][128 B].
 constexpr int kVHalfBytes = kVHalfPanels * kPanelBytes;  // 40 KB
 constexpr int kNumStages = 2;            // score CTA: KV tiles in flight
 constexpr int kNumVSlots = 4;            // output CTA: V half-tiles in flight
@@ -35,7 +39,7 @@ constexpr int kPBytes = kMaxHeads / 8 * kPGroupBytes;  // 20 KB
 constexpr int kRecFloats = 3;                          // per row: alpha, l, m
 constexpr int kPMsgBytes = kPBytes + kRecFloats * kMaxHeads * 4;  // 22016 B per tile
 constexpr int kPBufBytes = 22528;                      // message rounded to 512 B
-constexpr int kThreads = 224;            // 7 warps per CTA
+constexpr int kThreads = 256;            // 8 warps per CTA
 constexpr int kTmemCols = 512;
 // Score CTA TMEM columns: Q (576 bf16 packed in pairs) then two S buffers.
 constexpr int kTmemQ = 0;
@@ -69,8 +73,14 @@ struct CombineItem {
 };
 
 struct DecodeParams {
-  CUtensorMap tmap_kv16;          // 2-D view [num_blocks*block_size rows][576] bf16, 64x16 boxes
-  CUtensorMap tmap_kv32;          // the same view with 64x32 boxes (block_size >= 32)
+  // 3-D views of the cache {64 columns, num_blocks*block_size rows, 9 panels}
+  // (row stride 1152 B, panel stride 128 B): one box brings a page-aligned
+  // run of 16 or 32 rows across several 64-column panels, landing in shared
+  // memory as [panel][row][128 B] with the 128-byte swizzle.
+  CUtensorMap tmap_k16;           // box {64, 16, 9}: all 576 columns
+  CUtensorMap tmap_k32;           // box {64, 32, 9} (block_size >= 32)
+  CUtensorMap tmap_v16;           // box {64, 16, 4}: one 256-column half of V
+  CUtensorMap tmap_v32;           // box {64, 32, 4} (block_size >= 32)
   const void* kv_cache;           // the cache itself, for L2 line prefetches
   const uint16_t* q_nope;         // [B, H, 512]
   const uint16_t* q_pe;           // [B, H, 64]

@@ -79,23 +79,50 @@ MLA_DEVI bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the completion of the phase with the given parity. Returns false
-// if the wait ran out of time.
-MLA_DEVI bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try(bar, parity)) return true;
+// if the wait ran out of time. The first try is inline; the bounded retry
+// loop is out of line, so the many wait sites stay small in the
+// instruction cache.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {
     if (clock64() - t0 > kWaitLimitCycles) return false;
   }
   return true;
 }
+MLA_DEVI bool mbar_wait(uint32_t bar, uint32_t parity) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity);
+}
 // Same, with acquire at cluster scope: for barriers completed by the peer CTA.
-MLA_DEVI bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-  if (mbar_try_cluster(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try_cluster(bar, parity)) {
     if (clock64() - t0 > kWaitLimitCycles) return false;
   }
   return true;
+}
+MLA_DEVI bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  return mbar_try_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity);
+}
+
+// Polling wait (mbarrier.test_wait, no suspension): for a thread whose wake-up
+// latency sits on the critical path. Bounded like mbar_wait.
+MLA_DEVI bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __noinline__ bool mbar_poll_slow(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+MLA_DEVI bool mbar_poll(uint32_t bar, uint32_t parity) {
+  return mbar_test(bar, parity) || mbar_poll_slow(bar, parity);
 }
 
 MLA_DEVI void fence_proxy_async_smem() {
@@ -112,6 +139,24 @@ MLA_DEVI void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
+}
+// 3-D tiled TMA load (coordinates innermost first), completion on `bar`.
+MLA_DEVI void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar,
+                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy) : "memory");
+}
+// 2-D tiled TMA load multicast to the CTAs of cta_mask: the box lands at the
+// same shared-memory offset in each, completing on the barrier at the same
+// offset in each.
+MLA_DEVI void tma_load_2d_multicast(uint32_t dst, const void* tmap, int x, int y, uint32_t bar,
+                                    uint16_t cta_mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(policy) : "memory");
 }
 MLA_DEVI uint64_t policy_evict_first() {
   uint64_t p;
@@ -222,6 +267,24 @@ MLA_DEVI void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
+}
+// Order later uses of registers filled by tcgen05.ld after tcgen05.wait::ld:
+// an empty asm that "rewrites" them, placed after the wait.
+MLA_DEVI void reg_fence16(uint32_t* r) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+               "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+               "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+MLA_DEVI void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+MLA_DEVI void reg_fence8(uint32_t* r) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+               "+r"(r[6]), "+r"(r[7]));
 }
 MLA_DEVI void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
