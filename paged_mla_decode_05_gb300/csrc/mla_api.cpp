@@ -365,31 +365,33 @@ void free_plan(mla_plan_s* p) {
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 // Tensor maps of the cache at kv_cache, kept in the plan until the cache
-// pointer or pool size changes. The cache is viewed as a 3-D tensor
-// {64 columns, rows, 9 panels} with a row stride of 1152 B and a panel stride
-// of 128 B, so one box brings a run of rows across several panels and lands
-// as [panel][row][128 B] (128-byte swizzle, zero fill outside the pool).
-// Boxes: 16 or min(block_size, 32) rows; 9 panels (K: all 576 columns) or 4
+// pointer or pool size changes. The cache is viewed as a 4-D tensor
+// {64 columns, 8 rows, 9 panels, row groups of 8} with strides of 1152 B
+// (row), 128 B (panel) and 9216 B (row group), so one box brings a run of
+// 16 or 32 rows across several panels and lands as [row group][panel]
+// [8 rows][128 B] (128-byte swizzle, zero fill outside the pool). Boxes:
+// 2 or min(block_size, 32)/8 row groups; 9 panels (K: all 576 columns) or 4
 // panels (one half of V).
 mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_blocks) {
   if (p->tmap_ptr == kv_cache && p->tmap_blocks == num_blocks) return MLA_OK;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return MLA_ERR_CUDA;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(mla::kPanelCols),
-                              static_cast<cuuint64_t>(num_blocks) * p->block_size,
-                              static_cast<cuuint64_t>(mla::kNumPanels)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(mla::kD) * 2,
-                                 static_cast<cuuint64_t>(mla::kPanelCols) * 2};
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(mla::kPanelCols), 8,
+                              static_cast<cuuint64_t>(mla::kNumPanels),
+                              static_cast<cuuint64_t>(num_blocks) * p->block_size / 8};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(mla::kD) * 2,
+                                 static_cast<cuuint64_t>(mla::kPanelCols) * 2,
+                                 static_cast<cuuint64_t>(mla::kD) * 2 * 8};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUtensorMap* maps[4] = {&p->tmap_k16, &p->tmap_k32, &p->tmap_v16, &p->tmap_v32};
   const int large = std::min(p->block_size, mla::kRowsLargeBox);
-  const int heights[4] = {mla::kRowsSmallBox, large, mla::kRowsSmallBox, large};
+  const int groups[4] = {mla::kRowsSmallBox / 8, large / 8, mla::kRowsSmallBox / 8, large / 8};
   const int panels[4] = {mla::kNumPanels, mla::kNumPanels, mla::kVHalfPanels, mla::kVHalfPanels};
   for (int i = 0; i < 4; ++i) {
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(mla::kPanelCols),
-                               static_cast<cuuint32_t>(heights[i]),
-                               static_cast<cuuint32_t>(panels[i])};
-    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv_cache), dims,
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(mla::kPanelCols), 8,
+                               static_cast<cuuint32_t>(panels[i]),
+                               static_cast<cuuint32_t>(groups[i])};
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), dims,
             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       p->tmap_ptr = nullptr;

@@ -14,17 +14,19 @@
 // one 2-CTA cluster per work list, with split roles, because the fp32 output
 // accumulator of 128 heads x 512 columns fills a whole SM's tensor memory:
 //  * score CTA (cluster rank 0): streams 80-token KV tiles (all 576 columns)
-//    into two 90 KB shared-memory stages, one 3-D TMA box per page piece (a
+//    into two 90 KB shared-memory stages, one 4-D TMA box per page piece (a
 //    page-aligned run of 32 or 16 rows across all 9 panels; per-SM TMA cost
-//    is per box, so few large boxes keep up with HBM), keeps Q [128 heads x
-//    576] in tensor memory, and computes S = Q.K^T with tcgen05 (M = 128
-//    heads, N = the piece's rows, A from tensor memory) from three issuer
-//    threads, one per piece. The fp32 online softmax (one thread per head
-//    row, one pass per tile with a lazy rescale) stages P (bf16) and the
-//    per-row rescale record in shared memory and ships each tile to the
-//    output CTA with one bulk copy into its shared memory.
+//    is per box, so few large boxes keep up with HBM). The 4-D view lands
+//    every 8-row swizzle atom of the tile at a fixed offset whichever page it
+//    came from, so one MMA can span the whole tile. Q [128 heads x 576] stays
+//    in tensor memory; S = Q.K^T runs on tcgen05 (M = 128 heads, A from
+//    tensor memory) from two issuer threads, each taking part of the tile's
+//    rows. The fp32 online softmax (one thread per head row, one pass per
+//    tile with a lazy rescale) stages P (bf16) and the per-row rescale record
+//    in shared memory and ships each tile to the output CTA with one bulk
+//    copy into its shared memory.
 //  * output CTA (rank 1): holds O [128 x 512] fp32 in tensor memory, streams
-//    V half-tiles (256 columns) into a 4-slot ring with 3-D TMA boxes (L2
+//    V half-tiles (256 columns) into a 4-slot ring with 4-D TMA boxes (L2
 //    hits: the score CTA just read the same lines), issues O += P.V with
 //    tcgen05 (N = 256), applies the rescale when the softmax max moved, and
 //    writes the normalised output.
@@ -38,16 +40,18 @@
 namespace mla {
 namespace {
 
-constexpr int kScoreIssuers = 3;   // score MMA issuer threads (warps 1, 6, 7 of the score CTA)
+constexpr int kScoreIssuers = 2;   // score MMA issuer threads (warps 1 and 6 of the score CTA)
+constexpr int kSplitRows = 48;      // issuer 0: tile rows [0, 48); issuer 1: [48, 80)
+constexpr int kQPrefetchLead = 4;   // tiles before an item's end: L2 prefetch of the next Q
 
 // Control block: identical offsets in both CTAs of the pair, so a barrier can
 // be addressed in the peer by offset (mapa, multicast commit).
 struct Ctrl {
-  uint64_t kv_full[kNumStages * kMaxPieces];    // score: piece of a stage landed (TMA bytes)
-  uint64_t kv_empty[kNumStages * kMaxPieces];   // score: S MMAs done reading the piece
+  uint64_t kv_full[kNumStages];   // score: all pieces of a stage landed (TMA bytes)
+  uint64_t kv_empty[kNumStages];  // score: S MMAs done reading the stage (one arrival per issuer)
   uint64_t s_full[2];             // score: S tile in tensor memory
   uint64_t s_free[2];             // score: softmax copied S out
-  uint64_t q_ready;               // score: Q of the next item in tensor memory
+  uint64_t q_ready[3];            // score: Q of the next item in tensor memory, per 96 columns
   uint64_t p_empty[kNumPBufs];    // score: peer finished P.V on its P buffer k
   uint64_t v_full[kNumVSlots];    // output: V half landed
   uint64_t v_empty[kNumVSlots];   // output: P.V done reading the V half
@@ -60,8 +64,8 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
-constexpr uint32_t kIdescS32 = idesc_bf16_f32(128, kRowsLargeBox, 0, 0);  // K-major A and B
-constexpr uint32_t kIdescS16 = idesc_bf16_f32(128, kRowsSmallBox, 0, 0);
+constexpr uint32_t kIdescSLo = idesc_bf16_f32(128, kSplitRows, 0, 0);          // K-major A and B
+constexpr uint32_t kIdescSHi = idesc_bf16_f32(128, kTile - kSplitRows, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);    // V is MN-major
 constexpr float kRescaleThreshold = 8.0f;                        // log2 units
 constexpr uint32_t kFullMask = 0xffffffffu;
@@ -162,27 +166,6 @@ MLA_DEVI int cache_row(const DecodeParams& p, const WorkItem& w, int t, const Pa
   return (blk << sh) + (t & (p.block_size - 1));
 }
 
-// The piece holding tile row kr (a multiple of 16): its first row and height.
-MLA_DEVI void piece_of_row(int block_size, int tile_t0, int kr, int& r0, int& rows) {
-  if (block_size < kRowsLargeBox) {
-    r0 = kr & ~15;
-    rows = kRowsSmallBox;
-  } else if ((tile_t0 & 31) == 0) {
-    r0 = kr < 64 ? (kr & ~31) : 64;
-    rows = kr < 64 ? kRowsLargeBox : kRowsSmallBox;
-  } else {
-    r0 = kr < 16 ? 0 : 16 + ((kr - 16) & ~31);
-    rows = kr < 16 ? kRowsSmallBox : kRowsLargeBox;
-  }
-}
-
-// Index of the piece holding tile row kr (any row) in the tile starting at tile_t0.
-MLA_DEVI int piece_index_of_row(int block_size, int tile_t0, int kr) {
-  if (block_size < kRowsLargeBox) return kr >> 4;
-  if ((tile_t0 & 31) == 0) return kr < 64 ? (kr >> 5) : 2;
-  return kr < 16 ? 0 : 1 + ((kr - 16) >> 5);
-}
-
 // Lane 0 waits on a barrier; the whole warp learns the outcome.
 MLA_DEVI bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
   bool ok = true;
@@ -192,68 +175,57 @@ MLA_DEVI bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
 
 // ------------------------------------------------------------ score CTA roles
 
-// TMA producer warp: each 80-token tile into stage g % 2 as one 3-D box per
-// piece (all 9 panels), lane j loading piece j, each piece on its own
-// barrier. A stage holds piece j of the tile at r0_j * 1152 B as
-// [panel][rows][128 B]; consecutive tiles may be cut into pieces differently
-// (a tile's cut depends on its first token modulo 32), so before a piece
-// overwrites its rows the lane waits until the S MMAs are done with the old
-// piece holding the new piece's last row (they finish pieces in order).
+// TMA producer warp: each 80-token tile into stage g % 2, one 4-D box per
+// page piece (all 9 panels), lane j loading piece j. The stage layout
+// [row group][panel][8 rows][128 B] does not depend on how the tile is cut
+// into pieces; one barrier per stage counts the bytes of all pieces.
 MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int lane, int it0,
                              int it1) {
   uint32_t err = 0;
   const uint64_t policy = policy_evict_normal();
   int g = 0;
   bool ok = true;
-  int prev_t0_even = 0, prev_t0_odd = 0;   // first token of the tile each stage last held
-  static_assert(kNumStages == 2, "one previous-tile record per stage");
   const int n = pieces_per_tile(p.block_size);
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
-    if (lane == 0) {
-      if (__ldg(&p.seq_lens[w.b]) != w.seq_len) err |= 2u;  // MLA_DEVERR_SEQLEN_MISMATCH
-      // Warm L2 with the Q rows of the next non-empty item.
-      for (int nx = it + 1; nx < it1; ++nx) {
-        const WorkItem wn = p.items[nx];
-        if (tiles_of(wn) == 0) continue;
-        const uint16_t* qn = p.q_nope + static_cast<int64_t>(wn.b) * p.H * kDc;
-        const uint16_t* qp = p.q_pe + static_cast<int64_t>(wn.b) * p.H * kDr;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qn), "r"(p.H * kDc * 2) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qp), "r"(p.H * kDr * 2) : "memory");
-        break;
-      }
-    }
+    if (lane == 0 && __ldg(&p.seq_lens[w.b]) != w.seq_len) err |= 2u;  // MLA_DEVERR_SEQLEN_MISMATCH
     PageWindow win;
     const int nt = tiles_of(w);
     for (int i = 0; i < nt && ok; ++i, ++g) {
+      // Warm L2 with the Q rows of the next non-empty item a few tiles before
+      // they are loaded (earlier, the streaming cache would evict them).
+      if (lane == 0 && i == max(nt - kQPrefetchLead, 0)) {
+        for (int nx = it + 1; nx < it1; ++nx) {
+          const WorkItem wn = p.items[nx];
+          if (tiles_of(wn) == 0) continue;
+          const uint16_t* qn = p.q_nope + static_cast<int64_t>(wn.b) * p.H * kDc;
+          const uint16_t* qp = p.q_pe + static_cast<int64_t>(wn.b) * p.H * kDr;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qn), "r"(p.H * kDc * 2) : "memory");
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qp), "r"(p.H * kDr * 2) : "memory");
+          break;
+        }
+      }
       const int s = g & 1;
       const int tile_t0 = w.t0 + i * kTile;
       int r0, large;
       piece_shape(p.block_size, tile_t0, lane < n ? lane : 0, r0, large);
       window_cover(p, w, tile_t0, win, lane);
-      const int y = cache_row(p, w, tile_t0 + r0, win, err);
-      const int rows = large ? kRowsLargeBox : kRowsSmallBox;
+      const int y = cache_row(p, w, tile_t0 + r0, win, err);   // a multiple of 8
       MLA_TRACE_AT(0, g);
-      bool good = true;
-      if (lane < n) {
-        if (g >= kNumStages) {
-          const int jw = piece_index_of_row(p.block_size, s ? prev_t0_odd : prev_t0_even,
-                                            r0 + rows - 1);
-          good = mbar_wait(smem_addr(&c->kv_empty[s * kMaxPieces + jw]), ((g >> 1) - 1) & 1);
-        }
-        if (good) {
-          const uint32_t full = smem_addr(&c->kv_full[s * kMaxPieces + lane]);
-          mbar_arrive_expect_tx(full, rows * kD * 2);
-          tma_load_3d(smem_addr(data + s * kStageBytes + r0 * (kD * 2)),
-                      large ? static_cast<const void*>(&p.tmap_k32)
-                            : static_cast<const void*>(&p.tmap_k16),
-                      0, y, 0, full, policy);
-        }
-        if (lane == 0) MLA_TRACE_AT(26, g);
+      if (g >= kNumStages &&
+          !warp_wait(smem_addr(&c->kv_empty[s]), ((g >> 1) - 1) & 1, lane)) {
+        ok = false;
+        break;
       }
-      if (s) prev_t0_odd = tile_t0;
-      else prev_t0_even = tile_t0;
-      if (!__all_sync(kFullMask, good)) ok = false;
+      const uint32_t full = smem_addr(&c->kv_full[s]);
+      if (lane == 0) mbar_arrive_expect_tx(full, kStageBytes);
+      __syncwarp();
+      if (lane < n)
+        tma_load_4d(smem_addr(data + s * kStageBytes + (r0 >> 3) * kKGroupBytes),
+                    large ? static_cast<const void*>(&p.tmap_k32)
+                          : static_cast<const void*>(&p.tmap_k16),
+                    0, 0, 0, y >> 3, full, policy);
+      if (lane == 0) MLA_TRACE_AT(26, g);
     }
   }
   if (!ok) err |= 4u;
@@ -261,60 +233,64 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
   if (lane == 0) report(p, err);
 }
 
-// S MMA issuers: S[g%2] = Q . K^T over the 576 columns, per piece (N = the
-// piece's 16 or 32 rows, written to the piece's own S columns; 36 k-steps of
-// 16). kScoreIssuers threads in different warps each take the pieces j with
-// j % kScoreIssuers == m: one thread issues at most one MMA every ~50 cycles,
-// so small-N MMAs from a single thread would leave the tensor pipe idle. Each
-// issuer commits its own MMAs: kv_empty of its pieces, then s_full (which
-// counts one arrival per issuer).
+// S MMA issuers: S[g%2] = Q . K^T over the 576 columns (36 k-steps of 16).
+// The tile's 80 rows are split between two issuer threads in different warps
+// (rows 0-47, N = 48, and rows 48-79, N = 32), since one thread issues at
+// most one MMA every ~50 cycles. Each issuer commits its own MMAs: kv_empty
+// and s_full count one arrival per issuer.
 MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
                         int it1, int m) {
   int g = 0, n_items = 0;
   bool ok = true;
-  const int n = pieces_per_tile(p.block_size);
+  const int row0 = m == 0 ? 0 : kSplitRows;
+  const uint32_t idesc = m == 0 ? kIdescSLo : kIdescSHi;
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
     const int nt = tiles_of(w);
     if (nt == 0) continue;
-    if (!mbar_wait(smem_addr(&c->q_ready), n_items & 1)) { ok = false; break; }
+    const uint32_t q_par = n_items & 1;
     ++n_items;
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
       if (g >= 2 && !mbar_wait(smem_addr(&c->s_free[s]), ((g >> 1) - 1) & 1)) { ok = false; break; }
       if (m == 0) MLA_TRACE_AT(2, g);
-      const int tile_t0 = w.t0 + i * kTile;
-      const uint32_t stage = smem_addr(data + s * kStageBytes);
+      if (!mbar_wait(smem_addr(&c->kv_full[s]), (g >> 1) & 1)) { ok = false; break; }
+      if (m == 0) MLA_TRACE_AT(1, g);
+      tc_after_sync();
+      const uint32_t d = tmem + kTmemS0 + s * kTile + row0;
+      // Descriptor of panel 0 of the issuer's rows (8-row atoms kKGroupBytes
+      // apart); later k-steps only move the start-address field (low word,
+      // 16-byte units, never carries out): +1 KB per panel, +32 B per k-step.
+      const uint64_t bp =
+          smem_desc(smem_addr(data + s * kStageBytes + (row0 >> 3) * kKGroupBytes), 16, kKGroupBytes);
+      const uint32_t hi = static_cast<uint32_t>(bp >> 32);
+      uint32_t blo = static_cast<uint32_t>(bp);
+      uint32_t a = tmem + kTmemQ;
+      if (i == 0) {
+        // First tile of an item: its Q arrives in three groups of 3 panels.
 #pragma unroll 1
-      for (int j = m; j < n; j += kScoreIssuers) {
-        int r0, large;
-        piece_shape(p.block_size, tile_t0, j, r0, large);
-        const int slot = s * kMaxPieces + j;
-        if (!mbar_wait(smem_addr(&c->kv_full[slot]), (g >> 1) & 1)) { ok = false; break; }
-        if (m == 0 && j == 0) MLA_TRACE_AT(1, g);
-        if (m > 0 && j < kScoreIssuers) MLA_TRACE_AT(26 + 2 * m, g);
-        tc_after_sync();
-        const uint32_t d = tmem + kTmemS0 + s * kTile + r0;
-        const uint32_t idesc = large ? kIdescS32 : kIdescS16;
-        // Descriptor of the piece's first panel; later k-steps only move the
-        // start-address field (low word, 16-byte units, never carries out).
-        const uint64_t bp = smem_desc(stage + r0 * (kD * 2), 16, 1024);
-        const uint32_t lo = static_cast<uint32_t>(bp);
-        const uint32_t hi = static_cast<uint32_t>(bp >> 32);
-        const uint32_t panel_step = (large ? kRowsLargeBox : kRowsSmallBox) * 128 / 16;
-        uint32_t a = tmem + kTmemQ;
-        uint32_t blo = lo;
+        for (int pc = 0; pc < kNumPanels; ++pc, a += 32, blo += kAtomBytes / 16) {
+          if (pc % 3 == 0) {
+            if (!mbar_wait(smem_addr(&c->q_ready[pc / 3]), q_par)) { ok = false; break; }
+            tc_after_sync();
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            mma_ts(d, a + q * 8, (static_cast<uint64_t>(hi) << 32) | (blo + q * 2), idesc,
+                   (pc > 0 || q > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+      } else {
 #pragma unroll 1
-        for (int pc = 0; pc < kNumPanels; ++pc, a += 32, blo += panel_step) {
+        for (int pc = 0; pc < kNumPanels; ++pc, a += 32, blo += kAtomBytes / 16) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)   // 32 bytes per k-step inside the 128-byte swizzle row
             mma_ts(d, a + q * 8, (static_cast<uint64_t>(hi) << 32) | (blo + q * 2), idesc,
                    (pc > 0 || q > 0) ? 1u : 0u);
         }
-        if (j < kScoreIssuers) MLA_TRACE_AT(m == 0 ? 24 : 27 + 2 * m, g);
-        tc_commit(smem_addr(&c->kv_empty[slot]));
       }
-      if (!ok) break;
+      if (m == 0) MLA_TRACE_AT(24, g);
+      tc_commit(smem_addr(&c->kv_empty[s]));
       tc_commit(smem_addr(&c->s_full[s]));
       if (m == 0) MLA_TRACE_AT(3, g);
     }
@@ -324,10 +300,14 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
 
 // Load Q rows of request b into tensor memory columns [0, 288): lane = head,
 // two bf16 per column. Rows at or past H are zero (in-kernel head padding).
-__device__ __noinline__ void load_q(const DecodeParams& p, int b, int row, uint32_t trow) {
+__device__ __noinline__ void load_q(const DecodeParams& p, Ctrl* c, int b, int row,
+                                    uint32_t trow) {
   const bool valid = row < p.H;
   const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<int64_t>(b) * p.H + row) * kDc);
   const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + (static_cast<int64_t>(b) * p.H + row) * kDr);
+  // Three groups of 3 panels (96 columns), each announced on its own barrier:
+  // the S MMAs of the item's first tile start on the first panels while the
+  // later groups are still loading.
 #pragma unroll
   for (int grp = 0; grp < 3; ++grp) {
     uint4 v[3][8];
@@ -350,8 +330,10 @@ __device__ __noinline__ void load_q(const DecodeParams& p, int b, int row, uint3
       }
       tmem_st32(trow + kTmemQ + (grp * 3 + j) * 32, r);
     }
+    tmem_wait_st();
+    tc_before_sync();
+    mbar_arrive(smem_addr(&c->q_ready[grp]));
   }
-  tmem_wait_st();
 }
 
 // Softmax warps: one thread per head row (TMEM lane). Two compact passes over
@@ -378,9 +360,7 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
   int cur = it0;
   while (cur < it1 && tiles_of(p.items[cur]) == 0) ++cur;
   if (cur < it1) {
-    load_q(p, p.items[cur].b, row, trow);
-    tc_before_sync();
-    mbar_arrive(smem_addr(&c->q_ready));
+    load_q(p, c, p.items[cur].b, row, trow);
   }
   while (cur < it1 && ok) {
     const WorkItem w = p.items[cur];
@@ -408,6 +388,12 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
         break;
       }
       tc_after_sync();
+      if (i == nt - 1 && nxt < it1) {
+        // The item's last S tile is complete, so Q's columns are free: load
+        // the next item's Q now, letting its first S MMAs run while this
+        // tile's softmax is computed.
+        load_q(p, c, p.items[nxt].b, row, trow);
+      }
       uint8_t* st = staging + k * kPBufBytes;
       // p = 2^(s*scale*log2e - m) with the running maximum m, row sum, bf16
       // pack into the staging tile (one 16-byte core-matrix row per 8
@@ -476,12 +462,6 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
         rec[kMaxHeads + row] = l;
         rec[2 * kMaxHeads + row] = m_used;
       }
-      if (i == nt - 1 && nxt < it1) {
-        // All S MMAs of this item are complete: Q's columns are free.
-        load_q(p, p.items[nxt].b, row, trow);
-        tc_before_sync();
-        mbar_arrive(smem_addr(&c->q_ready));
-      }
       fence_proxy_async_smem();
       named_barrier_sync(1, 128);
       if (row == 0) MLA_TRACE_AT(5, g);
@@ -549,10 +529,10 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
         __syncwarp();
         // One warp instruction: lane j loads piece j (4 panels of this half).
         if (lane < n) {
-          tma_load_3d(smem_addr(data + v * kVHalfBytes) + r0 * (kVHalfPanels * 128),
+          tma_load_4d(smem_addr(data + v * kVHalfBytes) + (r0 >> 3) * kVGroupBytes,
                       large ? static_cast<const void*>(&p.tmap_v32)
                             : static_cast<const void*>(&p.tmap_v16),
-                      0, y, half * kVHalfPanels, full, policy);
+                      0, 0, half * kVHalfPanels, y >> 3, full, policy);
         }
       }
     }
@@ -619,7 +599,6 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
     const int nt = tiles_of(w);
     for (int i = 0; i < nt; ++i, ++g) {
       const int k = g & 1;
-      const int tile_t0 = w.t0 + i * kTile;
       if (!mbar_wait(smem_addr(&c->o_ready[g & 1]), (g >> 1) & 1)) { ok = false; break; }
       MLA_TRACE_AT(10, g);
       tc_after_sync();
@@ -635,16 +614,14 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
         if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
         MLA_TRACE_AT(11 + half, g);
         tc_after_sync();
-        // V half: MN-major, 128-byte swizzle; the 16 tokens of k-step kk lie
-        // in one piece, whose panels are (piece rows x 128 B) apart.
-        const uint32_t vs = smem_addr(data + v * kVHalfBytes);
+        // V half: MN-major, 128-byte swizzle; 64-column panels 1 KB apart
+        // (LBO), 8-token row groups kVGroupBytes apart (SBO); a k-step of 16
+        // tokens is two row groups.
+        const uint64_t b0 = smem_desc(smem_addr(data + v * kVHalfBytes), kAtomBytes, kVGroupBytes);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          int r0, rows;
-          piece_of_row(p.block_size, tile_t0, kk * 16, r0, rows);
           const uint64_t ad = a0 + static_cast<uint64_t>((kk * 256) >> 4);
-          const uint64_t bd = smem_desc(vs + r0 * (kVHalfPanels * 128) + (kk * 16 - r0) * 128,
-                                        rows * 128, 1024);
+          const uint64_t bd = b0 + static_cast<uint64_t>((kk * 2 * kVGroupBytes) >> 4);
           mma_ss(tmem + half * 256, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_addr(&c->v_empty[v]));
@@ -779,9 +756,9 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNumStages * kMaxPieces; ++s) {
+    for (int s = 0; s < kNumStages; ++s) {
       mbar_init(smem_addr(&c->kv_full[s]), 1);
-      mbar_init(smem_addr(&c->kv_empty[s]), 1);
+      mbar_init(smem_addr(&c->kv_empty[s]), kScoreIssuers);
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(smem_addr(&c->s_full[j]), kScoreIssuers);
@@ -789,7 +766,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->o_ready[j]), 128);
       mbar_init(smem_addr(&c->o_done[j]), 1);
     }
-    mbar_init(smem_addr(&c->q_ready), 128);
+    for (int j = 0; j < 3; ++j) mbar_init(smem_addr(&c->q_ready[j]), 128);
     for (int k = 0; k < kNumPBufs; ++k) {
       mbar_init(smem_addr(&c->p_empty[k]), 1);
       mbar_init(smem_addr(&c->p_full[k]), 1);
@@ -830,9 +807,9 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   if (rank == 0) {
     if (warp == 0) {
       score_producer(p, c, data, lane, it0, it1);
-    } else if (warp == 1 || warp >= 6) {
-      if (lane == 0) score_mma(p, c, data, tmem, it0, it1, warp == 1 ? 0 : warp - 5);
-    } else {
+    } else if (warp == 1 || warp == 6) {
+      if (lane == 0) score_mma(p, c, data, tmem, it0, it1, warp == 1 ? 0 : 1);
+    } else if (warp < 6) {
       score_softmax(p, c, data, tmem, warp, lane, it0, it1);
     }
   } else {

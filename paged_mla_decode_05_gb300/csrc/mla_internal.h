@@ -20,13 +20,15 @@ constexpr int kMaxPieces = kTile / kRowsSmallBox;      // at most 5 boxes per pa
 constexpr int kPanelCols = 64;           // bf16 columns of one 128-byte swizzle panel
 constexpr int kNumPanels = kD / kPanelCols;            // 9 panels per row
 constexpr int kPanelBytes = kTile * 128;               // one panel of one tile: 10 KB
-// Score stage: the piece of rows r0.. of the tile at r0 * 1152 B, laid out as
-// [9 panels][rows of the piece][128 B].
+// Score stage: [row group (10)][panel (9)][8 rows][128 B]; 8-row atoms are
+// kKGroupBytes apart along the rows and 1 KB apart along the panels.
 constexpr int kStageBytes = kNumPanels * kPanelBytes;  // full 576-wide tile: 90 KB
 constexpr int kVHalfPanels = 4;                        // V half = 256 columns
-// V half slot: the piece of rows r0.. of the tile at r0 * 512 B, laid out as
-// [4 panels][rows of the piece][128 B].
+// V half slot: [row group (10)][panel (4)][8 rows][128 B].
 constexpr int kVHalfBytes = kVHalfPanels * kPanelBytes;  // 40 KB
+constexpr int kAtomBytes = 8 * 128;                      // 8 rows x 128 B (one swizzle atom)
+constexpr int kKGroupBytes = kNumPanels * kAtomBytes;    // 9216: row-group stride of a stage
+constexpr int kVGroupBytes = kVHalfPanels * kAtomBytes;  // 4096: row-group stride of a V slot
 constexpr int kNumStages = 2;            // score CTA: KV tiles in flight
 constexpr int kNumVSlots = 4;            // output CTA: V half-tiles in flight
 constexpr int kNumPBufs = 2;             // P tiles in flight (staging and peer buffers)
@@ -73,14 +75,16 @@ struct CombineItem {
 };
 
 struct DecodeParams {
-  // 3-D views of the cache {64 columns, num_blocks*block_size rows, 9 panels}
-  // (row stride 1152 B, panel stride 128 B): one box brings a page-aligned
-  // run of 16 or 32 rows across several 64-column panels, landing in shared
-  // memory as [panel][row][128 B] with the 128-byte swizzle.
-  CUtensorMap tmap_k16;           // box {64, 16, 9}: all 576 columns
-  CUtensorMap tmap_k32;           // box {64, 32, 9} (block_size >= 32)
-  CUtensorMap tmap_v16;           // box {64, 16, 4}: one 256-column half of V
-  CUtensorMap tmap_v32;           // box {64, 32, 4} (block_size >= 32)
+  // 4-D views of the cache {64 columns, 8 rows, 9 panels, row groups of 8}
+  // (strides: row 1152 B, panel 128 B, row group 9216 B). One box brings a
+  // page-aligned run of 16 or 32 rows (2 or 4 row groups) across several
+  // 64-column panels and lands in shared memory as [row group][panel][8 rows]
+  // [128 B] with the 128-byte swizzle: every 8-row x 128-byte atom of a tile
+  // sits at (row group * panels + panel) * 1 KB, whichever page it came from.
+  CUtensorMap tmap_k16;           // box {64, 8, 9, 2}: all 576 columns
+  CUtensorMap tmap_k32;           // box {64, 8, 9, 4} (block_size >= 32)
+  CUtensorMap tmap_v16;           // box {64, 8, 4, 2}: one 256-column half of V
+  CUtensorMap tmap_v32;           // box {64, 8, 4, 4} (block_size >= 32)
   const void* kv_cache;           // the cache itself, for L2 line prefetches
   const uint16_t* q_nope;         // [B, H, 512]
   const uint16_t* q_pe;           // [B, H, 64]

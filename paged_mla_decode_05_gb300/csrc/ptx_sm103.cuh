@@ -158,6 +158,14 @@ MLA_DEVI void tma_load_2d_multicast(uint32_t dst, const void* tmap, int x, int y
       ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(policy) : "memory");
 }
+// 4-D tiled TMA load (coordinates innermost first), completion on `bar`.
+MLA_DEVI void tma_load_4d(uint32_t dst, const void* tmap, int x, int y, int z, int w,
+                          uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy) : "memory");
+}
 MLA_DEVI uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
