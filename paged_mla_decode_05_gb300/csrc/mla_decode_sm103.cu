@@ -336,11 +336,44 @@ __device__ __noinline__ void load_q(const DecodeParams& p, Ctrl* c, int b, int r
   }
 }
 
-// Softmax warps: one thread per head row (TMEM lane). Two compact passes over
-// the S tile in 16-column chunks (row max, then exp/sum/pack) keep the code
-// small: several warp roles share each sub-partition's instruction cache.
-// P goes straight into a staging buffer; one elected thread ships the tile to
-// the peer with a bulk copy.
+// 40 columns of one S row (registers r) -> p = 2^(s*scale*log2e - m) into
+// the staging tile (5 core-matrix rows of 16 bytes at st_row + q*128), with
+// the running row sums ls0/ls1 and maxima mx0/mx1 of the raw scores. MASKED
+// treats columns at or past vh (the item's end) as -inf: only an item's tail
+// tile needs it.
+template <bool MASKED>
+MLA_DEVI void softmax_half(const uint32_t (&r)[40], int vh, float sl2, float m_used, bool active,
+                           uint8_t* st_row, float& ls0, float& ls1, float& mx0, float& mx1) {
+#pragma unroll
+  for (int q = 0; q < 5; ++q) {
+    uint32_t pk[4];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const int cc = 8 * q + j;
+      float s0 = __uint_as_float(r[cc]);
+      float s1 = __uint_as_float(r[cc + 1]);
+      if (MASKED) {
+        s0 = cc < vh ? s0 : -INFINITY;
+        s1 = cc + 1 < vh ? s1 : -INFINITY;
+      }
+      mx0 = fmaxf(mx0, s0);
+      mx1 = fmaxf(mx1, s1);
+      const float e0 = fast_exp2(fmaf(s0, sl2, -m_used));
+      const float e1 = fast_exp2(fmaf(s1, sl2, -m_used));
+      ls0 += e0;
+      ls1 += e1;
+      pk[j / 2] = pack_bf16x2(e0, e1);
+    }
+    if (active)
+      *reinterpret_cast<uint4*>(st_row + q * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+// Softmax warps: one thread per head row (TMEM lane), one pass per tile in the
+// steady state (see below); rolled loops keep the code small, since several
+// warp roles share each sub-partition's instruction cache. P goes straight
+// into a staging buffer that one elected thread ships to the peer with a bulk
+// copy.
 MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem,
                             int warp, int lane, int it0, int it1) {
   const int row = (warp & 3) * 32 + lane;
@@ -380,64 +413,55 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       if (row == 0) MLA_TRACE_AT(4, g);
       float alpha = 1.0f;
       if (row == 0) MLA_TRACE_AT(16, g);
+      tc_after_sync();
+      // The first 40 columns start loading before the staging buffer is known
+      // to be free (the load does not touch it).
+      uint32_t r[40];
+      tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+      tmem_ld8(scol + 32, &r[32]);
       // Stage P(g) in buffer k once the copy that last read it (tile g-2) is done.
       if (elected && g >= kNumPBufs) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
       named_barrier_sync(1, 128);
       if (c->abort_flag) {
+        tmem_wait_ld();
         ok = false;
         break;
       }
-      tc_after_sync();
       if (i == nt - 1 && nxt < it1) {
         // The item's last S tile is complete, so Q's columns are free: load
         // the next item's Q now, letting its first S MMAs run while this
         // tile's softmax is computed.
+        tmem_wait_ld();
         load_q(p, c, p.items[nxt].b, row, trow);
       }
       uint8_t* st = staging + k * kPBufBytes;
       // p = 2^(s*scale*log2e - m) with the running maximum m, row sum, bf16
-      // pack into the staging tile (one 16-byte core-matrix row per 8
-      // columns); the tile's own maximum is tracked on the way. If it lies
-      // more than kRescaleThreshold above m for some row (always on an
-      // item's first tile, rarely after), the warp redoes the tile with the
-      // new maximum. S is read in two halves of 40 columns, one batched load
-      // and one wait each, in rolled loops: compact code.
+      // pack into the staging tile; the tile's own maximum is tracked on the
+      // way. If it lies more than kRescaleThreshold above m for some row
+      // (always on an item's first tile, rarely after), the warp redoes the
+      // tile with the new maximum. S is read in two halves of 40 columns, one
+      // batched load and one wait each, in rolled loops: compact code.
       float ls0, ls1;
 #pragma unroll 1
-      while (true) {
+      for (int attempt = 0;; ++attempt) {
         ls0 = 0.0f;
         ls1 = 0.0f;
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
-          uint32_t r[40];
-          tmem_ld32(scol + hh * 40, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-          tmem_ld8(scol + hh * 40 + 32, &r[32]);
+          if (attempt > 0 || hh > 0) {
+            tmem_ld32(scol + hh * 40, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+            tmem_ld8(scol + hh * 40 + 32, &r[32]);
+          }
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 40; j += 8) reg_fence8(&r[j]);
           if (row == 0) MLA_TRACE_AT(18 + 2 * hh, g);
-          const int vh = valid - hh * 40;
-#pragma unroll
-          for (int q = 0; q < 5; ++q) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-              const int cc = 8 * q + j;
-              const float s0 = cc < vh ? __uint_as_float(r[cc]) : -INFINITY;
-              const float s1 = cc + 1 < vh ? __uint_as_float(r[cc + 1]) : -INFINITY;
-              mx0 = fmaxf(mx0, s0);
-              mx1 = fmaxf(mx1, s1);
-              const float e0 = fast_exp2(fmaf(s0, sl2, -m_used));
-              const float e1 = fast_exp2(fmaf(s1, sl2, -m_used));
-              ls0 += e0;
-              ls1 += e1;
-              pk[j / 2] = pack_bf16x2(e0, e1);
-            }
-            if (active)
-              *reinterpret_cast<uint4*>(st + prow_off + (hh * 5 + q) * 128) =
-                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
+          uint8_t* st_row = st + prow_off + hh * 5 * 128;
+          if (valid == kTile)
+            softmax_half<false>(r, 40, sl2, m_used, active, st_row, ls0, ls1, mx0, mx1);
+          else
+            softmax_half<true>(r, valid - hh * 40, sl2, m_used, active, st_row, ls0, ls1, mx0, mx1);
           if (row == 0) MLA_TRACE_AT(19 + 2 * hh, g);
         }
         const float m_tile = fmaxf(mx0, mx1) * sl2;
