@@ -40,15 +40,13 @@
 namespace mla {
 namespace {
 
-constexpr int kScoreIssuers = 2;   // score MMA issuer threads (warps 1 and 6 of the score CTA)
-constexpr int kSplitRows = 48;      // issuer 0: tile rows [0, 48); issuer 1: [48, 80)
 constexpr int kQPrefetchLead = 4;   // tiles before an item's end: L2 prefetch of the next Q
 
 // Control block: identical offsets in both CTAs of the pair, so a barrier can
 // be addressed in the peer by offset (mapa, multicast commit).
 struct Ctrl {
   uint64_t kv_full[kNumStages];   // score: all pieces of a stage landed (TMA bytes)
-  uint64_t kv_empty[kNumStages];  // score: S MMAs done reading the stage (one arrival per issuer)
+  uint64_t kv_empty[kNumStages];  // score: S MMAs done reading the stage
   uint64_t s_full[2];             // score: S tile in tensor memory
   uint64_t s_free[2];             // score: softmax copied S out
   uint64_t q_ready[3];            // score: Q of the next item in tensor memory, per 96 columns
@@ -64,8 +62,7 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
-constexpr uint32_t kIdescSLo = idesc_bf16_f32(128, kSplitRows, 0, 0);          // K-major A and B
-constexpr uint32_t kIdescSHi = idesc_bf16_f32(128, kTile - kSplitRows, 0, 0);
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTile, 0, 0);   // K-major A and B
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);    // V is MN-major
 constexpr float kRescaleThreshold = 8.0f;                        // log2 units
 constexpr uint32_t kFullMask = 0xffffffffu;
@@ -233,17 +230,15 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
   if (lane == 0) report(p, err);
 }
 
-// S MMA issuers: S[g%2] = Q . K^T over the 576 columns (36 k-steps of 16).
-// The tile's 80 rows are split between two issuer threads in different warps
-// (rows 0-47, N = 48, and rows 48-79, N = 32), since one thread issues at
-// most one MMA every ~50 cycles. Each issuer commits its own MMAs: kv_empty
-// and s_full count one arrival per issuer.
+// S MMA issuer: S[g%2] = Q . K^T over the 576 columns, 36 k-steps of 16 with
+// N = 80 (the whole tile: its 8-row atoms are kKGroupBytes apart in the
+// stage whichever pages they came from). The steady-state loop is fully
+// unrolled: one thread issues one MMA every ~50 cycles at best.
 MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
-                        int it1, int m) {
+                        int it1) {
   int g = 0, n_items = 0;
   bool ok = true;
-  const int row0 = m == 0 ? 0 : kSplitRows;
-  const uint32_t idesc = m == 0 ? kIdescSLo : kIdescSHi;
+  constexpr uint32_t idesc = kIdescS;
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
     const int nt = tiles_of(w);
@@ -253,16 +248,15 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
       if (g >= 2 && !mbar_wait(smem_addr(&c->s_free[s]), ((g >> 1) - 1) & 1)) { ok = false; break; }
-      if (m == 0) MLA_TRACE_AT(2, g);
+      MLA_TRACE_AT(2, g);
       if (!mbar_wait(smem_addr(&c->kv_full[s]), (g >> 1) & 1)) { ok = false; break; }
-      if (m == 0) MLA_TRACE_AT(1, g);
+      MLA_TRACE_AT(1, g);
       tc_after_sync();
-      const uint32_t d = tmem + kTmemS0 + s * kTile + row0;
-      // Descriptor of panel 0 of the issuer's rows (8-row atoms kKGroupBytes
-      // apart); later k-steps only move the start-address field (low word,
-      // 16-byte units, never carries out): +1 KB per panel, +32 B per k-step.
-      const uint64_t bp =
-          smem_desc(smem_addr(data + s * kStageBytes + (row0 >> 3) * kKGroupBytes), 16, kKGroupBytes);
+      const uint32_t d = tmem + kTmemS0 + s * kTile;
+      // Descriptor of panel 0 (8-row atoms kKGroupBytes apart); later k-steps
+      // only move the start-address field (low word, 16-byte units, never
+      // carries out): +1 KB per panel, +32 B per k-step.
+      const uint64_t bp = smem_desc(smem_addr(data + s * kStageBytes), 16, kKGroupBytes);
       const uint32_t hi = static_cast<uint32_t>(bp >> 32);
       uint32_t blo = static_cast<uint32_t>(bp);
       uint32_t a = tmem + kTmemQ;
@@ -281,18 +275,16 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
         }
         if (!ok) break;
       } else {
-#pragma unroll 1
-        for (int pc = 0; pc < kNumPanels; ++pc, a += 32, blo += kAtomBytes / 16) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)   // 32 bytes per k-step inside the 128-byte swizzle row
-            mma_ts(d, a + q * 8, (static_cast<uint64_t>(hi) << 32) | (blo + q * 2), idesc,
-                   (pc > 0 || q > 0) ? 1u : 0u);
-        }
+        for (int kq = 0; kq < kNumPanels * 4; ++kq)   // panel kq/4, 32 bytes per k-step
+          mma_ts(d, a + kq * 8,
+                 (static_cast<uint64_t>(hi) << 32) | (blo + (kq >> 2) * (kAtomBytes / 16) + (kq & 3) * 2),
+                 idesc, kq > 0 ? 1u : 0u);
       }
-      if (m == 0) MLA_TRACE_AT(24, g);
+      MLA_TRACE_AT(24, g);
       tc_commit(smem_addr(&c->kv_empty[s]));
       tc_commit(smem_addr(&c->s_full[s]));
-      if (m == 0) MLA_TRACE_AT(3, g);
+      MLA_TRACE_AT(3, g);
     }
   }
   if (!ok) report(p, 4u);
@@ -782,10 +774,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNumStages; ++s) {
       mbar_init(smem_addr(&c->kv_full[s]), 1);
-      mbar_init(smem_addr(&c->kv_empty[s]), kScoreIssuers);
+      mbar_init(smem_addr(&c->kv_empty[s]), 1);
     }
     for (int j = 0; j < 2; ++j) {
-      mbar_init(smem_addr(&c->s_full[j]), kScoreIssuers);
+      mbar_init(smem_addr(&c->s_full[j]), 1);
       mbar_init(smem_addr(&c->s_free[j]), 128);
       mbar_init(smem_addr(&c->o_ready[j]), 128);
       mbar_init(smem_addr(&c->o_done[j]), 1);
@@ -831,8 +823,8 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   if (rank == 0) {
     if (warp == 0) {
       score_producer(p, c, data, lane, it0, it1);
-    } else if (warp == 1 || warp == 6) {
-      if (lane == 0) score_mma(p, c, data, tmem, it0, it1, warp == 1 ? 0 : 1);
+    } else if (warp == 1) {
+      if (lane == 0) score_mma(p, c, data, tmem, it0, it1);
     } else if (warp < 6) {
       score_softmax(p, c, data, tmem, warp, lane, it0, it1);
     }
