@@ -330,35 +330,58 @@ __device__ __noinline__ void load_q(const DecodeParams& p, Ctrl* c, int b, int r
 
 // 40 columns of one S row (registers r) -> p = 2^(s*scale*log2e - m) into
 // the staging tile (5 core-matrix rows of 16 bytes at st_row + q*128), with
-// the running row sums ls0/ls1 and maxima mx0/mx1 of the raw scores. MASKED
-// treats columns at or past vh (the item's end) as -inf: only an item's tail
-// tile needs it.
+// the row sum in ls2 (two fp32 lanes) and the largest p so far in pmax (two
+// bf16 lanes): p above 2^8 means the row maximum moved past the lazy-rescale
+// threshold. MASKED treats columns at or past vh (the item's end) as -inf:
+// only an item's tail tile needs it.
 template <bool MASKED>
-MLA_DEVI void softmax_half(const uint32_t (&r)[40], int vh, float sl2, float m_used, bool active,
-                           uint8_t* st_row, float& ls0, float& ls1, float& mx0, float& mx1) {
+MLA_DEVI void softmax_half(const uint32_t (&r)[40], int vh, uint64_t sl2x2, uint64_t negm2,
+                           bool active, uint8_t* st_row, uint64_t& ls2, uint32_t& pmax) {
+  constexpr uint32_t kNegInf = 0xFF800000u;
 #pragma unroll
   for (int q = 0; q < 5; ++q) {
     uint32_t pk[4];
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
       const int cc = 8 * q + j;
-      float s0 = __uint_as_float(r[cc]);
-      float s1 = __uint_as_float(r[cc + 1]);
+      uint32_t u0 = r[cc], u1 = r[cc + 1];
       if (MASKED) {
-        s0 = cc < vh ? s0 : -INFINITY;
-        s1 = cc + 1 < vh ? s1 : -INFINITY;
+        u0 = cc < vh ? u0 : kNegInf;
+        u1 = cc + 1 < vh ? u1 : kNegInf;
       }
-      mx0 = fmaxf(mx0, s0);
-      mx1 = fmaxf(mx1, s1);
-      const float e0 = fast_exp2(fmaf(s0, sl2, -m_used));
-      const float e1 = fast_exp2(fmaf(s1, sl2, -m_used));
-      ls0 += e0;
-      ls1 += e1;
+      float d0, d1;
+      unpack_f32x2(fma_f32x2(pack_b32x2(u0, u1), sl2x2, negm2), d0, d1);
+      const float e0 = fast_exp2(d0);
+      const float e1 = fast_exp2(d1);
+      ls2 = add_f32x2(ls2, pack_f32x2(e0, e1));
       pk[j / 2] = pack_bf16x2(e0, e1);
+      pmax = max_bf16x2(pmax, pk[j / 2]);
     }
     if (active)
       *reinterpret_cast<uint4*>(st_row + q * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
+}
+
+// Row maximum of the raw scores of one S tile (both halves), masked past the
+// item's end: only needed when the running maximum must move.
+MLA_DEVI float tile_row_max(uint32_t scol, int valid) {
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t r[40];
+    tmem_ld32(scol + hh * 40, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tmem_ld8(scol + hh * 40 + 32, &r[32]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 40; j += 8) reg_fence8(&r[j]);
+    const int vh = valid - hh * 40;
+#pragma unroll
+    for (int j = 0; j < 40; j += 2) {
+      mx0 = fmaxf(mx0, j < vh ? __uint_as_float(r[j]) : -INFINITY);
+      mx1 = fmaxf(mx1, j + 1 < vh ? __uint_as_float(r[j + 1]) : -INFINITY);
+    }
+  }
+  return fmaxf(mx0, mx1);
 }
 
 // Softmax warps: one thread per head row (TMEM lane), one pass per tile in the
@@ -433,12 +456,13 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       // (always on an item's first tile, rarely after), the warp redoes the
       // tile with the new maximum. S is read in two halves of 40 columns, one
       // batched load and one wait each, in rolled loops: compact code.
-      float ls0, ls1;
+      const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+      uint64_t ls2;
 #pragma unroll 1
       for (int attempt = 0;; ++attempt) {
-        ls0 = 0.0f;
-        ls1 = 0.0f;
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        ls2 = pack_f32x2(0.0f, 0.0f);
+        uint32_t pmax = 0u;
+        const uint64_t negm2 = pack_f32x2(-m_used, -m_used);
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
           if (attempt > 0 || hh > 0) {
@@ -451,14 +475,18 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
           if (row == 0) MLA_TRACE_AT(18 + 2 * hh, g);
           uint8_t* st_row = st + prow_off + hh * 5 * 128;
           if (valid == kTile)
-            softmax_half<false>(r, 40, sl2, m_used, active, st_row, ls0, ls1, mx0, mx1);
+            softmax_half<false>(r, 40, sl2x2, negm2, active, st_row, ls2, pmax);
           else
-            softmax_half<true>(r, valid - hh * 40, sl2, m_used, active, st_row, ls0, ls1, mx0, mx1);
+            softmax_half<true>(r, valid - hh * 40, sl2x2, negm2, active, st_row, ls2, pmax);
           if (row == 0) MLA_TRACE_AT(19 + 2 * hh, g);
         }
-        const float m_tile = fmaxf(mx0, mx1) * sl2;
-        const bool need = m_tile > m_used + kRescaleThreshold;
+        // p above 2^8 (bf16 0x4380; inf and NaN compare above it too) means
+        // the row maximum moved past the threshold: always on an item's first
+        // tile (m = -inf), rarely after. Then the warp finds the true row
+        // maxima and redoes the tile.
+        const bool need = (pmax & 0xFFFFu) > 0x4380u || (pmax >> 16) > 0x4380u;
         if (!__any_sync(kFullMask, need)) break;
+        const float m_tile = tile_row_max(scol, valid) * sl2;
         if (need) {
           const float a = fast_exp2(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
           alpha *= a;
@@ -466,6 +494,8 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
           m_used = m_tile;
         }
       }
+      float ls0, ls1;
+      unpack_f32x2(ls2, ls0, ls1);
       const float lsum = ls0 + ls1;
       // S is no longer needed: its buffer may take tile g + 2.
       tc_before_sync();
