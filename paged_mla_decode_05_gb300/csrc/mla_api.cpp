@@ -191,6 +191,22 @@ void build_schedule(mla_plan_s* p) {
       split_request(b, tiles[b], n, pieces);
     }
   };
+  // Cost of a candidate under perfect balance: a lower bound on evaluate().
+  // It never decreases as the chunks get smaller (more items, more split
+  // partials), so the search below stops once it reaches the best cost found.
+  auto lower_bound = [&](const std::vector<Piece>& pieces) {
+    std::vector<int> count(B, 0);
+    for (const Piece& pc : pieces) count[pc.b]++;
+    double sum = 0.0;
+    int split_items = 0;
+    for (const Piece& pc : pieces) {
+      sum += (pc.tile_end - pc.tile_begin) + kItemOverheadTiles;
+      if (count[pc.b] > 1) ++split_items;
+    }
+    double m = sum / nc;
+    if (split_items > 0) m += kCombineLaunchTiles + split_items * pen / nc;
+    return m;
+  };
   auto evaluate = [&](const std::vector<Piece>& pieces, std::vector<int>* order,
                       std::vector<int>* owner) {
     std::vector<double> cost(pieces.size());
@@ -218,6 +234,7 @@ void build_schedule(mla_plan_s* p) {
       last_chunk = chunk;
       make_pieces(chunk, cand);
       if (cand.size() > static_cast<size_t>(std::max(64 * nc, B))) break;
+      if (!best.empty() && lower_bound(cand) >= best_cost - 1e-9) break;
       const double c = evaluate(cand, nullptr, nullptr);
       if (best.empty() || c < best_cost - 1e-9) {
         best_cost = c;
