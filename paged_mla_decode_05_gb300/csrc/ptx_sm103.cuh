@@ -104,61 +104,14 @@ MLA_DEVI bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
   return mbar_try_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity);
 }
 
-// Polling wait (mbarrier.test_wait, no suspension): for a thread whose wake-up
-// latency sits on the critical path. Bounded like mbar_wait.
-MLA_DEVI bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile("{\n\t.reg .pred p;\n\t"
-               "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-               "selp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
-}
-__device__ __noinline__ bool mbar_poll_slow(uint32_t bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_test(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
-  }
-  return true;
-}
-MLA_DEVI bool mbar_poll(uint32_t bar, uint32_t parity) {
-  return mbar_test(bar, parity) || mbar_poll_slow(bar, parity);
-}
-
 MLA_DEVI void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMA
-// 2-D tiled load of one box into shared memory; completion is counted in
-// bytes on `bar`. The innermost coordinate x is in elements and must be a
-// multiple of 8 for bf16 (16-byte boundary); callers pass multiples of 64.
-MLA_DEVI void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar,
-                          uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
-}
-// 3-D tiled TMA load (coordinates innermost first), completion on `bar`.
-MLA_DEVI void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar,
-                          uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
-      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy) : "memory");
-}
-// 2-D tiled TMA load multicast to the CTAs of cta_mask: the box lands at the
-// same shared-memory offset in each, completing on the barrier at the same
-// offset in each.
-MLA_DEVI void tma_load_2d_multicast(uint32_t dst, const void* tmap, int x, int y, uint32_t bar,
-                                    uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;"
-      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(policy) : "memory");
-}
-// 4-D tiled TMA load (coordinates innermost first), completion on `bar`.
+// 4-D tiled TMA load (coordinates innermost first), completion counted in
+// bytes on `bar`. The innermost coordinate x is in elements; callers pass 0
+// (16-byte aligned).
 MLA_DEVI void tma_load_4d(uint32_t dst, const void* tmap, int x, int y, int z, int w,
                           uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -178,32 +131,6 @@ MLA_DEVI uint64_t policy_evict_normal() {
 }
 MLA_DEVI void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
-}
-
-// ------------------------------------------------- distributed shared memory
-// Store 16 bytes into the peer CTA's shared memory; the write is counted in
-// bytes on the peer's barrier `remote_bar` (both addresses from map_to_rank).
-MLA_DEVI void st_async_v4(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                          uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-               :: "r"(remote_addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar) : "memory");
-}
-MLA_DEVI void st_async_b32(uint32_t remote_addr, uint32_t a, uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
-               :: "r"(remote_addr), "r"(a), "r"(remote_bar) : "memory");
-}
-
-// ------------------------------------------------ cp.async (load/store path)
-// 16-byte global -> shared copy through L2 (bypassing L1); src_bytes = 0
-// writes 16 zero bytes and reads nothing.
-MLA_DEVI void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
-               :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (the barrier's expected count includes this arrival).
-MLA_DEVI void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -265,23 +192,6 @@ MLA_DEVI void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
-}
-MLA_DEVI void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-// Order later uses of registers filled by tcgen05.ld after tcgen05.wait::ld:
-// an empty asm that "rewrites" them, placed after the wait.
-MLA_DEVI void reg_fence16(uint32_t* r) {
-  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-               "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-               "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 MLA_DEVI void tmem_ld8(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
