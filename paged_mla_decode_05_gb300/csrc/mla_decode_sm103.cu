@@ -294,33 +294,47 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
 // two bf16 per column. Rows at or past H are zero (in-kernel head padding).
 __device__ __noinline__ void load_q(const DecodeParams& p, Ctrl* c, int b, int row,
                                     uint32_t trow) {
-  const bool valid = row < p.H;
-  const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<int64_t>(b) * p.H + row) * kDc);
-  const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + (static_cast<int64_t>(b) * p.H + row) * kDr);
+  // The warp writes its 32-lane quarter of Q as two 16-lane halves in the
+  // 16x256b fragment: a quad of threads reads 32 consecutive bytes of one head
+  // row, so each load instruction fills whole sectors of 8 rows.
+  const int lane = row & 31;
+  const int q0 = row - lane;                    // first head of this quarter
+  const int g4 = lane >> 2, u = lane & 3;
+  const int64_t r0 = static_cast<int64_t>(b) * p.H + q0 + g4;
+  const uint2* qn = reinterpret_cast<const uint2*>(p.q_nope + r0 * kDc) + u;
+  const uint2* qp = reinterpret_cast<const uint2*>(p.q_pe + r0 * kDr) + u;
+  const int nv = p.H - (q0 + g4);               // heads q0+g4+8m exist while 8m < nv
   // Three groups of 3 panels (96 columns), each announced on its own barrier:
   // the S MMAs of the item's first tile start on the first panels while the
   // later groups are still loading.
 #pragma unroll
   for (int grp = 0; grp < 3; ++grp) {
-    uint4 v[3][8];
+    uint2 v[3][4][4];   // [panel][head q0+g4+8m][32-byte column block]
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
       const int cc = grp * 3 + j;
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        v[j][e] = valid ? __ldg(cc < 8 ? qn + cc * 8 + e : qp + e) : make_uint4(0u, 0u, 0u, 0u);
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          v[j][m][e] = 8 * m < nv ? __ldg(cc < 8 ? qn + m * 8 * (kDc / 4) + cc * 16 + e * 4
+                                                 : qp + m * 8 * (kDr / 4) + e * 4)
+                                  : make_uint2(0u, 0u);
     }
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
-      uint32_t r[32];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        r[4 * e + 0] = v[j][e].x;
-        r[4 * e + 1] = v[j][e].y;
-        r[4 * e + 2] = v[j][e].z;
-        r[4 * e + 3] = v[j][e].w;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[16];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          r[4 * e + 0] = v[j][2 * h][e].x;
+          r[4 * e + 1] = v[j][2 * h][e].y;
+          r[4 * e + 2] = v[j][2 * h + 1][e].x;
+          r[4 * e + 3] = v[j][2 * h + 1][e].y;
+        }
+        tmem_st16x256b_x4(trow + (static_cast<uint32_t>(16 * h) << 16) + kTmemQ + (grp * 3 + j) * 32, r);
       }
-      tmem_st32(trow + kTmemQ + (grp * 3 + j) * 32, r);
     }
     tmem_wait_st();
     tc_before_sync();
@@ -453,18 +467,21 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       // p = 2^(s*scale*log2e - m) with the running maximum m, row sum, bf16
       // pack into the staging tile; the tile's own maximum is tracked on the
       // way. If it lies more than kRescaleThreshold above m for some row
-      // (always on an item's first tile, rarely after), the warp redoes the
-      // tile with the new maximum. S is read in two halves of 40 columns, one
+      // (rarely), the warp redoes the tile with the new maximum. S is read in two halves of 40 columns, one
       // batched load and one wait each, in rolled loops: compact code.
       const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
       uint64_t ls2;
+      // On an item's first tile the running maximum is -inf, so the first
+      // pass is skipped: the tile goes straight to the row maxima and the pass
+      // against them.
 #pragma unroll 1
-      for (int attempt = 0;; ++attempt) {
+      for (int attempt = (i == 0 ? -1 : 0);; ++attempt) {
         ls2 = pack_f32x2(0.0f, 0.0f);
-        uint32_t pmax = 0u;
+        uint32_t pmax = 0xFFFFFFFFu;   // forces the row maxima (attempt -1)
         const uint64_t negm2 = pack_f32x2(-m_used, -m_used);
+        if (attempt >= 0) pmax = 0u;
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = 0; hh < 2 && attempt >= 0; ++hh) {
           if (attempt > 0 || hh > 0) {
             tmem_ld32(scol + hh * 40, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
             tmem_ld8(scol + hh * 40 + 32, &r[32]);
@@ -481,14 +498,13 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
           if (row == 0) MLA_TRACE_AT(19 + 2 * hh, g);
         }
         // p above 2^8 (bf16 0x4380; inf and NaN compare above it too) means
-        // the row maximum moved past the threshold: always on an item's first
-        // tile (m = -inf), rarely after. Then the warp finds the true row
-        // maxima and redoes the tile.
+        // the row maximum moved past the threshold. Then the warp finds the
+        // true row maxima and redoes the tile.
         const bool need = (pmax & 0xFFFFu) > 0x4380u || (pmax >> 16) > 0x4380u;
         if (!__any_sync(kFullMask, need)) break;
         const float m_tile = tile_row_max(scol, valid) * sl2;
         if (need) {
-          const float a = fast_exp2(m_used - m_tile);  // 0 on the first tile (m_used = -inf)
+          const float a = fast_exp2(m_used - m_tile);  // 0 on an item's first tile (m_used = -inf)
           alpha *= a;
           l *= a;
           m_used = m_tile;

@@ -204,6 +204,21 @@ MLA_DEVI void reg_fence8(uint32_t* r) {
   asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
                "+r"(r[6]), "+r"(r[7]));
 }
+// 16 lanes x 32 columns from the 16x256b fragment, 4 repetitions along the
+// columns: in repetition e, thread t holds columns 8e + 2(t%4) and 8e + 2(t%4) + 1
+// of lane t/4 (registers 4e, 4e+1) and of lane t/4 + 8 (registers 4e+2, 4e+3),
+// lanes counted from the address's lane. A quad of threads then covers 32
+// consecutive bytes of one row.
+MLA_DEVI void tmem_st16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};"
+      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+         "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+         "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 MLA_DEVI void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
