@@ -134,7 +134,8 @@ void split_request(int b, int tiles, int n, std::vector<Piece>& out) {
 }
 
 // Longest-processing-time-first assignment; returns the makespan in cost
-// units and fills owner[i] with the CTA pair of piece i (in assignment order).
+// units and fills owner[i] with the CTA pair of piece i; order lists the
+// pieces longest first.
 double lpt(const std::vector<double>& cost, int nc, std::vector<int>* order,
            std::vector<int>* owner) {
   std::vector<int> idx(cost.size());
@@ -157,7 +158,79 @@ double lpt(const std::vector<double>& cost, int nc, std::vector<int>* order,
   return makespan;
 }
 
-// Cost model in units of one 96-token tile of the steady-state pipeline:
+// Exchange pass over an assignment. While the most loaded pair can hand an
+// item to another pair, or swap it for a smaller item there, so that both end
+// below the current makespan, it does so: partner pairs are tried from the
+// least loaded up, and with the first partner that admits an improvement the
+// exchange leaving the larger of the two loads smallest is made. Returns the
+// new makespan.
+double refine_assignment(const std::vector<double>& cost, int nc, std::vector<int>& owner) {
+  std::vector<double> load(nc, 0.0);
+  std::vector<std::vector<int>> held(nc);
+  for (size_t i = 0; i < cost.size(); ++i) {
+    load[owner[i]] += cost[i];
+    held[owner[i]].push_back(static_cast<int>(i));
+  }
+  std::vector<int> by_load(nc);   // pairs in increasing load
+  for (int c = 0; c < nc; ++c) by_load[c] = c;
+  auto resort = [&]() {           // insertion sort: at most two pairs moved
+    for (int a = 1; a < nc; ++a) {
+      const int c = by_load[a];
+      int b = a;
+      while (b > 0 && load[by_load[b - 1]] > load[c]) {
+        by_load[b] = by_load[b - 1];
+        --b;
+      }
+      by_load[b] = c;
+    }
+  };
+  std::sort(by_load.begin(), by_load.end(), [&](int a, int b) { return load[a] < load[b]; });
+  constexpr double kEps = 1e-9;
+  const int max_rounds = 8 * nc;
+  for (int round = 0; round < max_rounds; ++round) {
+    const int top = by_load[nc - 1];
+    const double lt = load[top];
+    int bi = -1, bc = -1, bj = -1;   // item of top, partner pair, item coming back (-1: none)
+    for (int k = 0; k < nc - 1 && bi < 0; ++k) {
+      const int c = by_load[k];
+      const double lc = load[c];
+      if (lc + kEps >= lt) break;
+      double best = lt - kEps;
+      const std::vector<int>& ht = held[top];
+      const std::vector<int>& hc = held[c];
+      for (size_t a = 0; a < ht.size(); ++a) {
+        const double ci = cost[ht[a]];
+        const double moved = std::max(lt - ci, lc + ci);
+        if (moved < best) { best = moved; bi = static_cast<int>(a); bc = c; bj = -1; }
+        for (size_t q = 0; q < hc.size(); ++q) {
+          const double d = ci - cost[hc[q]];
+          if (d <= 0.0) continue;
+          const double swapped = std::max(lt - d, lc + d);
+          if (swapped < best) { best = swapped; bi = static_cast<int>(a); bc = c; bj = static_cast<int>(q); }
+        }
+      }
+    }
+    if (bi < 0) break;
+    const int i = held[top][bi];
+    held[top].erase(held[top].begin() + bi);
+    load[top] -= cost[i];
+    if (bj >= 0) {
+      const int j = held[bc][bj];
+      held[bc].erase(held[bc].begin() + bj);
+      load[bc] -= cost[j];
+      held[top].push_back(j);
+      load[top] += cost[j];
+      owner[j] = top;
+    }
+    held[bc].push_back(i);
+    load[bc] += cost[i];
+    owner[i] = bc;
+    resort();
+  }
+  return load[by_load[nc - 1]];
+}
+
+// Cost model in units of one 80-token tile of the steady-state pipeline:
 //  - every item costs its tiles plus a fixed start/finish overhead (Q load
 //    into tensor memory, pipeline fill, epilogue);
 //  - every split item also writes an fp32 partial of H x 512 that the
@@ -245,6 +318,12 @@ void build_schedule(mla_plan_s* p) {
   }
   std::vector<int> order, owner;
   evaluate(best, &order, &owner);
+  {
+    std::vector<double> cost(best.size());
+    for (size_t i = 0; i < best.size(); ++i)
+      cost[i] = (best[i].tile_end - best[i].tile_begin) + kItemOverheadTiles;
+    refine_assignment(cost, nc, owner);
+  }
 
   // Slots for split pieces, combine list, per-request split counts.
   std::vector<int> count(B, 0);

@@ -49,7 +49,7 @@ struct Ctrl {
   uint64_t kv_empty[kNumStages];  // score: S MMAs done reading the stage
   uint64_t s_full[2];             // score: S tile in tensor memory
   uint64_t s_free[2];             // score: softmax copied S out
-  uint64_t q_ready[3];            // score: Q of the next item in tensor memory, per 96 columns
+  uint64_t q_ready[kNumPanels];   // score: Q of the next item in tensor memory, per panel
   uint64_t p_empty[kNumPBufs];    // score: peer finished P.V on its P buffer k
   uint64_t v_full[kNumVSlots];    // output: V half landed
   uint64_t v_empty[kNumVSlots];   // output: P.V done reading the V half
@@ -261,13 +261,11 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
       uint32_t blo = static_cast<uint32_t>(bp);
       uint32_t a = tmem + kTmemQ;
       if (i == 0) {
-        // First tile of an item: its Q arrives in three groups of 3 panels.
+        // First tile of an item: its Q arrives panel by panel.
 #pragma unroll 1
         for (int pc = 0; pc < kNumPanels; ++pc, a += 32, blo += kAtomBytes / 16) {
-          if (pc % 3 == 0) {
-            if (!mbar_wait(smem_addr(&c->q_ready[pc / 3]), q_par)) { ok = false; break; }
-            tc_after_sync();
-          }
+          if (!mbar_wait(smem_addr(&c->q_ready[pc]), q_par)) { ok = false; break; }
+          tc_after_sync();
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             mma_ts(d, a + q * 8, (static_cast<uint64_t>(hi) << 32) | (blo + q * 2), idesc,
@@ -304,41 +302,42 @@ __device__ __noinline__ void load_q(const DecodeParams& p, Ctrl* c, int b, int r
   const uint2* qn = reinterpret_cast<const uint2*>(p.q_nope + r0 * kDc) + u;
   const uint2* qp = reinterpret_cast<const uint2*>(p.q_pe + r0 * kDr) + u;
   const int nv = p.H - (q0 + g4);               // heads q0+g4+8m exist while 8m < nv
-  // Three groups of 3 panels (96 columns), each announced on its own barrier:
-  // the S MMAs of the item's first tile start on the first panels while the
-  // later groups are still loading.
+  // Panels stream through a ring of three register buffers: panel cc + 3 is
+  // requested as soon as panel cc is in tensor memory, so three panels are in
+  // flight throughout. Each panel is announced on its own barrier (one arrival
+  // per warp), and the item's first S MMAs follow it panel by panel.
+  uint2 v[3][4][4];   // [ring slot][head q0+g4+8m][32-byte column block]
+  auto request = [&](int cc, uint2 (&dst)[4][4]) {
 #pragma unroll
-  for (int grp = 0; grp < 3; ++grp) {
-    uint2 v[3][4][4];   // [panel][head q0+g4+8m][32-byte column block]
+    for (int m = 0; m < 4; ++m)
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const int cc = grp * 3 + j;
+      for (int e = 0; e < 4; ++e)
+        dst[m][e] = 8 * m < nv ? __ldg(cc < 8 ? qn + m * 8 * (kDc / 4) + cc * 16 + e * 4
+                                              : qp + m * 8 * (kDr / 4) + e * 4)
+                               : make_uint2(0u, 0u);
+  };
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
+  for (int cc = 0; cc < 3; ++cc) request(cc, v[cc]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          v[j][m][e] = 8 * m < nv ? __ldg(cc < 8 ? qn + m * 8 * (kDc / 4) + cc * 16 + e * 4
-                                                 : qp + m * 8 * (kDr / 4) + e * 4)
-                                  : make_uint2(0u, 0u);
-    }
+  for (int cc = 0; cc < kNumPanels; ++cc) {
+    uint2 (&cur)[4][4] = v[cc % 3];
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
+    for (int h = 0; h < 2; ++h) {
+      uint32_t r[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t r[16];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          r[4 * e + 0] = v[j][2 * h][e].x;
-          r[4 * e + 1] = v[j][2 * h][e].y;
-          r[4 * e + 2] = v[j][2 * h + 1][e].x;
-          r[4 * e + 3] = v[j][2 * h + 1][e].y;
-        }
-        tmem_st16x256b_x4(trow + (static_cast<uint32_t>(16 * h) << 16) + kTmemQ + (grp * 3 + j) * 32, r);
+      for (int e = 0; e < 4; ++e) {
+        r[4 * e + 0] = cur[2 * h][e].x;
+        r[4 * e + 1] = cur[2 * h][e].y;
+        r[4 * e + 2] = cur[2 * h + 1][e].x;
+        r[4 * e + 3] = cur[2 * h + 1][e].y;
       }
+      tmem_st16x256b_x4(trow + (static_cast<uint32_t>(16 * h) << 16) + kTmemQ + cc * 32, r);
     }
     tmem_wait_st();
     tc_before_sync();
-    mbar_arrive(smem_addr(&c->q_ready[grp]));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&c->q_ready[cc]));
+    if (cc + 3 < kNumPanels) request(cc + 3, cur);
   }
 }
 
@@ -828,7 +827,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->o_ready[j]), 128);
       mbar_init(smem_addr(&c->o_done[j]), 1);
     }
-    for (int j = 0; j < 3; ++j) mbar_init(smem_addr(&c->q_ready[j]), 128);
+    for (int j = 0; j < kNumPanels; ++j) mbar_init(smem_addr(&c->q_ready[j]), 4);
     for (int k = 0; k < kNumPBufs; ++k) {
       mbar_init(smem_addr(&c->p_empty[k]), 1);
       mbar_init(smem_addr(&c->p_full[k]), 1);

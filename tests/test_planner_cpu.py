@@ -107,3 +107,17 @@ def test_search_returns_the_best_candidate(m, seed):
             break
     got = plan_cost(plan, H, nc)
     assert got <= best + 1e-6, (got, best)
+
+
+def test_exchange_pass_fixes_a_known_lpt_miss(m):
+    """Two CTA pairs and requests of 3, 3, 2, 2 and 2 tiles (costs 5.5, 5.5,
+    4.5, 4.5, 4.5 with the 2.5-tile item overhead). LPT alone ends at 14.5
+    ({5.5, 4.5, 4.5} against {5.5, 4.5}). The best split of the five whole
+    requests is {5.5, 5.5} against {4.5, 4.5, 4.5}, makespan 13.5: every other
+    split leaves one pair at 14.5 or more, and splitting a request costs more
+    than it saves here."""
+    lens = np.array([240, 240, 160, 160, 160], dtype=np.int32)
+    plan = m.mla_decode_plan(5, 16, lens, 64, 4, num_clusters=2, host_only=True)
+    assert all(plan.num_splits(b) == 1 for b in range(5))
+    assert plan_cost(plan, 16, 2) == pytest.approx(13.5)
+    assert lpt_makespan([5.5, 5.5, 4.5, 4.5, 4.5], 2) == pytest.approx(14.5)
