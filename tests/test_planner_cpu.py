@@ -13,6 +13,8 @@ import heapq
 import numpy as np
 import pytest
 
+from test_abi_cpu import check_schedule
+
 ITEM_OVERHEAD = 2.5
 COMBINE_LAUNCH = 3.0
 
@@ -107,6 +109,7 @@ def test_search_returns_the_best_candidate(m, seed):
             break
     got = plan_cost(plan, H, nc)
     assert got <= best + 1e-6, (got, best)
+    check_schedule(plan, lens, H, nc)
 
 
 def test_exchange_pass_fixes_a_known_lpt_miss(m):
