@@ -210,6 +210,29 @@ const char* mla_status_string(mla_status_t status);
 /* 1 if the current device can run mla_decode, 0 otherwise. */
 int mla_device_supported(void);
 
+/*
+ * mla_selftest_wait_timeout — health check of the error path that every
+ * decode relies on when one of its waits cannot complete. The method's
+ * sources have no counterpart (they describe no failure detection beyond
+ * retries in CI).
+ *
+ * One warp of a one-block kernel waits, through the same bounded wait routine
+ * the decode roles use, on a shared-memory barrier that nothing ever
+ * completes. After the wait limit (2e9 SM cycles, about a second) every thread
+ * gives up, and the kernel sets MLA_DEVERR_TIMEOUT in a device word that is
+ * copied to *bits_out. No trap and no fault is involved: the device stays
+ * usable, and a decode issued afterwards runs normally.
+ *
+ * stream: a cudaStream_t (NULL = the legacy default stream); the call
+ * synchronises it and takes about a second. bits_out: host memory, receives
+ * the MLA_DEVERR_* bits (MLA_DEVERR_TIMEOUT when the wait gave up as
+ * designed). The call allocates and frees 4 bytes of device memory.
+ *
+ * Errors: MLA_ERR_INVALID_ARG if bits_out is NULL, MLA_ERR_UNSUPPORTED_DEVICE
+ * off sm_103, MLA_ERR_CUDA if an allocation, launch or copy fails.
+ */
+mla_status_t mla_selftest_wait_timeout(void* stream, uint32_t* bits_out);
+
 #ifdef __cplusplus
 }
 #endif

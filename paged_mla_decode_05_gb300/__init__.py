@@ -10,7 +10,8 @@ that first use raises ImportError. There is no fallback path.
 """
 _EXPORTS = ("MLAError", "Plan", "mla_check_device_error", "mla_decode", "mla_decode_no_alloc",
             "mla_decode_plan",
-            "mla_device_supported", "mla_status_string", "header_functions",
+            "mla_device_supported", "mla_selftest_wait_timeout", "mla_status_string",
+            "header_functions",
             "MLA_DEVERR_BAD_BLOCK", "MLA_DEVERR_SEQLEN_MISMATCH", "MLA_DEVERR_TIMEOUT")
 
 

@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
         "mla_plan_destroy": (None, [p]),
         "mla_status_string": (ctypes.c_char_p, [i32]),
         "mla_device_supported": (i32, []),
+        "mla_selftest_wait_timeout": (i32, [p, ctypes.POINTER(u32)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -264,6 +265,16 @@ def mla_check_device_error(plan: Plan, stream=None) -> int:
     st = LIB.mla_check_device_error(plan.handle, _stream_ptr(stream), ctypes.byref(bits))
     if st not in (MLA_OK, 5):
         raise MLAError(st, "mla_check_device_error")
+    return int(bits.value)
+
+
+def mla_selftest_wait_timeout(stream=None) -> int:
+    """Run the bounded-wait health check (about a second on the current device)
+    and return the MLA_DEVERR_* bits it produced: MLA_DEVERR_TIMEOUT when the
+    wait gave up as designed."""
+    bits = ctypes.c_uint32(0)
+    _check(LIB.mla_selftest_wait_timeout(_stream_ptr(stream), ctypes.byref(bits)),
+           "mla_selftest_wait_timeout")
     return int(bits.value)
 
 

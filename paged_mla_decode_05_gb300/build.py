@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libmla_decode_sm103.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
-SOURCES = ["mla_decode_sm103.cu", "mla_combine_sm103.cu", "mla_no_alloc_sm103.cu", "mla_api.cpp"]
+SOURCES = ["mla_decode_sm103.cu", "mla_combine_sm103.cu", "mla_no_alloc_sm103.cu",
+           "mla_selftest_sm103.cu", "mla_api.cpp"]
 HEADERS = ["mla_internal.h", "ptx_sm103.cuh"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 

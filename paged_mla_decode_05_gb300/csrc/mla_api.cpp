@@ -786,4 +786,22 @@ int mla_device_supported(void) {
   return device_is_sm103(dev) ? 1 : 0;
 }
 
+mla_status_t mla_selftest_wait_timeout(void* stream, uint32_t* bits_out) {
+  if (!bits_out) return MLA_ERR_INVALID_ARG;
+  *bits_out = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || !device_is_sm103(dev)) return MLA_ERR_UNSUPPORTED_DEVICE;
+  uint32_t* word = nullptr;
+  if (cudaMalloc(&word, sizeof(uint32_t)) != cudaSuccess) return MLA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  mla_status_t st = MLA_OK;
+  if (cudaMemsetAsync(word, 0, sizeof(uint32_t), s) != cudaSuccess ||
+      mla::launch_wait_timeout_selftest(word, s) != cudaSuccess ||
+      cudaMemcpyAsync(bits_out, word, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    st = MLA_ERR_CUDA;
+  cudaFree(word);
+  return st;
+}
+
 }  // extern "C"

@@ -118,6 +118,9 @@ cudaError_t launch_decode(const DecodeParams& p, int num_clusters, cudaStream_t 
 cudaError_t launch_combine(const CombineParams& p, int num_items, cudaStream_t stream);
 cudaError_t decode_max_clusters(int* num_clusters);
 cudaError_t decode_prepare_device();
+// One-warp kernel whose wait on a barrier nothing completes must time out
+// (sets MLA_DEVERR_TIMEOUT in *err).
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, cudaStream_t stream);
 
 // Bytes of the fixed device scratch behind mla_decode_no_alloc.
 constexpr size_t kNoAllocScratchBytes = size_t{32} << 20;
