@@ -122,3 +122,16 @@ def test_host_only_plan_cannot_decode(m):
                                *([ctypes.c_void_p(16)] * 2), ctypes.c_float(0.1),
                                *([ctypes.c_void_p(16)] * 3), 0, None)
     assert rc == 1
+
+
+def test_selftest_argument_checks(m):
+    """mla_selftest_wait_timeout rejects a NULL result pointer before touching
+    CUDA, and on a machine without a GPU answers 'unsupported device'."""
+    lib = m._lib.LIB
+    assert lib.mla_selftest_wait_timeout(None, None) == 1          # MLA_ERR_INVALID_ARG
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the unsupported-device answer needs a machine without a GPU")
+    bits = ctypes.c_uint32(7)
+    assert lib.mla_selftest_wait_timeout(None, ctypes.byref(bits)) == 2   # UNSUPPORTED_DEVICE
+    assert bits.value == 0
