@@ -396,9 +396,10 @@ mla_status_t upload(mla_plan_s* p, cudaStream_t stream, bool sync) {
   if (p->sched_bytes > p->d_cap) {
     // Growing: the old buffer may still be read by queued decodes.
     if (p->d_buf) {
+      // The error word is sticky until mla_check_device_error: carry it over.
       if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
       uint32_t bits = 0;
-      cudaMemcpy(&bits, p->d_buf, 4, cudaMemcpyDeviceToHost);
+      if (cudaMemcpy(&bits, p->d_buf, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
       cudaFree(p->d_buf);
       p->d_buf = nullptr;
       const size_t cap = align_up(p->sched_bytes * 2, 4096);
