@@ -205,3 +205,15 @@ def test_argument_errors(lib):
         m.mla_decode_plan(2, 16, np.array([10**6, 1]), 32, int(w["max_blocks"]))
     m.mla_decode(plan, *args, 0.1, o, l, ws)
     assert m.mla_check_device_error(plan) == 0
+
+
+def test_convenience_decode_matches_oracle(lib, oracle_mod):
+    """The one-call wrapper (plan from the device lengths, outputs and
+    workspace allocated for the caller) on a workload that splits requests."""
+    w = wl.generate(wl.WORKLOADS[1])
+    t = to_device(w)
+    out, lse = lib.decode(t["q_nope"], t["q_pe"], t["kv_cache"], t["block_table"], t["seq_lens"],
+                          float(w["sm_scale"]))
+    ref_out, ref_lse = oracle_mod.mla_decode(*oracle_args(w))
+    assert_parity(out.float().cpu().numpy().astype(np.float64),
+                  lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, "decode()")
