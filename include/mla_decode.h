@@ -94,10 +94,14 @@ mla_status_t mla_decode_plan_ex(int B, int H, const int32_t* seq_lens_host, int 
 /*
  * Rebuild an existing plan for new lengths with the same B, H, block_size and
  * max_blocks, reusing its device allocation when large enough. The upload is
- * an asynchronous copy on `stream` from host memory held by the plan, so a
- * decode enqueued later on the same stream sees the new schedule. Do not
- * update a plan while a decode that uses it may still be running on another
- * stream. Errors as mla_decode_plan.
+ * an asynchronous copy on `stream` from pinned host memory held by the plan
+ * (two buffers used in turn), so a decode enqueued later on the same stream
+ * sees the new schedule. The call never synchronises the device: when the
+ * schedule outgrows the plan's device buffer, a larger one is allocated, the
+ * error word is carried over by a copy on `stream`, and the old buffer is
+ * kept until mla_plan_destroy. It waits on the host only for the upload made
+ * two updates earlier. Do not update a plan while a decode that uses it may
+ * still be running on another stream. Errors as mla_decode_plan.
  */
 mla_status_t mla_plan_update(mla_plan_t plan, const int32_t* seq_lens_host, void* stream);
 
@@ -156,35 +160,40 @@ mla_status_t mla_decode(mla_plan_t plan, const void* q_nope, const void* q_pe,
  * for serving engines whose caching allocator already holds nearly all of
  * HBM, so that a cudaMalloc outside the pool fails or fragments it, and for
  * host threads that must not wait on the device-wide synchronisation that
- * cudaMalloc and cudaFree can bring.
+ * cudaMalloc and cudaFree can bring. (Each call copies the work list from
+ * pageable host memory, and such a copy may hold the calling thread until
+ * the driver has staged it; it does not wait for the device.)
  *
  * Same computation, kernels and argument rules as mla_decode, with three
  * differences:
- *  - No workspace argument. The split partials, a copy of the plan's work
- *    list and the device error word live in one fixed array of
- *    MLA_NO_ALLOC_SCRATCH_BYTES inside the library's device image. Every GPU
- *    that loads the library holds it until the process exits.
+ *  - No workspace argument. The split partials and a copy of the plan's work
+ *    list live in one fixed array of MLA_NO_ALLOC_SCRATCH_BYTES inside the
+ *    library's device image. Every GPU that loads the library holds it until
+ *    the process exits.
  *  - The plan may be host-only (mla_decode_plan_ex with host_only = 1, so
  *    that planning allocates no device memory either). Each call copies the
  *    plan's work list from host memory into the scratch on `stream`.
- *  - err_bits (device uint32, may be NULL) receives this call's
- *    MLA_DEVERR_* bits: the call zeroes it, then the kernels OR into it. With
- *    NULL the bits go to a word in the scratch that the call zeroes and
- *    nobody reads. mla_check_device_error does not see this call's errors.
+ *  - err_bits (device uint32, required) receives this call's MLA_DEVERR_*
+ *    bits: the call zeroes it, then the kernels OR into it. Read it after the
+ *    stream has reached the end of the call. mla_check_device_error does not
+ *    see this call's errors.
  *
  * The call allocates nothing: no cudaMalloc, no cudaFree, no pinned memory.
  * Its first call on each device looks up the scratch's device address (and
- * sets the kernel attributes mla_decode also needs); make that first call
- * before any stream capture on that device.
+ * sets the kernel attributes mla_decode also needs). It refuses a stream
+ * that is being captured into a CUDA graph (MLA_ERR_INVALID_ARG): its
+ * work-list copies read the plan's host memory, which a later
+ * mla_plan_update or mla_plan_destroy may change or free before a replay.
  *
  * Every call on a device shares the one scratch array, which keeps what the
  * last call left there. Calls whose work may overlap on the GPU (different
  * streams, or several threads) race on it and corrupt each other's results:
  * order them on one stream or synchronise between them.
  *
- * Errors: those of mla_decode, and MLA_ERR_WORKSPACE_TOO_SMALL when the
- * plan's work list plus its split partials (mla_plan_workspace_bytes) need
- * more than MLA_NO_ALLOC_SCRATCH_BYTES; such a plan must use mla_decode.
+ * Errors: those of mla_decode; MLA_ERR_INVALID_ARG also for a NULL err_bits
+ * and for a capturing stream; MLA_ERR_WORKSPACE_TOO_SMALL when the plan's
+ * work list plus its split partials (mla_plan_workspace_bytes) need more
+ * than MLA_NO_ALLOC_SCRATCH_BYTES; such a plan must use mla_decode.
  */
 mla_status_t mla_decode_no_alloc(mla_plan_t plan, const void* q_nope, const void* q_pe,
                                  const void* kv_cache, int64_t num_blocks,

@@ -228,7 +228,7 @@ def mla_decode(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, sm_sca
 
 
 def mla_decode_no_alloc(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens,
-                        sm_scale: float, out, lse, err_bits=None, stream=None):
+                        sm_scale: float, out, lse, err_bits, stream=None):
     """Enqueue one decode that allocates nothing (see mla_decode_no_alloc in
     include/mla_decode.h): for callers whose device memory all belongs to a
     caching allocator, or who must not stall on cudaMalloc's synchronisation.
@@ -236,8 +236,8 @@ def mla_decode_no_alloc(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_len
     Same tensors as ``mla_decode`` but no workspace: the split partials live in
     the library's fixed device scratch, shared by every call on the device, so
     calls that may overlap on the GPU race. ``plan`` may be host-only.
-    ``err_bits`` is an optional CUDA int32 tensor of one element that receives
-    this call's device error bits.
+    ``err_bits`` is a CUDA int32 tensor of one element that receives this
+    call's device error bits. A stream under graph capture is refused.
     """
     import torch
     B, H = plan.B, plan.H
@@ -253,7 +253,7 @@ def mla_decode_no_alloc(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_len
     sl = _tensor(seq_lens, torch.int32, (B,), "seq_lens")
     o = _tensor(out, torch.bfloat16, (B, H, D_C), "out")
     l = _tensor(lse, torch.float32, (B, H), "lse")
-    eb = ctypes.c_void_p(0) if err_bits is None else _tensor(err_bits, torch.int32, (1,), "err_bits")
+    eb = _tensor(err_bits, torch.int32, (1,), "err_bits")
     _check(LIB.mla_decode_no_alloc(plan.handle, args[0], args[1], args[2], nb, bt, sl,
                                    ctypes.c_float(sm_scale), o, l, eb, _stream_ptr(stream)),
            "mla_decode_no_alloc")

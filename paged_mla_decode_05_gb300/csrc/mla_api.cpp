@@ -41,9 +41,16 @@ struct mla_plan_s {
   // Device copy of the schedule: [error word | items | offsets | combine].
   uint8_t* d_buf = nullptr;
   size_t d_cap = 0;
-  uint8_t* h_stage = nullptr;  // pinned staging for asynchronous uploads
-  size_t h_cap = 0;
-  cudaEvent_t upload_done = nullptr;
+  // Pinned staging for asynchronous uploads, two buffers used in turn, each
+  // with the event of the last copy that read it.
+  uint8_t* h_stage[2] = {nullptr, nullptr};
+  size_t h_cap[2] = {0, 0};
+  cudaEvent_t upload_done[2] = {nullptr, nullptr};
+  int stage_turn = 0;
+  // Buffers replaced by a larger one while queued work might still read them;
+  // freed by mla_plan_destroy, after its device synchronisation.
+  std::vector<uint8_t*> retired_dev;
+  std::vector<uint8_t*> retired_host;
   size_t off_items = 0, off_offsets = 0, off_combine = 0, sched_bytes = 0;
   // Cached TMA descriptors (K and V boxes, 16- and 32-row) of the last cache seen.
   CUtensorMap tmap_k16;
@@ -389,46 +396,48 @@ mla_status_t check_plan_args(int B, int H, const int32_t* seq_lens, int block_si
   return MLA_OK;
 }
 
-// Copy the schedule to the device. Synchronous when stream_or_null is
-// nullptr-and-sync, else asynchronous on the stream from pinned staging.
+// Copy the schedule to the device: synchronously (plan creation) or as an
+// asynchronous copy on `stream` from pinned staging (mla_plan_update). The
+// asynchronous path never waits for the device: a device buffer that must
+// grow is replaced, the error word is carried over by a copy ordered on the
+// stream, and the old buffer is kept until the plan is destroyed; the two
+// staging buffers alternate, so a copy from one may still be queued while the
+// other is filled.
 mla_status_t upload(mla_plan_s* p, cudaStream_t stream, bool sync) {
   if (p->host_only) return MLA_OK;
   if (p->sched_bytes > p->d_cap) {
-    // Growing: the old buffer may still be read by queued decodes.
+    const size_t cap = align_up(p->sched_bytes * 2, 4096);
+    uint8_t* nb = nullptr;
+    if (cudaMalloc(&nb, cap) != cudaSuccess) return MLA_ERR_CUDA;
+    cudaError_t e;
     if (p->d_buf) {
       // The error word is sticky until mla_check_device_error: carry it over.
-      if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
-      uint32_t bits = 0;
-      if (cudaMemcpy(&bits, p->d_buf, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
-      cudaFree(p->d_buf);
-      p->d_buf = nullptr;
-      const size_t cap = align_up(p->sched_bytes * 2, 4096);
-      if (cudaMalloc(&p->d_buf, cap) != cudaSuccess) return MLA_ERR_CUDA;
-      p->d_cap = cap;
-      if (cudaMemcpy(p->d_buf, &bits, 4, cudaMemcpyHostToDevice) != cudaSuccess) return MLA_ERR_CUDA;
+      e = sync ? cudaMemcpy(nb, p->d_buf, kErrBytes, cudaMemcpyDeviceToDevice)
+               : cudaMemcpyAsync(nb, p->d_buf, kErrBytes, cudaMemcpyDeviceToDevice, stream);
+      p->retired_dev.push_back(p->d_buf);
     } else {
-      const size_t cap = align_up(p->sched_bytes * 2, 4096);
-      if (cudaMalloc(&p->d_buf, cap) != cudaSuccess) return MLA_ERR_CUDA;
-      p->d_cap = cap;
-      if (cudaMemset(p->d_buf, 0, kErrBytes) != cudaSuccess) return MLA_ERR_CUDA;
+      e = cudaMemset(nb, 0, kErrBytes);
     }
+    p->d_buf = nb;
+    p->d_cap = cap;
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
   }
-  if (p->sched_bytes > p->h_cap) {
-    if (p->h_stage) {
-      if (p->upload_done) cudaEventSynchronize(p->upload_done);
-      cudaFreeHost(p->h_stage);
-      p->h_stage = nullptr;
-    }
-    const size_t cap = align_up(p->sched_bytes * 2, 4096);
-    if (cudaMallocHost(&p->h_stage, cap) != cudaSuccess) return MLA_ERR_CUDA;
-    p->h_cap = cap;
-  }
-  if (!p->upload_done &&
-      cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming) != cudaSuccess)
+  const int k = p->stage_turn;
+  p->stage_turn ^= 1;
+  if (!p->upload_done[k] &&
+      cudaEventCreateWithFlags(&p->upload_done[k], cudaEventDisableTiming) != cudaSuccess)
     return MLA_ERR_CUDA;
-  // The staging buffer may still feed the previous asynchronous copy.
-  if (cudaEventSynchronize(p->upload_done) != cudaSuccess) return MLA_ERR_CUDA;
-  uint8_t* h = p->h_stage;
+  // This staging buffer may still feed the copy before last.
+  if (cudaEventSynchronize(p->upload_done[k]) != cudaSuccess) return MLA_ERR_CUDA;
+  if (p->sched_bytes > p->h_cap[k]) {
+    if (p->h_stage[k]) p->retired_host.push_back(p->h_stage[k]);
+    p->h_stage[k] = nullptr;
+    p->h_cap[k] = 0;
+    const size_t cap = align_up(p->sched_bytes * 2, 4096);
+    if (cudaMallocHost(&p->h_stage[k], cap) != cudaSuccess) return MLA_ERR_CUDA;
+    p->h_cap[k] = cap;
+  }
+  uint8_t* h = p->h_stage[k];
   std::memcpy(h + p->off_items, p->items.data(), p->items.size() * sizeof(WorkItem));
   std::memcpy(h + p->off_offsets, p->cluster_offsets.data(), p->cluster_offsets.size() * 4);
   std::memcpy(h + p->off_combine, p->combine.data(), p->combine.size() * sizeof(CombineItem));
@@ -441,21 +450,25 @@ mla_status_t upload(mla_plan_s* p, cudaStream_t stream, bool sync) {
         cudaSuccess)
       return MLA_ERR_CUDA;
   }
-  if (cudaEventRecord(p->upload_done, sync ? nullptr : stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaEventRecord(p->upload_done[k], sync ? nullptr : stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
 void free_plan(mla_plan_s* p) {
   if (!p) return;
-  if (p->d_buf) {
+  if (p->d_buf || !p->retired_dev.empty()) {
     cudaDeviceSynchronize();
-    cudaFree(p->d_buf);
+    if (p->d_buf) cudaFree(p->d_buf);
+    for (uint8_t* b : p->retired_dev) cudaFree(b);
   }
-  if (p->upload_done) {
-    cudaEventSynchronize(p->upload_done);
-    cudaEventDestroy(p->upload_done);
+  for (int k = 0; k < 2; ++k) {
+    if (p->upload_done[k]) {
+      cudaEventSynchronize(p->upload_done[k]);
+      cudaEventDestroy(p->upload_done[k]);
+    }
+    if (p->h_stage[k]) cudaFreeHost(p->h_stage[k]);
   }
-  if (p->h_stage) cudaFreeHost(p->h_stage);
+  for (uint8_t* b : p->retired_host) cudaFreeHost(b);
   delete p;
 }
 
@@ -661,18 +674,18 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   return MLA_OK;
 }
 
-// The allocation-free variant: the workspace, the device copy of the work
-// list and the error word are carved from the library's fixed device scratch
-// (mla_no_alloc_sm103.cu) instead of caller or plan memory. Layout of the
-// scratch per call: [error word | work list as laid out by build_schedule |
-// split partials o | split partials lse].
+// The allocation-free variant: the workspace and the device copy of the work
+// list are carved from the library's fixed device scratch
+// (mla_no_alloc_sm103.cu) instead of caller or plan memory; the error word is
+// the caller's. Layout of the scratch per call: [unused 256 B | work list as
+// laid out by build_schedule | split partials o | split partials lse].
 mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q_pe,
                                  const void* kv_cache, int64_t num_blocks,
                                  const int32_t* block_table, const int32_t* seq_lens,
                                  float sm_scale, void* out, float* lse, uint32_t* err_bits,
                                  void* stream) {
   if (!p) return MLA_ERR_INVALID_ARG;
-  if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !lse)
+  if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !lse || !err_bits)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
       !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
@@ -686,6 +699,15 @@ mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q
   const size_t o_bytes = static_cast<size_t>(p->num_slots) * p->H * mla::kDc * 4;
   if (p->sched_bytes + p->workspace_bytes > mla::kNoAllocScratchBytes)
     return MLA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The work list is copied from the plan's host vectors. Under stream
+  // capture such a copy would become a graph node that reads those vectors
+  // at every replay, after a later mla_plan_update or mla_plan_destroy may
+  // have reallocated or freed them, so a capturing stream is refused, before
+  // any other CUDA call (some would invalidate the caller's capture).
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &capture) != cudaSuccess) return MLA_ERR_CUDA;
+  if (capture != cudaStreamCaptureStatusNone) return MLA_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_UNSUPPORTED_DEVICE;
   if (p->device >= 0 && dev != p->device) return MLA_ERR_INVALID_ARG;
@@ -696,15 +718,14 @@ mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q
   st = refresh_kv_maps(p, kv_cache, num_blocks);
   if (st != MLA_OK) return st;
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The error word is the only state that must start at zero: the work list
-  // is rewritten below, and every partial slot is written in full by its work
-  // item before the combine kernel reads it.
-  uint32_t* err = err_bits ? err_bits : reinterpret_cast<uint32_t*>(scratch);
+  // The caller's error word is the only state that must start at zero: the
+  // work list is rewritten below, and every partial slot is written in full
+  // by its work item before the combine kernel reads it.
+  uint32_t* err = err_bits;
   if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MLA_ERR_CUDA;
-  // The plan's host vectors are the source; a copy from pageable memory has
-  // been staged by the time cudaMemcpyAsync returns, so a later
-  // mla_plan_update cannot change what this call reads.
+  // Outside capture, a copy from pageable memory has been staged by the time
+  // cudaMemcpyAsync returns, so a later mla_plan_update cannot change what
+  // this call reads.
   if (cudaMemcpyAsync(scratch + p->off_items, p->items.data(), p->items.size() * sizeof(WorkItem),
                       cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(scratch + p->off_offsets, p->cluster_offsets.data(),

@@ -74,17 +74,6 @@ def assert_parity(out, lse, ref_out, ref_lse, what=""):
     return float(err.max()), float(lerr.max()) if lerr.size else 0.0
 
 
-def sample_rows(w, n_random, seed, full_requests=()):
-    """(b, h) rows to check at sizes where the full oracle is too slow: every
-    head of the listed requests plus n_random random rows."""
-    rng = np.random.default_rng(seed)
-    B, H = int(w["B"]), int(w["H"])
-    rows = [(b, h) for b in full_requests for h in range(H)]
-    rows += [(int(rng.integers(0, B)), int(rng.integers(0, H))) for _ in range(n_random)]
-    rows = sorted(set(rows))
-    return np.array([r[0] for r in rows]), np.array([r[1] for r in rows])
-
-
 def oracle_args(w):
     return (w["q_nope"], w["q_pe"], w["kv_cache"], w["block_table"], w["seq_lens"], w["sm_scale"])
 
