@@ -54,11 +54,13 @@ struct Ctrl {
   uint64_t v_full[kNumVSlots];    // output: V half landed
   uint64_t v_empty[kNumVSlots];   // output: P.V done reading the V half
   uint64_t p_full[kNumPBufs];     // output: P tile and row record landed (copy bytes)
-  uint64_t o_ready[2];            // output: O rescaled / drained for tile g (alternating)
+  uint64_t o_ready[2];            // output: O rescaled for a non-first tile of an item (alternating)
   uint64_t o_done[2];             // output: P.V of tile g complete (alternating)
+  uint64_t o_drained[2];          // output: epilogue has read O columns [256h, 256h+256) of an item
   uint32_t tmem_base;
   int32_t abort_flag;             // score softmax warps: leave the loop together
   int32_t p_seen;                 // output: P tiles received so far (paces the prefetcher)
+  int32_t k_issued;               // score: K tiles whose TMA loads are issued (paces the prefetcher)
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
@@ -67,6 +69,13 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);    // V is MN-majo
 constexpr float kRescaleThreshold = 8.0f;                        // log2 units
 constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr int kPrefetchTiles = 4;   // output prefetcher: distance ahead of received P (tiles)
+#ifndef PF_MODE
+#define PF_MODE 0
+#endif
+#ifndef PF_DIST
+#define PF_DIST 4
+#endif
+constexpr int kPfDist = PF_DIST;    // score prefetcher: tiles ahead of the TMA producer
 
 MLA_DEVI int tiles_of(const WorkItem& it) {
   return it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
@@ -81,20 +90,17 @@ MLA_DEVI void named_barrier_sync(int id, int threads) {
 }
 
 // Optional timeline instrumentation (compiled only with -DMLA_TRACE): each
-// role of the CTA pairs listed in the trace buffer records %globaltimer at
+// role of the CTA pairs listed in the trace buffer records the SM clock at
 // fixed points of every tile. Records time only; skips no work.
 #ifdef MLA_TRACE
 __device__ uint64_t* g_mla_trace = nullptr;   // [pairs][2 ranks][kTraceEvents][kTraceTiles]
 constexpr int kTracePairs = 4, kTraceEvents = 64, kTraceTiles = 256;
-// Events 0..31 record %globaltimer; slot 32 + ev records clock64 of the same event.
+// Slot 32 + ev records clock64 of event ev (SM cycles; comparable within one SM).
 MLA_DEVI void trace(int ev, int g) {
   uint64_t* t = g_mla_trace;
   const int pair = static_cast<int>(cluster_id_x());
   if (t == nullptr || pair >= kTracePairs || g >= kTraceTiles) return;
-  uint64_t now;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
   const int base = (pair * 2 + static_cast<int>(cluster_rank())) * kTraceEvents;
-  t[(base + ev) * kTraceTiles + g] = now;
   t[(base + 32 + ev) * kTraceTiles + g] = static_cast<uint64_t>(clock64());
 }
 #define MLA_TRACE_AT(ev, g) trace(ev, g)
@@ -222,20 +228,82 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
                     large ? static_cast<const void*>(&p.tmap_k32)
                           : static_cast<const void*>(&p.tmap_k16),
                     0, 0, 0, y >> 3, full, policy);
-      if (lane == 0) MLA_TRACE_AT(26, g);
+      if (lane == 0) {
+        MLA_TRACE_AT(26, g);
+        *reinterpret_cast<volatile int32_t*>(&c->k_issued) = g + 1;
+      }
     }
   }
+  // Release the prefetcher whatever happened (it paces itself on this count).
+  if (lane == 0) *reinterpret_cast<volatile int32_t*>(&c->k_issued) = 0x7fffffff;
   if (!ok) err |= 4u;
   err = __reduce_or_sync(kFullMask, err);
   if (lane == 0) report(p, err);
+}
+
+// L2 prefetch warp of the score CTA: walks the pair's tiles kPfDist ahead of
+// the tiles whose loads the TMA producer has issued and prefetches each tile's
+// cache rows into L2, so the producer's loads find them there. The rows of a
+// tile are page-aligned runs (the same pieces the producer loads), each a
+// contiguous range of whole 1152-byte rows.
+MLA_DEVI void score_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0, int it1) {
+  const char* cache = reinterpret_cast<const char*>(p.kv_cache);
+  volatile int32_t* issued = &c->k_issued;
+  uint32_t err = 0;
+  int g = 0;
+  const int n = pieces_per_tile(p.block_size);
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem w = p.items[it];
+    const int nt = tiles_of(w);
+    PageWindow win;
+    for (int i = 0; i < nt; ++i, ++g) {
+      int ahead_ok = 1;
+      if (lane == 0) {
+        const long long t0 = clock64();
+        while (*issued < g - kPfDist + 1) {
+          if (clock64() - t0 > kWaitLimitCycles) { ahead_ok = 0; break; }
+          __nanosleep(256);
+        }
+      }
+      if (!__shfl_sync(kFullMask, ahead_ok, 0)) return;
+      const int tile_t0 = w.t0 + i * kTile;
+      window_cover(p, w, tile_t0, win, lane);
+#if PF_MODE == 2
+      // One bulk prefetch per piece (lane j: piece j).
+      int r0, large;
+      piece_shape(p.block_size, tile_t0, lane < n ? lane : 0, r0, large);
+      const int y = cache_row(p, w, tile_t0 + r0, win, err);
+      const int rows = min(large ? kRowsLargeBox : kRowsSmallBox, w.t1 - (tile_t0 + r0));
+      if (lane < n && rows > 0 && y < static_cast<int>(p.num_blocks * p.block_size))
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     :: "l"(cache + static_cast<int64_t>(y) * (kD * 2)), "r"(rows * kD * 2) : "memory");
+#else
+      // Per-line prefetches: the warp walks each piece's 128-byte lines.
+      for (int j = 0; j < n; ++j) {
+        int r0, large;
+        piece_shape(p.block_size, tile_t0, j, r0, large);
+        const int y = cache_row(p, w, tile_t0 + r0, win, err);
+        const int rows = min(large ? kRowsLargeBox : kRowsSmallBox, w.t1 - (tile_t0 + r0));
+        if (rows <= 0 || y >= static_cast<int>(p.num_blocks * p.block_size)) continue;
+        const char* base = cache + static_cast<int64_t>(y) * (kD * 2);
+        for (int ln = lane; ln < rows * (kD * 2 / 128); ln += 32)
+          asm volatile("prefetch.global.L2 [%0];" :: "l"(base + ln * 128));
+      }
+#endif
+    }
+  }
+  (void)err;   // bad block ids are reported by the producer
 }
 
 // S MMA issuer: S[g%2] = Q . K^T over the 576 columns, 36 k-steps of 16 with
 // N = 80 (the whole tile: its 8-row atoms are kKGroupBytes apart in the
 // stage whichever pages they came from). The steady-state loop is fully
 // unrolled: one thread issues one MMA every ~50 cycles at best.
+#ifndef S_ISSUERS
+#define S_ISSUERS 1
+#endif
 MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
-                        int it1) {
+                        int it1, int sel) {
   int g = 0, n_items = 0;
   bool ok = true;
   constexpr uint32_t idesc = kIdescS;
@@ -246,7 +314,14 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
     const uint32_t q_par = n_items & 1;
     ++n_items;
     for (int i = 0; i < nt; ++i, ++g) {
+      if (S_ISSUERS > 1 && (g & 1) != sel) continue;   // the other issuer's tile
       const int s = g & 1;
+      // With two issuers, the one taking an item's second tile makes sure
+      // all of Q is in tensor memory (its last panel barrier completes last).
+      if (S_ISSUERS > 1 && i == 1 && !mbar_wait(smem_addr(&c->q_ready[kNumPanels - 1]), q_par)) {
+        ok = false;
+        break;
+      }
       if (g >= 2 && !mbar_wait(smem_addr(&c->s_free[s]), ((g >> 1) - 1) & 1)) { ok = false; break; }
       MLA_TRACE_AT(2, g);
       if (!mbar_wait(smem_addr(&c->kv_full[s]), (g >> 1) & 1)) { ok = false; break; }
@@ -413,6 +488,8 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
   // Peer (output CTA) P buffers and their barriers, at the same offsets.
   const uint32_t peer_pbuf0 = map_to_rank(smem_addr(data + kNumVSlots * kVHalfBytes), 1);
   const uint32_t peer_pfull0 = map_to_rank(smem_addr(&c->p_full[0]), 1);
+  const uint32_t peer_rec0 =
+      map_to_rank(smem_addr(data + kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes), 1);
   // Byte offset of this row inside a P tile (core-matrix row); core q adds 128*q.
   const uint32_t prow_off = (row >> 3) * kPGroupBytes + (row & 7) * 16;
 
@@ -498,9 +575,12 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
         }
         // p above 2^8 (bf16 0x4380; inf and NaN compare above it too) means
         // the row maximum moved past the threshold. Then the warp finds the
-        // true row maxima and redoes the tile.
+        // true row maxima and redoes the tile. A pass against the true maxima
+        // has every p <= 1 unless the scores hold inf or NaN (bad inputs):
+        // after it the loop ends whatever the check says, so such inputs give
+        // non-finite outputs instead of an endless loop.
         const bool need = (pmax & 0xFFFFu) > 0x4380u || (pmax >> 16) > 0x4380u;
-        if (!__any_sync(kFullMask, need)) break;
+        if (!__any_sync(kFullMask, need) || attempt >= 1) break;
         const float m_tile = tile_row_max(scol, valid) * sl2;
         if (need) {
           const float a = fast_exp2(m_used - m_tile);  // 0 on an item's first tile (m_used = -inf)
@@ -531,10 +611,17 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
             !mbar_wait_cluster(smem_addr(&c->p_empty[k]), ((g >> 1) - 1) & 1)) {
           c->abort_flag = 1;   // seen by all at the next named barrier
         } else {
+          // P into the peer's buffer k, the row record into its ring slot
+          // g % kNumRecSlots; both count on the peer's p_full[k].
           asm volatile(
               "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-              :: "r"(peer_pbuf0 + k * kPBufBytes), "r"(smem_addr(st)), "r"(kPMsgBytes),
+              :: "r"(peer_pbuf0 + k * kPBufBytes), "r"(smem_addr(st)), "r"(kPBytes),
                  "r"(peer_pfull0 + k * 8)
+              : "memory");
+          asm volatile(
+              "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+              :: "r"(peer_rec0 + (g % kNumRecSlots) * kRecBytes), "r"(smem_addr(st + kPBytes)),
+                 "r"(kRecBytes), "r"(peer_pfull0 + k * 8)
               : "memory");
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
@@ -650,17 +737,27 @@ MLA_DEVI void out_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0, 
 }
 
 // MMA issuer: O[:, 256*half ...] += P . V_half (5 k-steps of 16 tokens each).
+// An item's first tile overwrites O, so it waits for P itself (no rescale is
+// due) and, per half, for the epilogue of the previous item to have read
+// those columns; later tiles wait for the correction warps' o_ready.
 MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
                       int it1) {
-  int g = 0, h = 0;
+  int g = 0, h = 0, r = 0, n_items = 0;
   bool ok = true;
   uint8_t* pbufs = data + kNumVSlots * kVHalfBytes;
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
     const int nt = tiles_of(w);
+    if (nt == 0) continue;
+    const int item = n_items++;
     for (int i = 0; i < nt; ++i, ++g) {
       const int k = g & 1;
-      if (!mbar_wait(smem_addr(&c->o_ready[g & 1]), (g >> 1) & 1)) { ok = false; break; }
+      if (i == 0) {
+        if (!mbar_wait_cluster(smem_addr(&c->p_full[k]), (g >> 1) & 1)) { ok = false; break; }
+      } else {
+        if (!mbar_wait(smem_addr(&c->o_ready[r & 1]), (r >> 1) & 1)) { ok = false; break; }
+        ++r;
+      }
       MLA_TRACE_AT(10, g);
       tc_after_sync();
       // P: no-swizzle K-major; K-adjacent core matrices 128 B apart, row
@@ -672,6 +769,8 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
       a0 |= static_cast<uint64_t>(1) << 46;
       for (int half = 0; half < 2; ++half, ++h) {
         const int v = h % kNumVSlots;
+        if (i == 0 && item > 0 &&
+            !mbar_wait(smem_addr(&c->o_drained[half]), (item - 1) & 1)) { ok = false; break; }
         if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
         MLA_TRACE_AT(11 + half, g);
         tc_after_sync();
@@ -696,15 +795,52 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
   if (!ok) report(p, 4u);
 }
 
-// Correction + epilogue warps: one thread per head row (TMEM lane).
+// 64 columns of this thread's O row (two batched tensor-memory loads, one
+// wait), scaled by inv_l, to the output row (bf16) or the split partial (fp32).
+MLA_DEVI void drain64(const DecodeParams& p, uint32_t taddr, float inv_l, bool to_out,
+                      uint16_t* out_row, float* part_row) {
+  uint32_t r[64];
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+  tmem_wait_ld();
+  if (out_row == nullptr && part_row == nullptr) return;
+  if (to_out) {
+    uint4* o = reinterpret_cast<uint4*>(out_row);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      uint4 v;
+      v.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
+      v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
+      v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
+      v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
+      o[e] = v;
+    }
+  } else {
+    float4* o = reinterpret_cast<float4*>(part_row);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      o[e] = make_float4(__uint_as_float(r[4 * e + 0]) * inv_l, __uint_as_float(r[4 * e + 1]) * inv_l,
+                         __uint_as_float(r[4 * e + 2]) * inv_l, __uint_as_float(r[4 * e + 3]) * inv_l);
+  }
+}
+
+// Correction + epilogue warps: one thread per head row (TMEM lane). P tiles
+// land on p_full, which the elected thread arms two tiles ahead (one phase per
+// tile and buffer), so the MMA warp can also wait on it for an item's first
+// tile while these warps are still in the previous item's epilogue.
 MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int warp,
                           int lane, int it0, int it1) {
   const int row = (warp & 3) * 32 + lane;
   const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const bool active = row < p.H;
   const bool elected = (warp == 2 && lane == 0);
-  const uint8_t* pbufs = data + kNumVSlots * kVHalfBytes;
-  int g = 0;
+  const uint8_t* recs = data + kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes;
+  int total = 0;
+  for (int it = it0; it < it1; ++it) total += tiles_of(p.items[it]);
+  if (elected)
+    for (int k = 0; k < kNumPBufs && k < total; ++k)
+      mbar_arrive_expect_tx(smem_addr(&c->p_full[k]), kPMsgBytes);
+  int g = 0, r = 0;
   bool ok = true;
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
@@ -721,7 +857,6 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
     float l_fin = 1.0f, m_fin = 0.0f;
     for (int i = 0; i < nt; ++i, ++g) {
       const int k = g & 1;
-      if (elected) mbar_arrive_expect_tx(smem_addr(&c->p_full[k]), kPMsgBytes);
       if (!__all_sync(kFullMask, mbar_wait_cluster(smem_addr(&c->p_full[k]), (g >> 1) & 1))) {
         ok = false;
         break;
@@ -730,29 +865,39 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
         MLA_TRACE_AT(14, g);
         atomicAdd(&c->p_seen, 1);
       }
-      const float* rec = reinterpret_cast<const float*>(pbufs + k * kPBufBytes + kPBytes);
+      // The record of tile g stays in its slot until tile g + kNumRecSlots:
+      // the peer ships that tile after P.V of tile g + 2, which waited for
+      // these warps to pass tile g + 2 (o_ready) or, for an item's first
+      // tile, for the previous item's epilogue, which follows all its tiles.
+      const float* rec = reinterpret_cast<const float*>(recs + (g % kNumRecSlots) * kRecBytes);
       const float alpha = active ? rec[row] : 1.0f;
       const float lv = rec[kMaxHeads + row];
       const float mv = rec[2 * kMaxHeads + row];
-      if (i > 0 && __any_sync(kFullMask, alpha != 1.0f)) {
-        if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_after_sync();
+      if (i > 0) {
+        if (__any_sync(kFullMask, alpha != 1.0f)) {
+          if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_after_sync();
 #pragma unroll 1
-        for (int cc = 0; cc < kDc / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(trow + cc * 32, r);
-          tmem_wait_ld();
+          for (int cc = 0; cc < kDc / 32; ++cc) {
+            uint32_t rr[32];
+            tmem_ld32(trow + cc * 32, rr);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-          tmem_st32(trow + cc * 32, r);
+            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+            tmem_st32(trow + cc * 32, rr);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
+        tc_before_sync();
+        mbar_arrive(smem_addr(&c->o_ready[r & 1]));
+        ++r;
       }
-      tc_before_sync();
-      mbar_arrive(smem_addr(&c->o_ready[g & 1]));
+      // The next phase of this buffer is P of tile g + 2.
+      if (elected && g + kNumPBufs < total)
+        mbar_arrive_expect_tx(smem_addr(&c->p_full[k]), kPMsgBytes);
       if (row == 0) MLA_TRACE_AT(15, g);
       if (i == nt - 1) {
         l_fin = lv;
@@ -760,7 +905,9 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
       }
     }
     if (!ok) break;
-    // Epilogue: O / l -> out (bf16) or the split partial (fp32).
+    // Epilogue: O / l -> out (bf16) or the split partial (fp32), one
+    // 256-column half at a time; each half is released to the next item's
+    // first P.V as soon as it has been read.
     if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
       ok = false;
       break;
@@ -768,36 +915,26 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
     tc_after_sync();
     const float inv_l = 1.0f / l_fin;
     const float lse_val = (m_fin + __log2f(l_fin)) * 0.69314718055994531f;
+    const bool to_out = w.slot < 0;
+    uint16_t* out_row = (active && to_out) ? p.out + orow * kDc : nullptr;
+    float* part_row = (active && !to_out)
+                          ? p.part_o + (static_cast<int64_t>(w.slot) * p.H + row) * kDc
+                          : nullptr;
 #pragma unroll 1
-    for (int cc = 0; cc < kDc / 32; ++cc) {
-      uint32_t r[32];
-      tmem_ld32(trow + cc * 32, r);
-      tmem_wait_ld();
-      if (!active) continue;
-      if (w.slot < 0) {
-        uint4* o = reinterpret_cast<uint4*>(p.out + orow * kDc + cc * 32);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
-          v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
-          v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
-          v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
-          o[e] = v;
-        }
-      } else {
-        float4* o = reinterpret_cast<float4*>(p.part_o + (static_cast<int64_t>(w.slot) * p.H + row) * kDc + cc * 32);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          o[e] = make_float4(__uint_as_float(r[4 * e + 0]) * inv_l, __uint_as_float(r[4 * e + 1]) * inv_l,
-                             __uint_as_float(r[4 * e + 2]) * inv_l, __uint_as_float(r[4 * e + 3]) * inv_l);
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        const int col = half * 256 + cc * 64;
+        drain64(p, trow + col, inv_l, to_out, out_row ? out_row + col : nullptr,
+                part_row ? part_row + col : nullptr);
       }
+      tc_before_sync();
+      mbar_arrive(smem_addr(&c->o_drained[half]));
     }
     if (active) {
-      if (w.slot < 0) p.lse[orow] = lse_val;
+      if (to_out) p.lse[orow] = lse_val;
       else p.part_lse[static_cast<int64_t>(w.slot) * p.H + row] = lse_val;
     }
-    tc_before_sync();
   }
   if (!ok) report(p, 4u);
 }
@@ -826,6 +963,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->s_free[j]), 128);
       mbar_init(smem_addr(&c->o_ready[j]), 128);
       mbar_init(smem_addr(&c->o_done[j]), 1);
+      mbar_init(smem_addr(&c->o_drained[j]), 128);
     }
     for (int j = 0; j < kNumPanels; ++j) mbar_init(smem_addr(&c->q_ready[j]), 4);
     for (int k = 0; k < kNumPBufs; ++k) {
@@ -838,6 +976,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
     }
     c->abort_flag = 0;
     c->p_seen = 0;
+    c->k_issued = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -869,10 +1008,20 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
     if (warp == 0) {
       score_producer(p, c, data, lane, it0, it1);
     } else if (warp == 1) {
-      if (lane == 0) score_mma(p, c, data, tmem, it0, it1);
+      if (lane == 0) score_mma(p, c, data, tmem, it0, it1, 0);
     } else if (warp < 6) {
       score_softmax(p, c, data, tmem, warp, lane, it0, it1);
     }
+#if S_ISSUERS > 1
+    else if (warp == 7) {
+      if (lane == 0) score_mma(p, c, data, tmem, it0, it1, 1);
+    }
+#endif
+#if PF_MODE != 0
+    else if (warp == 6) {
+      score_prefetcher(p, c, lane, it0, it1);
+    }
+#endif
   } else {
     if (warp == 0) {
       out_producer(p, c, data, lane, it0, it1);
@@ -880,9 +1029,12 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       if (lane == 0) out_mma(p, c, data, tmem, it0, it1);
     } else if (warp < 6) {
       out_correct(p, c, data, tmem, warp, lane, it0, it1);
-    } else if (warp == 6) {
+    }
+#if PF_MODE == 0
+    else if (warp == 6) {
       out_prefetcher(p, c, lane, it0, it1);
     }
+#endif
   }
   __syncwarp();
   tc_before_sync();

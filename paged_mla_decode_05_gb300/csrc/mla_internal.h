@@ -39,8 +39,12 @@ constexpr int kPCoreK = kTile / 8;                     // 10 core matrices along
 constexpr int kPGroupBytes = kPCoreK * 128;            // 1280
 constexpr int kPBytes = kMaxHeads / 8 * kPGroupBytes;  // 20 KB
 constexpr int kRecFloats = 3;                          // per row: alpha, l, m
-constexpr int kPMsgBytes = kPBytes + kRecFloats * kMaxHeads * 4;  // 22016 B per tile
+constexpr int kRecBytes = kRecFloats * kMaxHeads * 4;  // 1536 B row record per tile
+constexpr int kPMsgBytes = kPBytes + kRecBytes;        // 22016 B per tile
 constexpr int kPBufBytes = 22528;                      // message rounded to 512 B
+// The output CTA receives P in kNumPBufs buffers and the row record in a ring
+// of kNumRecSlots, so a record outlives the reuse of its P buffer.
+constexpr int kNumRecSlots = 4;
 constexpr int kThreads = 256;            // 8 warps per CTA
 constexpr int kTmemCols = 512;
 // Score CTA TMEM columns: Q (576 bf16 packed in pairs) then two S buffers.
@@ -49,7 +53,8 @@ constexpr int kTmemS0 = kD / 2;          // 288
 // Shared-memory data region (after the 1 KB control block).
 constexpr int kCtrlBytes = 1024;
 constexpr int kScoreDataBytes = kNumStages * kStageBytes + kNumPBufs * kPBufBytes;  // 225 KB
-constexpr int kOutDataBytes = kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes;    // 204 KB
+constexpr int kOutDataBytes =
+    kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes + kNumRecSlots * kRecBytes;   // 210 KB
 constexpr int kDataBytes = kScoreDataBytes > kOutDataBytes ? kScoreDataBytes : kOutDataBytes;
 constexpr int kSmemBytes = kCtrlBytes + kDataBytes + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
