@@ -62,7 +62,7 @@ typedef struct mla_plan_s* mla_plan_t; /* opaque; owned by the library */
 typedef struct {
   int num_clusters;   /* 0: query the device for co-resident CTA pairs; > 0: use this many */
   int force_splits;   /* 0: automatic; > 0: split every request into this many KV chunks
-                         (testing aid; chunks are whole 80-token tiles, empty ones dropped) */
+                         (testing aid; chunks are whole 96-token tiles, empty ones dropped) */
   int host_only;      /* nonzero: build the schedule on the host only (no device upload,
                          no device query unless num_clusters == 0); such a plan can be
                          inspected but not passed to mla_decode */

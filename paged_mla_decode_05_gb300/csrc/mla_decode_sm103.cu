@@ -58,7 +58,6 @@ struct Ctrl {
   uint64_t o_done[2];             // output: P.V of tile g complete (alternating)
   uint64_t o_drained[2];          // output: epilogue has read O columns [256h, 256h+256) of an item
   uint32_t tmem_base;
-  int32_t abort_flag;             // score softmax warps: leave the loop together
   int32_t p_seen;                 // output: P tiles received so far (paces the prefetcher)
   int32_t k_issued;               // score: K tiles whose TMA loads are issued (paces the prefetcher)
 };
@@ -115,25 +114,16 @@ struct PageWindow {
   int val = 0;
 };
 
-// The pieces of one 80-token tile: page-aligned runs of 32 rows where they fit
-// (block size >= 32), else 16. A tile starts at a multiple of 80 tokens, so at
-// offset 0 or 16 modulo 32, and every piece stays inside one page.
+// The pieces of one kTile-token tile: page-aligned runs of 32 rows (block
+// size >= 32) or 16 rows (block size 16). A tile starts at a multiple of 96
+// tokens, so at a multiple of 32, and every piece stays inside one page.
 MLA_DEVI int pieces_per_tile(int block_size) {
-  return block_size >= kRowsLargeBox ? 3 : kMaxPieces;
+  return block_size >= kRowsLargeBox ? kTile / kRowsLargeBox : kTile / kRowsSmallBox;
 }
-// Piece j of the tile starting at token tile_t0: first row inside the tile
-// and whether it is a 32-row box.
-MLA_DEVI void piece_shape(int block_size, int tile_t0, int j, int& r0, int& large) {
-  if (block_size < kRowsLargeBox) {
-    r0 = j * kRowsSmallBox;
-    large = 0;
-  } else if ((tile_t0 & 31) == 0) {
-    r0 = j * kRowsLargeBox;
-    large = j < 2;
-  } else {
-    r0 = j == 0 ? 0 : kRowsSmallBox + (j - 1) * kRowsLargeBox;
-    large = j > 0;
-  }
+// Piece j of a tile: first row inside the tile and whether it is a 32-row box.
+MLA_DEVI void piece_shape(int block_size, int j, int& r0, int& large) {
+  large = block_size >= kRowsLargeBox;
+  r0 = j * (large ? kRowsLargeBox : kRowsSmallBox);
 }
 
 // Make the warp's block-table window cover the pages of the tile starting at
@@ -211,7 +201,7 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
       const int s = g & 1;
       const int tile_t0 = w.t0 + i * kTile;
       int r0, large;
-      piece_shape(p.block_size, tile_t0, lane < n ? lane : 0, r0, large);
+      piece_shape(p.block_size, lane < n ? lane : 0, r0, large);
       window_cover(p, w, tile_t0, win, lane);
       const int y = cache_row(p, w, tile_t0 + r0, win, err);   // a multiple of 8
       MLA_TRACE_AT(0, g);
@@ -271,7 +261,7 @@ MLA_DEVI void score_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0
 #if PF_MODE == 2
       // One bulk prefetch per piece (lane j: piece j).
       int r0, large;
-      piece_shape(p.block_size, tile_t0, lane < n ? lane : 0, r0, large);
+      piece_shape(p.block_size, lane < n ? lane : 0, r0, large);
       const int y = cache_row(p, w, tile_t0 + r0, win, err);
       const int rows = min(large ? kRowsLargeBox : kRowsSmallBox, w.t1 - (tile_t0 + r0));
       if (lane < n && rows > 0 && y < static_cast<int>(p.num_blocks * p.block_size))
@@ -281,7 +271,7 @@ MLA_DEVI void score_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0
       // Per-line prefetches: the warp walks each piece's 128-byte lines.
       for (int j = 0; j < n; ++j) {
         int r0, large;
-        piece_shape(p.block_size, tile_t0, j, r0, large);
+        piece_shape(p.block_size, j, r0, large);
         const int y = cache_row(p, w, tile_t0 + r0, win, err);
         const int rows = min(large ? kRowsLargeBox : kRowsSmallBox, w.t1 - (tile_t0 + r0));
         if (rows <= 0 || y >= static_cast<int>(p.num_blocks * p.block_size)) continue;
@@ -416,81 +406,67 @@ __device__ __noinline__ void load_q(const DecodeParams& p, Ctrl* c, int b, int r
   }
 }
 
-// 40 columns of one S row (registers r) -> p = 2^(s*scale*log2e - m) into
-// the staging tile (5 core-matrix rows of 16 bytes at st_row + q*128), with
-// the row sum in ls2 (two fp32 lanes) and the largest p so far in pmax (two
-// bf16 lanes): p above 2^8 means the row maximum moved past the lazy-rescale
-// threshold. MASKED treats columns at or past vh (the item's end) as -inf:
-// only an item's tail tile needs it.
-template <bool MASKED>
-MLA_DEVI void softmax_half(const uint32_t (&r)[40], int vh, uint64_t sl2x2, uint64_t negm2,
-                           bool active, uint8_t* st_row, uint64_t& ls2, uint32_t& pmax) {
-  constexpr uint32_t kNegInf = 0xFF800000u;
+// One pass of the softmax over a tile's 96 raw scores r (columns at or past
+// the item's end already set to -inf): p = 2^(s*scale*log2e - m) rounded to
+// bf16, written in 12 core-matrix chunks of 8 tokens straight into the output
+// CTA's P buffer (p_dst, 128 B apart) with remote stores counted on its
+// p_full barrier; returns the row sum of the p values (fp32, before rounding).
+MLA_DEVI float softmax_tile(const uint32_t (&r)[kTile], uint64_t sl2x2, uint64_t negm2,
+                            uint32_t p_dst, uint32_t peer_bar) {
+  uint64_t ls2 = pack_f32x2(0.0f, 0.0f);
 #pragma unroll
-  for (int q = 0; q < 5; ++q) {
+  for (int q = 0; q < kTile / 8; ++q) {
     uint32_t pk[4];
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
-      const int cc = 8 * q + j;
-      uint32_t u0 = r[cc], u1 = r[cc + 1];
-      if (MASKED) {
-        u0 = cc < vh ? u0 : kNegInf;
-        u1 = cc + 1 < vh ? u1 : kNegInf;
-      }
       float d0, d1;
-      unpack_f32x2(fma_f32x2(pack_b32x2(u0, u1), sl2x2, negm2), d0, d1);
+      unpack_f32x2(fma_f32x2(pack_b32x2(r[8 * q + j], r[8 * q + j + 1]), sl2x2, negm2), d0, d1);
       const float e0 = fast_exp2(d0);
       const float e1 = fast_exp2(d1);
       ls2 = add_f32x2(ls2, pack_f32x2(e0, e1));
       pk[j / 2] = pack_bf16x2(e0, e1);
-      pmax = max_bf16x2(pmax, pk[j / 2]);
     }
-    if (active)
-      *reinterpret_cast<uint4*>(st_row + q * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    st_async_v4(p_dst + q * 128, pk[0], pk[1], pk[2], pk[3], peer_bar);
   }
+  float ls0, ls1;
+  unpack_f32x2(ls2, ls0, ls1);
+  return ls0 + ls1;
 }
 
-// Row maximum of the raw scores of one S tile (both halves), masked past the
-// item's end: only needed when the running maximum must move.
-MLA_DEVI float tile_row_max(uint32_t scol, int valid) {
-  float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {
-    uint32_t r[40];
-    tmem_ld32(scol + hh * 40, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-    tmem_ld8(scol + hh * 40 + 32, &r[32]);
-    tmem_wait_ld();
+// Largest of a tile's 96 raw scores.
+MLA_DEVI float tile_max(const uint32_t (&r)[kTile]) {
+  float m0 = __uint_as_float(r[0]), m1 = __uint_as_float(r[1]), m2 = __uint_as_float(r[2]);
 #pragma unroll
-    for (int j = 0; j < 40; j += 8) reg_fence8(&r[j]);
-    const int vh = valid - hh * 40;
-#pragma unroll
-    for (int j = 0; j < 40; j += 2) {
-      mx0 = fmaxf(mx0, j < vh ? __uint_as_float(r[j]) : -INFINITY);
-      mx1 = fmaxf(mx1, j + 1 < vh ? __uint_as_float(r[j + 1]) : -INFINITY);
-    }
+  for (int j = 3; j + 5 < kTile; j += 6) {
+    m0 = max3f(m0, __uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+    m1 = max3f(m1, __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+    m2 = max3f(m2, __uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
   }
-  return fmaxf(mx0, mx1);
+  m0 = max3f(m0, m1, m2);
+  return max3f(m0, __uint_as_float(r[kTile - 3]), max3f(__uint_as_float(r[kTile - 2]),
+                                                      __uint_as_float(r[kTile - 1]), m0));
 }
 
-// Softmax warps: one thread per head row (TMEM lane), one pass per tile in the
-// steady state (see below); rolled loops keep the code small, since several
-// warp roles share each sub-partition's instruction cache. P goes straight
-// into a staging buffer that one elected thread ships to the peer with a bulk
-// copy.
+// Softmax warps: one thread per head row (TMEM lane); each warp runs on its
+// own (no barrier between the four warps per tile). Per tile: the 96 scores
+// are read from tensor memory with one wait, the S buffer is released at
+// once, the running row maximum m moves only when the tile's maximum exceeds
+// it by more than kRescaleThreshold (log2 units; always on an item's first
+// tile), and one pass writes P and the row record {alpha, l, m} into the
+// output CTA with remote stores.
 MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem,
                             int warp, int lane, int it0, int it1) {
   const int row = (warp & 3) * 32 + lane;
   const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-  const bool active = row < p.H;
   const bool elected = (warp == 2 && lane == 0);
   const float sl2 = p.scale_log2;
-  uint8_t* staging = data + kNumStages * kStageBytes;
-  // Peer (output CTA) P buffers and their barriers, at the same offsets.
+  const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+  // Peer (output CTA) P buffers, record ring and p_full barriers.
   const uint32_t peer_pbuf0 = map_to_rank(smem_addr(data + kNumVSlots * kVHalfBytes), 1);
-  const uint32_t peer_pfull0 = map_to_rank(smem_addr(&c->p_full[0]), 1);
   const uint32_t peer_rec0 =
-      map_to_rank(smem_addr(data + kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes), 1);
-  // Byte offset of this row inside a P tile (core-matrix row); core q adds 128*q.
+      map_to_rank(smem_addr(data + kNumVSlots * kVHalfBytes + kNumPBufs * kPBytes), 1);
+  const uint32_t peer_pfull0 = map_to_rank(smem_addr(&c->p_full[0]), 1);
+  // Byte offset of this row inside a P tile (core-matrix row); chunk q adds 128*q.
   const uint32_t prow_off = (row >> 3) * kPGroupBytes + (row & 7) * 16;
 
   int g = 0;
@@ -511,137 +487,77 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       const int k = g & 1;
       const uint32_t scol = trow + kTmemS0 + s * kTile;
       const int valid = min(kTile, w.t1 - (w.t0 + i * kTile));
-      // A failed wait is recorded in the shared flag; every softmax thread
-      // still reaches the named barrier below and leaves the loop there.
-      const bool got_s = __all_sync(kFullMask, mbar_wait(smem_addr(&c->s_full[s]), (g >> 1) & 1));
-      if (!got_s && lane == 0) c->abort_flag = 1;
-      if (row == 0) MLA_TRACE_AT(4, g);
-      float alpha = 1.0f;
-      if (row == 0) MLA_TRACE_AT(16, g);
-      tc_after_sync();
-      // The first 40 columns start loading before the staging buffer is known
-      // to be free (the load does not touch it).
-      uint32_t r[40];
-      tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-      tmem_ld8(scol + 32, &r[32]);
-      // Stage P(g) in buffer k once the copy that last read it (tile g-2) is done.
-      if (elected && g >= kNumPBufs) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-      named_barrier_sync(1, 128);
-      if (c->abort_flag) {
-        tmem_wait_ld();
+      if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->s_full[s]), (g >> 1) & 1))) {
         ok = false;
         break;
       }
+      if (row == 0) MLA_TRACE_AT(4, g);
+      tc_after_sync();
       if (i == nt - 1 && nxt < it1) {
         // The item's last S tile is complete, so Q's columns are free: load
         // the next item's Q now, letting its first S MMAs run while this
         // tile's softmax is computed.
-        tmem_wait_ld();
         load_q(p, c, p.items[nxt].b, row, trow);
       }
-      uint8_t* st = staging + k * kPBufBytes;
-      // p = 2^(s*scale*log2e - m) with the running maximum m, row sum, bf16
-      // pack into the staging tile; the tile's own maximum is tracked on the
-      // way. If it lies more than kRescaleThreshold above m for some row
-      // (rarely), the warp redoes the tile with the new maximum. S is read in two halves of 40 columns, one
-      // batched load and one wait each, in rolled loops: compact code.
-      const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
-      uint64_t ls2;
-      // On an item's first tile the running maximum is -inf, so the first
-      // pass is skipped: the tile goes straight to the row maxima and the pass
-      // against them.
-#pragma unroll 1
-      for (int attempt = (i == 0 ? -1 : 0);; ++attempt) {
-        ls2 = pack_f32x2(0.0f, 0.0f);
-        uint32_t pmax = 0xFFFFFFFFu;   // forces the row maxima (attempt -1)
-        const uint64_t negm2 = pack_f32x2(-m_used, -m_used);
-        if (attempt >= 0) pmax = 0u;
-#pragma unroll 1
-        for (int hh = 0; hh < 2 && attempt >= 0; ++hh) {
-          if (attempt > 0 || hh > 0) {
-            tmem_ld32(scol + hh * 40, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            tmem_ld8(scol + hh * 40 + 32, &r[32]);
-          }
-          tmem_wait_ld();
+      uint32_t r[kTile];
 #pragma unroll
-          for (int j = 0; j < 40; j += 8) reg_fence8(&r[j]);
-          if (row == 0) MLA_TRACE_AT(18 + 2 * hh, g);
-          uint8_t* st_row = st + prow_off + hh * 5 * 128;
-          if (valid == kTile)
-            softmax_half<false>(r, 40, sl2x2, negm2, active, st_row, ls2, pmax);
-          else
-            softmax_half<true>(r, valid - hh * 40, sl2x2, negm2, active, st_row, ls2, pmax);
-          if (row == 0) MLA_TRACE_AT(19 + 2 * hh, g);
-        }
-        // p above 2^8 (bf16 0x4380; inf and NaN compare above it too) means
-        // the row maximum moved past the threshold. Then the warp finds the
-        // true row maxima and redoes the tile. A pass against the true maxima
-        // has every p <= 1 unless the scores hold inf or NaN (bad inputs):
-        // after it the loop ends whatever the check says, so such inputs give
-        // non-finite outputs instead of an endless loop.
-        const bool need = (pmax & 0xFFFFu) > 0x4380u || (pmax >> 16) > 0x4380u;
-        if (!__any_sync(kFullMask, need) || attempt >= 1) break;
-        const float m_tile = tile_row_max(scol, valid) * sl2;
-        if (need) {
-          const float a = fast_exp2(m_used - m_tile);  // 0 on an item's first tile (m_used = -inf)
-          alpha *= a;
-          l *= a;
-          m_used = m_tile;
-        }
-      }
-      float ls0, ls1;
-      unpack_f32x2(ls2, ls0, ls1);
-      const float lsum = ls0 + ls1;
-      // S is no longer needed: its buffer may take tile g + 2.
+      for (int j = 0; j < kTile; j += 32)
+        tmem_ld32(scol + j, *reinterpret_cast<uint32_t(*)[32]>(&r[j]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < kTile; j += 8) reg_fence8(&r[j]);
+      // The scores are in registers: the S buffer may take tile g + 2.
       tc_before_sync();
       mbar_arrive(smem_addr(&c->s_free[s]));
       if (row == 0) MLA_TRACE_AT(17, g);
-      if (active) {
-        l += lsum;
-        float* rec = reinterpret_cast<float*>(st + kPBytes);
-        rec[row] = alpha;
-        rec[kMaxHeads + row] = l;
-        rec[2 * kMaxHeads + row] = m_used;
+      if (valid < kTile) {   // the item's tail tile: columns past its end are -inf
+#pragma unroll
+        for (int j = 0; j < kTile; ++j) r[j] = j < valid ? r[j] : 0xFF800000u;
       }
-      fence_proxy_async_smem();
-      named_barrier_sync(1, 128);
-      if (row == 0) MLA_TRACE_AT(5, g);
-      if (elected) {
-        if (g >= kNumPBufs &&
-            !mbar_wait_cluster(smem_addr(&c->p_empty[k]), ((g >> 1) - 1) & 1)) {
-          c->abort_flag = 1;   // seen by all at the next named barrier
-        } else {
-          // P into the peer's buffer k, the row record into its ring slot
-          // g % kNumRecSlots; both count on the peer's p_full[k].
-          asm volatile(
-              "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-              :: "r"(peer_pbuf0 + k * kPBufBytes), "r"(smem_addr(st)), "r"(kPBytes),
-                 "r"(peer_pfull0 + k * 8)
-              : "memory");
-          asm volatile(
-              "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-              :: "r"(peer_rec0 + (g % kNumRecSlots) * kRecBytes), "r"(smem_addr(st + kPBytes)),
-                 "r"(kRecBytes), "r"(peer_pfull0 + k * 8)
-              : "memory");
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      // Lazy rescale: keep the running maximum unless the tile's maximum lies
+      // more than kRescaleThreshold above it (always on an item's first tile,
+      // where m is -inf); P rescaled by alpha then reaches the output CTA.
+      const float m_tile = tile_max(r) * sl2;
+      float alpha = 1.0f;
+      if (m_tile > m_used + kRescaleThreshold) {
+        alpha = fast_exp2(m_used - m_tile);   // 0 on an item's first tile
+        l *= alpha;
+        m_used = m_tile;
+      }
+      // P buffer k may be overwritten once P.V of tile g - 2 has read it
+      // (lane 0 waits with cluster acquire; the warp barrier orders the other
+      // lanes' remote stores after it).
+      if (g >= kNumPBufs) {
+        int got = 1;
+        if (lane == 0) got = mbar_wait_cluster(smem_addr(&c->p_empty[k]), ((g >> 1) - 1) & 1);
+        got = __shfl_sync(kFullMask, got, 0);
+        __syncwarp();
+        if (!got) {
+          ok = false;
+          break;
         }
-        MLA_TRACE_AT(6, g);
       }
+      if (row == 0) MLA_TRACE_AT(5, g);
+      const uint32_t bar = peer_pfull0 + k * 8;
+      l += softmax_tile(r, sl2x2, pack_f32x2(-m_used, -m_used), peer_pbuf0 + k * kPBytes + prow_off,
+                        bar);
+      st_async_v4(peer_rec0 + (g % kNumRecSlots) * kRecBytes + row * 16, __float_as_uint(alpha),
+                  __float_as_uint(l), __float_as_uint(m_used), 0u, bar);
+      if (row == 0) MLA_TRACE_AT(6, g);
     }
     cur = nxt;
   }
-  // Drain: every copy has landed, and the peer's last commits (arriving on
-  // p_empty) are consumed, so nothing remote is in flight when we exit.
+  // Drain: the peer's last commits (arriving on p_empty) are consumed, so
+  // nothing remote is in flight into this CTA when it exits.
   if (elected) {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    if (ok && !c->abort_flag)
+    if (ok)
       for (int gg = (g > 2 ? g - 2 : 0); gg < g; ++gg)
         if (!mbar_wait_cluster(smem_addr(&c->p_empty[gg & 1]), (gg >> 1) & 1)) {
           ok = false;
           break;
         }
-    if (!ok || c->abort_flag) report(p, 4u);
   }
+  if (!ok && lane == 0) report(p, 4u);
 }
 
 // ----------------------------------------------------------- output CTA roles
@@ -661,7 +577,7 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
       const int tile_t0 = w.t0 + i * kTile;
       const int n = pieces_per_tile(p.block_size);
       int r0, large;
-      piece_shape(p.block_size, tile_t0, lane < n ? lane : 0, r0, large);
+      piece_shape(p.block_size, lane < n ? lane : 0, r0, large);
       window_cover(p, w, tile_t0, win, lane);
       const int y = cache_row(p, w, tile_t0 + r0, win, err);
       for (int half = 0; half < 2; ++half, ++h) {
@@ -760,9 +676,12 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
       }
       MLA_TRACE_AT(10, g);
       tc_after_sync();
+      // P arrived through remote stores (generic proxy); make them visible to
+      // the tensor core's reads of shared memory.
+      fence_proxy_async_smem();
       // P: no-swizzle K-major; K-adjacent core matrices 128 B apart, row
       // groups kPGroupBytes apart (layout type 0 in bits 61-63).
-      const uint32_t pa = smem_addr(pbufs + k * kPBufBytes);
+      const uint32_t pa = smem_addr(pbufs + k * kPBytes);
       uint64_t a0 = static_cast<uint64_t>((pa >> 4) & 0x3FFFu);
       a0 |= static_cast<uint64_t>(128 >> 4) << 16;
       a0 |= static_cast<uint64_t>(kPGroupBytes >> 4) << 32;
@@ -834,7 +753,7 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
   const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const bool active = row < p.H;
   const bool elected = (warp == 2 && lane == 0);
-  const uint8_t* recs = data + kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes;
+  const uint8_t* recs = data + kNumVSlots * kVHalfBytes + kNumPBufs * kPBytes;
   int total = 0;
   for (int it = it0; it < it1; ++it) total += tiles_of(p.items[it]);
   if (elected)
@@ -869,10 +788,10 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
       // the peer ships that tile after P.V of tile g + 2, which waited for
       // these warps to pass tile g + 2 (o_ready) or, for an item's first
       // tile, for the previous item's epilogue, which follows all its tiles.
-      const float* rec = reinterpret_cast<const float*>(recs + (g % kNumRecSlots) * kRecBytes);
-      const float alpha = active ? rec[row] : 1.0f;
-      const float lv = rec[kMaxHeads + row];
-      const float mv = rec[2 * kMaxHeads + row];
+      const float4 rec = reinterpret_cast<const float4*>(recs + (g % kNumRecSlots) * kRecBytes)[row];
+      const float alpha = active ? rec.x : 1.0f;
+      const float lv = rec.y;
+      const float mv = rec.z;
       if (i > 0) {
         if (__any_sync(kFullMask, alpha != 1.0f)) {
           if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
@@ -974,7 +893,6 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->v_full[v]), 1);
       mbar_init(smem_addr(&c->v_empty[v]), 1);
     }
-    c->abort_flag = 0;
     c->p_seen = 0;
     c->k_issued = 0;
     fence_barrier_init();
@@ -985,15 +903,6 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   } else if (warp == 0 && lane == 1) {
     prefetch_tmap(&p.tmap_v16);
     prefetch_tmap(&p.tmap_v32);
-  }
-  {
-    // Zero the P staging buffers (score CTA) and P buffers (output CTA) once:
-    // rows >= H are never written and stay zero (padded heads).
-    uint4* pz = reinterpret_cast<uint4*>(
-        data + (rank == 0 ? kNumStages * kStageBytes : kNumVSlots * kVHalfBytes));
-    for (int e = threadIdx.x; e < kNumPBufs * kPBufBytes / 16; e += kThreads)
-      pz[e] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(&c->tmem_base), kTmemCols);

@@ -13,35 +13,35 @@ constexpr int kDc = 512;                 // latent c_kv columns (= V width)
 constexpr int kDr = 64;                  // rope k_pe columns
 constexpr int kD = kDc + kDr;            // 576 bf16 per cached token row
 constexpr int kMaxHeads = 128;           // MMA M; fewer heads are padded inside the kernel
-constexpr int kTile = 80;                // tokens per KV tile (MMA N of the score product)
-constexpr int kRowsSmallBox = 16;        // TMA box heights: 16 rows (any block size) and
+constexpr int kTile = 96;                // tokens per KV tile (MMA N of the score product)
+constexpr int kRowsSmallBox = 16;        // TMA box heights: 16 rows (block size 16) and
 constexpr int kRowsLargeBox = 32;        // 32 rows (block sizes >= 32), never crossing a page
-constexpr int kMaxPieces = kTile / kRowsSmallBox;      // at most 5 boxes per panel per tile
+constexpr int kMaxPieces = kTile / kRowsSmallBox;      // at most 6 boxes per tile
 constexpr int kPanelCols = 64;           // bf16 columns of one 128-byte swizzle panel
 constexpr int kNumPanels = kD / kPanelCols;            // 9 panels per row
-constexpr int kPanelBytes = kTile * 128;               // one panel of one tile: 10 KB
-// Score stage: [row group (10)][panel (9)][8 rows][128 B]; 8-row atoms are
+constexpr int kPanelBytes = kTile * 128;               // one panel of one tile: 12 KB
+// Score stage: [row group (12)][panel (9)][8 rows][128 B]; 8-row atoms are
 // kKGroupBytes apart along the rows and 1 KB apart along the panels.
-constexpr int kStageBytes = kNumPanels * kPanelBytes;  // full 576-wide tile: 90 KB
+constexpr int kStageBytes = kNumPanels * kPanelBytes;  // full 576-wide tile: 108 KB
 constexpr int kVHalfPanels = 4;                        // V half = 256 columns
-// V half slot: [row group (10)][panel (4)][8 rows][128 B].
-constexpr int kVHalfBytes = kVHalfPanels * kPanelBytes;  // 40 KB
+// V half slot: [row group (12)][panel (4)][8 rows][128 B].
+constexpr int kVHalfBytes = kVHalfPanels * kPanelBytes;  // 48 KB
 constexpr int kAtomBytes = 8 * 128;                      // 8 rows x 128 B (one swizzle atom)
 constexpr int kKGroupBytes = kNumPanels * kAtomBytes;    // 9216: row-group stride of a stage
 constexpr int kVGroupBytes = kVHalfPanels * kAtomBytes;  // 4096: row-group stride of a V slot
 constexpr int kNumStages = 2;            // score CTA: KV tiles in flight
-constexpr int kNumVSlots = 4;            // output CTA: V half-tiles in flight
-constexpr int kNumPBufs = 2;             // P tiles in flight (staging and peer buffers)
-// P [128 rows x 80 tokens] bf16 in the no-swizzle K-major layout of 8-row x
+constexpr int kNumVSlots = 3;            // output CTA: V half-tiles in flight
+constexpr int kNumPBufs = 2;             // P tiles in flight (output CTA buffers)
+// P [128 rows x 96 tokens] bf16 in the no-swizzle K-major layout of 8-row x
 // 16-byte core matrices: [row/8][token/8][row%8][16 B]; K-adjacent cores are
-// 128 B apart, row groups 1280 B apart.
-constexpr int kPCoreK = kTile / 8;                     // 10 core matrices along K
-constexpr int kPGroupBytes = kPCoreK * 128;            // 1280
-constexpr int kPBytes = kMaxHeads / 8 * kPGroupBytes;  // 20 KB
-constexpr int kRecFloats = 3;                          // per row: alpha, l, m
-constexpr int kRecBytes = kRecFloats * kMaxHeads * 4;  // 1536 B row record per tile
-constexpr int kPMsgBytes = kPBytes + kRecBytes;        // 22016 B per tile
-constexpr int kPBufBytes = 22528;                      // message rounded to 512 B
+// 128 B apart, row groups 1536 B apart. The score CTA's softmax threads write
+// it straight into the output CTA's buffer (asynchronous remote stores).
+constexpr int kPCoreK = kTile / 8;                     // 12 core matrices along K
+constexpr int kPGroupBytes = kPCoreK * 128;            // 1536
+constexpr int kPBytes = kMaxHeads / 8 * kPGroupBytes;  // 24 KB
+// Row record per tile: {alpha, l, m, 0} as 16 bytes per row.
+constexpr int kRecBytes = kMaxHeads * 16;              // 2 KB
+constexpr int kPMsgBytes = kPBytes + kRecBytes;        // 26 KB of remote stores per tile
 // The output CTA receives P in kNumPBufs buffers and the row record in a ring
 // of kNumRecSlots, so a record outlives the reuse of its P buffer.
 constexpr int kNumRecSlots = 4;
@@ -50,11 +50,12 @@ constexpr int kTmemCols = 512;
 // Score CTA TMEM columns: Q (576 bf16 packed in pairs) then two S buffers.
 constexpr int kTmemQ = 0;
 constexpr int kTmemS0 = kD / 2;          // 288
+static_assert(kTmemS0 + 2 * kTile <= kTmemCols, "Q and two S buffers must fit in tensor memory");
 // Shared-memory data region (after the 1 KB control block).
 constexpr int kCtrlBytes = 1024;
-constexpr int kScoreDataBytes = kNumStages * kStageBytes + kNumPBufs * kPBufBytes;  // 225 KB
+constexpr int kScoreDataBytes = kNumStages * kStageBytes;                            // 216 KB
 constexpr int kOutDataBytes =
-    kNumVSlots * kVHalfBytes + kNumPBufs * kPBufBytes + kNumRecSlots * kRecBytes;   // 210 KB
+    kNumVSlots * kVHalfBytes + kNumPBufs * kPBytes + kNumRecSlots * kRecBytes;      // 200 KB
 constexpr int kDataBytes = kScoreDataBytes > kOutDataBytes ? kScoreDataBytes : kOutDataBytes;
 constexpr int kSmemBytes = kCtrlBytes + kDataBytes + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");

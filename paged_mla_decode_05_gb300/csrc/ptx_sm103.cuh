@@ -104,6 +104,15 @@ MLA_DEVI bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
   return mbar_try_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity);
 }
 
+// 16-byte asynchronous store into the shared memory of a CTA of this cluster
+// (addresses from map_to_rank); the peer's barrier `bar` counts the bytes
+// (complete_tx), so its waiter sees them once the phase completes.
+MLA_DEVI void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                          uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+               :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar) : "memory");
+}
+
 MLA_DEVI void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -284,6 +293,12 @@ MLA_DEVI uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
 MLA_DEVI uint64_t add_f32x2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Three-input fp32 maximum (sm_100+).
+MLA_DEVI float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 MLA_DEVI uint32_t max_bf16x2(uint32_t a, uint32_t b) {

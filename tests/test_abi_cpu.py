@@ -8,6 +8,8 @@ import pytest
 
 import mla_workloads as wl
 
+TILE = 96   # tokens per KV tile: work items cover whole tiles
+
 
 @pytest.fixture(scope="module")
 def m():
@@ -43,7 +45,7 @@ def check_schedule(plan, lens, H, n_clusters):
     slots = []
     for (b, t0, t1, slot, cl) in items:
         assert 0 <= cl < n_clusters
-        assert t0 % 80 == 0 and t0 <= t1 <= lens[b]
+        assert t0 % TILE == 0 and t0 <= t1 <= lens[b]
         covered[b].append((t0, t1, slot))
         if slot >= 0:
             slots.append(slot)
@@ -90,7 +92,7 @@ def test_forced_splits(m, force):
     plan = m.mla_decode_plan(5, 32, lens, 32, 200, num_clusters=8, force_splits=force,
                              host_only=True)
     check_schedule(plan, lens, 32, 8)
-    tiles = (lens + 79) // 80
+    tiles = (lens + TILE - 1) // TILE
     for b in range(5):
         assert plan.num_splits(b) == max(1, min(force, int(tiles[b])))
 
@@ -102,7 +104,7 @@ def test_balance_with_few_pairs(m):
     check_schedule(plan, lens, 16, 10)
     load = np.zeros(10)
     for (b, t0, t1, slot, cl) in plan.work_items():
-        load[cl] += (t1 - t0 + 79) // 80 + 2.5
+        load[cl] += (t1 - t0 + TILE - 1) // TILE + 2.5
     assert load.max() <= 1.1 * load.mean()
 
 

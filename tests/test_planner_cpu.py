@@ -2,7 +2,7 @@
 best of all the chunk sizes it may consider, under its cost model, although
 it stops evaluating candidates early.
 
-Cost model (in units of one 80-token tile): every work item costs its tiles
+Cost model (in units of one 96-token tile): every work item costs its tiles
 plus 2.5; a plan that splits any request adds 3 (the combine launch) plus, per
 split item, the fp32 partial's write and read spread over the CTA pairs.
 Candidates split every request into chunks of ceil(max_tiles / k) tiles,
@@ -13,14 +13,14 @@ import heapq
 import numpy as np
 import pytest
 
-from test_abi_cpu import check_schedule
+from test_abi_cpu import TILE, check_schedule
 
 ITEM_OVERHEAD = 2.5
 COMBINE_LAUNCH = 3.0
 
 
 def split_penalty(H):
-    return 2.0 * (H * 512 * 4 + H * 4) / (80 * 576 * 2)
+    return 2.0 * (H * 512 * 4 + H * 4) / (TILE * 576 * 2)
 
 
 def pieces_for(tiles, chunk):
@@ -64,7 +64,7 @@ def plan_cost(plan, H, nc):
     for (b, t0, t1, slot, cl) in items:
         per_request[b] = per_request.get(b, 0) + 1
     for (b, t0, t1, slot, cl) in items:
-        load[cl] += (t1 - t0 + 79) // 80 + ITEM_OVERHEAD
+        load[cl] += (t1 - t0 + TILE - 1) // TILE + ITEM_OVERHEAD
     split_items = sum(1 for (b, *_rest) in items if per_request[b] > 1)
     m = load.max()
     if split_items:
@@ -91,7 +91,7 @@ def test_search_returns_the_best_candidate(m, seed):
     lens = rng.integers(0, hi, size=B).astype(np.int32)
     max_blocks = int(np.ceil(max(int(lens.max()), 1) / 64)) + 1
     plan = m.mla_decode_plan(B, H, lens, 64, max_blocks, num_clusters=nc, host_only=True)
-    tiles = [(int(L) + 79) // 80 for L in lens]
+    tiles = [(int(L) + TILE - 1) // TILE for L in lens]
     max_tiles = max(tiles)
     best = None
     last = -1
@@ -119,8 +119,8 @@ def test_exchange_pass_fixes_a_known_lpt_miss(m):
     requests is {5.5, 5.5} against {4.5, 4.5, 4.5}, makespan 13.5: every other
     split leaves one pair at 14.5 or more, and splitting a request costs more
     than it saves here."""
-    lens = np.array([240, 240, 160, 160, 160], dtype=np.int32)
-    plan = m.mla_decode_plan(5, 16, lens, 64, 4, num_clusters=2, host_only=True)
+    lens = np.array([3 * TILE, 3 * TILE, 2 * TILE, 2 * TILE, 2 * TILE], dtype=np.int32)
+    plan = m.mla_decode_plan(5, 16, lens, 64, 5, num_clusters=2, host_only=True)
     assert all(plan.num_splits(b) == 1 for b in range(5))
     assert plan_cost(plan, 16, 2) == pytest.approx(13.5)
     assert lpt_makespan([5.5, 5.5, 4.5, 4.5, 4.5], 2) == pytest.approx(14.5)
