@@ -54,7 +54,13 @@ struct Ctrl {
   uint64_t v_full[kNumVSlots];    // output: V half landed
   uint64_t v_empty[kNumVSlots];   // output: P.V done reading the V half
   uint64_t p_full[kNumPBufs];     // output: P tile and row record landed (copy bytes)
-  uint64_t o_ready[2];            // output: O rescaled for a non-first tile of an item (alternating)
+  // output: O rescaled for a non-first tile of an item. 128 arrivals (the
+  // four correction warps, which run independently) per phase; a warp can be
+  // up to kNumPBufs - 1 such tiles ahead of another (it needs P of its tile,
+  // shipped after P.V of the tile kNumPBufs earlier), so the ring has
+  // kNumPBufs barriers and an early arrival never lands in a phase that a
+  // slower warp has not completed.
+  uint64_t o_ready[kNumPBufs];
   uint64_t o_done[2];             // output: P.V of tile g complete (alternating)
   uint64_t o_drained[2];          // output: epilogue has read O columns [256h, 256h+256) of an item
   uint32_t tmem_base;
@@ -67,7 +73,10 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTile, 0, 0);   // K-major A an
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);    // V is MN-major
 constexpr float kRescaleThreshold = 8.0f;                        // log2 units
 constexpr uint32_t kFullMask = 0xffffffffu;
-constexpr int kPrefetchTiles = 4;   // output prefetcher: distance ahead of received P (tiles)
+#ifndef PF_TILES
+#define PF_TILES 4
+#endif
+constexpr int kPrefetchTiles = PF_TILES;   // output prefetcher: distance ahead of received P (tiles)
 #ifndef PF_MODE
 #define PF_MODE 0
 #endif
@@ -484,7 +493,8 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
     float m_used = -INFINITY, l = 0.0f;
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
-      const int k = g & 1;
+      const int k = g % kNumPBufs;
+      const uint32_t ph = static_cast<uint32_t>(g / kNumPBufs) & 1u;   // P buffer use parity
       const uint32_t scol = trow + kTmemS0 + s * kTile;
       const int valid = min(kTile, w.t1 - (w.t0 + i * kTile));
       if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->s_full[s]), (g >> 1) & 1))) {
@@ -529,7 +539,7 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       // lanes' remote stores after it).
       if (g >= kNumPBufs) {
         int got = 1;
-        if (lane == 0) got = mbar_wait_cluster(smem_addr(&c->p_empty[k]), ((g >> 1) - 1) & 1);
+        if (lane == 0) got = mbar_wait_cluster(smem_addr(&c->p_empty[k]), ph ^ 1u);
         got = __shfl_sync(kFullMask, got, 0);
         __syncwarp();
         if (!got) {
@@ -551,8 +561,8 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
   // nothing remote is in flight into this CTA when it exits.
   if (elected) {
     if (ok)
-      for (int gg = (g > 2 ? g - 2 : 0); gg < g; ++gg)
-        if (!mbar_wait_cluster(smem_addr(&c->p_empty[gg & 1]), (gg >> 1) & 1)) {
+      for (int gg = (g > kNumPBufs ? g - kNumPBufs : 0); gg < g; ++gg)
+        if (!mbar_wait_cluster(smem_addr(&c->p_empty[gg % kNumPBufs]), (gg / kNumPBufs) & 1)) {
           ok = false;
           break;
         }
@@ -667,11 +677,14 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
     if (nt == 0) continue;
     const int item = n_items++;
     for (int i = 0; i < nt; ++i, ++g) {
-      const int k = g & 1;
-      if (i == 0) {
-        if (!mbar_wait_cluster(smem_addr(&c->p_full[k]), (g >> 1) & 1)) { ok = false; break; }
-      } else {
-        if (!mbar_wait(smem_addr(&c->o_ready[r & 1]), (r >> 1) & 1)) { ok = false; break; }
+      const int k = g % kNumPBufs;
+      // P of this tile arrived through the peer's remote stores, counted on
+      // p_full[k]: this thread acquires that phase itself (cluster scope)
+      // for every tile, so the stores are visible to it before the proxy
+      // fence below. A non-first tile also waits for the correction warps.
+      if (!mbar_wait_cluster(smem_addr(&c->p_full[k]), (g / kNumPBufs) & 1)) { ok = false; break; }
+      if (i > 0) {
+        if (!mbar_wait(smem_addr(&c->o_ready[r % kNumPBufs]), (r / kNumPBufs) & 1)) { ok = false; break; }
         ++r;
       }
       MLA_TRACE_AT(10, g);
@@ -775,19 +788,24 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
     }
     float l_fin = 1.0f, m_fin = 0.0f;
     for (int i = 0; i < nt; ++i, ++g) {
-      const int k = g & 1;
-      if (!__all_sync(kFullMask, mbar_wait_cluster(smem_addr(&c->p_full[k]), (g >> 1) & 1))) {
+      const int k = g % kNumPBufs;
+      if (!__all_sync(kFullMask, mbar_wait_cluster(smem_addr(&c->p_full[k]), (g / kNumPBufs) & 1))) {
         ok = false;
         break;
       }
+      // The record arrived through the peer's remote stores; order them
+      // before this thread's ordinary shared-memory loads of it.
+      fence_proxy_async_smem();
       if (row == 0) {
         MLA_TRACE_AT(14, g);
         atomicAdd(&c->p_seen, 1);
       }
-      // The record of tile g stays in its slot until tile g + kNumRecSlots:
-      // the peer ships that tile after P.V of tile g + 2, which waited for
-      // these warps to pass tile g + 2 (o_ready) or, for an item's first
-      // tile, for the previous item's epilogue, which follows all its tiles.
+      // The record of tile g stays in its slot until tile g + kNumRecSlots,
+      // which the peer ships after P.V of tile g + kNumRecSlots - kNumPBufs
+      // (at least g + 1) has completed. That P.V waited for these warps to
+      // pass its tile (o_ready) or, for an item's first tile, for the
+      // previous item's epilogue, which follows all its tiles: either way
+      // after this read of tile g.
       const float4 rec = reinterpret_cast<const float4*>(recs + (g % kNumRecSlots) * kRecBytes)[row];
       const float alpha = active ? rec.x : 1.0f;
       const float lv = rec.y;
@@ -799,19 +817,23 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
             break;
           }
           tc_after_sync();
+          // tcgen05.st reads its source registers asynchronously: each store
+          // completes (wait::st) before the next load may reuse them.
 #pragma unroll 1
           for (int cc = 0; cc < kDc / 32; ++cc) {
             uint32_t rr[32];
             tmem_ld32(trow + cc * 32, rr);
             tmem_wait_ld();
 #pragma unroll
+            for (int j = 0; j < 32; j += 8) reg_fence8(&rr[j]);
+#pragma unroll
             for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
             tmem_st32(trow + cc * 32, rr);
+            tmem_wait_st();
           }
-          tmem_wait_st();
         }
         tc_before_sync();
-        mbar_arrive(smem_addr(&c->o_ready[r & 1]));
+        mbar_arrive(smem_addr(&c->o_ready[r % kNumPBufs]));
         ++r;
       }
       // The next phase of this buffer is P of tile g + 2.
@@ -877,10 +899,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->kv_full[s]), 1);
       mbar_init(smem_addr(&c->kv_empty[s]), 1);
     }
+    for (int j = 0; j < kNumPBufs; ++j) mbar_init(smem_addr(&c->o_ready[j]), 128);
     for (int j = 0; j < 2; ++j) {
       mbar_init(smem_addr(&c->s_full[j]), 1);
       mbar_init(smem_addr(&c->s_free[j]), 128);
-      mbar_init(smem_addr(&c->o_ready[j]), 128);
       mbar_init(smem_addr(&c->o_done[j]), 1);
       mbar_init(smem_addr(&c->o_drained[j]), 128);
     }
