@@ -50,6 +50,7 @@ struct Ctrl {
   uint64_t s_full[2];             // score: S tile in tensor memory
   uint64_t s_free[2];             // score: softmax copied S out
   uint64_t q_ready[kNumPanels];   // score: Q of the next item in tensor memory, per panel
+  uint64_t q_free;                // score: S MMAs of an item's last tile done (Q may be replaced)
   uint64_t p_empty[kNumPBufs];    // score: peer finished P.V on its P buffer k
   uint64_t v_full[kNumVSlots];    // output: V half landed
   uint64_t v_empty[kNumVSlots];   // output: P.V done reading the V half
@@ -356,6 +357,7 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
       MLA_TRACE_AT(24, g);
       tc_commit(smem_addr(&c->kv_empty[s]));
       tc_commit(smem_addr(&c->s_full[s]));
+      if (i == nt - 1) tc_commit(smem_addr(&c->q_free));   // Q may now be replaced
       MLA_TRACE_AT(3, g);
     }
   }
@@ -364,8 +366,12 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
 
 // Load Q rows of request b into tensor memory columns [0, 288): lane = head,
 // two bf16 per column. Rows at or past H are zero (in-kernel head padding).
-__device__ __noinline__ void load_q(const DecodeParams& p, Ctrl* c, int b, int row,
-                                    uint32_t trow) {
+// The first three panels are loaded into registers first; then, when
+// wait_parity >= 0, the warp waits for that phase of q_free (the S MMAs of
+// the previous item's last tile are done) before it overwrites Q. Returns
+// false if that wait ran out of time.
+__device__ __noinline__ bool load_q(const DecodeParams& p, Ctrl* c, int b, int row,
+                                    uint32_t trow, int wait_parity) {
   // The warp writes its 32-lane quarter of Q as two 16-lane halves in the
   // 16x256b fragment: a quad of threads reads 32 consecutive bytes of one head
   // row, so each load instruction fills whole sectors of 8 rows.
@@ -392,6 +398,11 @@ __device__ __noinline__ void load_q(const DecodeParams& p, Ctrl* c, int b, int r
   };
 #pragma unroll
   for (int cc = 0; cc < 3; ++cc) request(cc, v[cc]);
+  if (wait_parity >= 0) {
+    if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->q_free), static_cast<uint32_t>(wait_parity))))
+      return false;
+    tc_after_sync();
+  }
 #pragma unroll
   for (int cc = 0; cc < kNumPanels; ++cc) {
     uint2 (&cur)[4][4] = v[cc % 3];
@@ -412,6 +423,29 @@ __device__ __noinline__ void load_q(const DecodeParams& p, Ctrl* c, int b, int r
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&c->q_ready[cc]));
     if (cc + 3 < kNumPanels) request(cc + 3, cur);
+  }
+  return true;
+}
+
+// Q loader warps (one per tensor-memory lane quadrant): the Q of each of the
+// pair's items in turn, so the softmax warps never stop for it. Each call
+// loads the next item's first Q panels into registers right after the
+// previous Q is written, then waits on q_free for the S MMAs of the previous
+// item's last tile (phase j - 1 for the j-th non-empty item: the barrier
+// cannot run ahead, since item j's last tile needs this Q first).
+MLA_DEVI void score_qloader(const DecodeParams& p, Ctrl* c, uint32_t tmem, int warp, int lane,
+                            int it0, int it1) {
+  const int row = (warp & 3) * 32 + lane;
+  const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  int n_items = 0;
+  for (int it = it0; it < it1; ++it) {
+    if (tiles_of(p.items[it]) == 0) continue;
+    const int wait_parity = n_items > 0 ? (n_items - 1) & 1 : -1;
+    if (!load_q(p, c, p.items[it].b, row, trow, wait_parity)) {
+      if (lane == 0) report(p, 4u);
+      return;
+    }
+    ++n_items;
   }
 }
 
@@ -482,9 +516,6 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
   bool ok = true;
   int cur = it0;
   while (cur < it1 && tiles_of(p.items[cur]) == 0) ++cur;
-  if (cur < it1) {
-    load_q(p, c, p.items[cur].b, row, trow);
-  }
   while (cur < it1 && ok) {
     const WorkItem w = p.items[cur];
     const int nt = tiles_of(w);
@@ -503,12 +534,6 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       }
       if (row == 0) MLA_TRACE_AT(4, g);
       tc_after_sync();
-      if (i == nt - 1 && nxt < it1) {
-        // The item's last S tile is complete, so Q's columns are free: load
-        // the next item's Q now, letting its first S MMAs run while this
-        // tile's softmax is computed.
-        load_q(p, c, p.items[nxt].b, row, trow);
-      }
       uint32_t r[kTile];
 #pragma unroll
       for (int j = 0; j < kTile; j += 32)
@@ -907,6 +932,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->o_drained[j]), 128);
     }
     for (int j = 0; j < kNumPanels; ++j) mbar_init(smem_addr(&c->q_ready[j]), 4);
+    mbar_init(smem_addr(&c->q_free), 1);
     for (int k = 0; k < kNumPBufs; ++k) {
       mbar_init(smem_addr(&c->p_empty[k]), 1);
       mbar_init(smem_addr(&c->p_full[k]), 1);
@@ -948,6 +974,9 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       if (lane == 0) score_mma(p, c, data, tmem, it0, it1, 1);
     }
 #endif
+    else if (warp >= 8) {
+      score_qloader(p, c, tmem, warp, lane, it0, it1);
+    }
 #if PF_MODE != 0
     else if (warp == 6) {
       score_prefetcher(p, c, lane, it0, it1);

@@ -50,7 +50,7 @@ constexpr int kPMsgBytes = kPBytes + kRecBytes;        // 26 KB of remote stores
 // of kNumRecSlots, so a record outlives the reuse of its P buffer.
 constexpr int kNumRecSlots = 4;
 static_assert(kNumRecSlots >= kNumPBufs + 1, "a record must outlive the reuse of its P buffer");
-constexpr int kThreads = 256;            // 8 warps per CTA
+constexpr int kThreads = 384;            // 12 warps per CTA
 constexpr int kTmemCols = 512;
 // Score CTA TMEM columns: Q (576 bf16 packed in pairs) then two S buffers.
 constexpr int kTmemQ = 0;
