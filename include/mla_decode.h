@@ -77,9 +77,11 @@ typedef struct {
  * which CTA pair processes each chunk (longest first), and sizes the
  * workspace. Launches no kernel. Copies the schedule (a few KB) to device
  * memory owned by the plan, on the current device.
- * Arguments: B >= 1 requests; 1 <= H <= 128 query heads (padded to 128 inside
- * the kernel, never in memory); block_size in {16, 32, 64, 128};
- * max_blocks >= 1 is the row length of block_table.
+ * Arguments: B >= 1 requests; 1 <= H <= 1024 query heads, processed in head
+ * groups of 128 (one MMA M tile each; each group reads the request's KV once;
+ * a group of fewer than 128 heads is padded inside the kernel, never in
+ * memory); block_size in {16, 32, 64, 128}; max_blocks >= 1 is the row length
+ * of block_table.
  * On success *plan_out receives a new plan (free it with mla_plan_destroy).
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED_DEVICE, MLA_ERR_CUDA.
  */
@@ -116,6 +118,9 @@ int mla_plan_num_clusters(mla_plan_t plan);       /* CTA pairs launched */
  * out/lse directly) and the CTA pair that runs it. */
 int mla_plan_work_item(mla_plan_t plan, int i, int32_t* b, int32_t* t0, int32_t* t1,
                        int32_t* slot, int32_t* cluster);
+/* Query heads [*h_begin, *h_end) of work item i: its head group (128 heads,
+ * or the rest of H for the last group). */
+int mla_plan_work_item_heads(mla_plan_t plan, int i, int32_t* h_begin, int32_t* h_end);
 
 /*
  * mla_decode — one decode step over the paged latent cache.

@@ -58,6 +58,7 @@ def _load() -> ctypes.CDLL:
         "mla_plan_num_work_items": (i32, [p]),
         "mla_plan_num_clusters": (i32, [p]),
         "mla_plan_work_item": (i32, [p, i32, p, p, p, p, p]),
+        "mla_plan_work_item_heads": (i32, [p, i32, p, p]),
         "mla_decode": (i32, [p, p, p, p, i64, p, p, ctypes.c_float, p, p, p, sz, p]),
         "mla_decode_no_alloc": (i32, [p, p, p, p, i64, p, p, ctypes.c_float, p, p, p, p]),
         "mla_check_device_error": (i32, [p, p, ctypes.POINTER(u32)]),
@@ -142,6 +143,17 @@ class Plan:
             if rc != 0:
                 raise MLAError(MLA_OK + 1, "mla_plan_work_item")
             out.append(tuple(v.value for v in vals))
+        return out
+
+    def work_item_heads(self) -> List[Tuple[int, int]]:
+        """Query heads [h_begin, h_end) of every work item (its head group)."""
+        out = []
+        hb, he = ctypes.c_int32(), ctypes.c_int32()
+        for i in range(self.num_work_items):
+            rc = LIB.mla_plan_work_item_heads(self.handle, i, ctypes.byref(hb), ctypes.byref(he))
+            if rc != 0:
+                raise MLAError(MLA_OK + 1, "mla_plan_work_item_heads")
+            out.append((hb.value, he.value))
         return out
 
     def update(self, seq_lens_host, stream=None):

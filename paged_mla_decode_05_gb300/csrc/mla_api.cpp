@@ -246,10 +246,14 @@ double refine_assignment(const std::vector<double>& cost, int nc, std::vector<in
 constexpr double kItemOverheadTiles = 2.5;
 constexpr double kCombineLaunchTiles = 3.0;
 
+// Partial write and read-back of one split item (its head group's rows).
 double split_cost_tiles(int H) {
-  const double bytes = 2.0 * (static_cast<double>(H) * mla::kDc * 4 + H * 4);
+  const double h = std::min(H, mla::kMaxHeads);
+  const double bytes = 2.0 * (h * mla::kDc * 4 + h * 4);
   return bytes / (static_cast<double>(mla::kTile) * mla::kD * 2);
 }
+
+int head_groups(int H) { return (H + mla::kMaxHeads - 1) / mla::kMaxHeads; }
 
 void build_schedule(mla_plan_s* p) {
   const int B = p->B;
@@ -261,6 +265,7 @@ void build_schedule(mla_plan_s* p) {
   }
   const int nc = p->num_clusters;
   const double pen = split_cost_tiles(p->H);
+  const int ng = head_groups(p->H);   // every KV piece is processed once per head group
 
   auto make_pieces = [&](int chunk, std::vector<Piece>& pieces) {
     pieces.clear();
@@ -280,22 +285,24 @@ void build_schedule(mla_plan_s* p) {
     double sum = 0.0;
     int split_items = 0;
     for (const Piece& pc : pieces) {
-      sum += (pc.tile_end - pc.tile_begin) + kItemOverheadTiles;
-      if (count[pc.b] > 1) ++split_items;
+      sum += ng * ((pc.tile_end - pc.tile_begin) + kItemOverheadTiles);
+      if (count[pc.b] > 1) split_items += ng;
     }
     double m = sum / nc;
     if (split_items > 0) m += kCombineLaunchTiles + split_items * pen / nc;
     return m;
   };
+  // Items: piece i, head group q -> index i * ng + q.
   auto evaluate = [&](const std::vector<Piece>& pieces, std::vector<int>* order,
                       std::vector<int>* owner) {
-    std::vector<double> cost(pieces.size());
+    std::vector<double> cost(pieces.size() * ng);
     std::vector<int> count(B, 0);
     for (const Piece& pc : pieces) count[pc.b]++;
     int split_items = 0;
     for (size_t i = 0; i < pieces.size(); ++i) {
-      cost[i] = (pieces[i].tile_end - pieces[i].tile_begin) + kItemOverheadTiles;
-      if (count[pieces[i].b] > 1) ++split_items;
+      for (int q = 0; q < ng; ++q)
+        cost[i * ng + q] = (pieces[i].tile_end - pieces[i].tile_begin) + kItemOverheadTiles;
+      if (count[pieces[i].b] > 1) split_items += ng;
     }
     double m = lpt(cost, nc, order, owner);
     if (split_items > 0) m += kCombineLaunchTiles + split_items * pen / nc;
@@ -313,7 +320,7 @@ void build_schedule(mla_plan_s* p) {
       if (chunk == last_chunk) continue;
       last_chunk = chunk;
       make_pieces(chunk, cand);
-      if (cand.size() > static_cast<size_t>(std::max(64 * nc, B))) break;
+      if (cand.size() * ng > static_cast<size_t>(std::max(64 * nc, B * ng))) break;
       if (!best.empty() && lower_bound(cand) >= best_cost - 1e-9) break;
       const double c = evaluate(cand, nullptr, nullptr);
       if (best.empty() || c < best_cost - 1e-9) {
@@ -326,9 +333,9 @@ void build_schedule(mla_plan_s* p) {
   std::vector<int> order, owner;
   evaluate(best, &order, &owner);
   {
-    std::vector<double> cost(best.size());
-    for (size_t i = 0; i < best.size(); ++i)
-      cost[i] = (best[i].tile_end - best[i].tile_begin) + kItemOverheadTiles;
+    std::vector<double> cost(best.size() * ng);
+    for (size_t i = 0; i < cost.size(); ++i)
+      cost[i] = (best[i / ng].tile_end - best[i / ng].tile_begin) + kItemOverheadTiles;
     refine_assignment(cost, nc, owner);
   }
 
@@ -347,8 +354,10 @@ void build_schedule(mla_plan_s* p) {
       slots += count[b];
     }
   }
+  // A split piece owns one partial slot, shared by its head groups (each
+  // writes its own heads' rows).
   std::vector<int> next_slot = first_slot;
-  std::vector<WorkItem> piece_item(best.size());
+  std::vector<WorkItem> piece_item(best.size() * ng);
   for (size_t i = 0; i < best.size(); ++i) {
     const Piece& pc = best[i];
     WorkItem w{};
@@ -357,7 +366,10 @@ void build_schedule(mla_plan_s* p) {
     w.t1 = std::min(pc.tile_end * mla::kTile, p->seq_lens[pc.b]);
     w.slot = count[pc.b] > 1 ? next_slot[pc.b]++ : -1;
     w.seq_len = p->seq_lens[pc.b];
-    piece_item[i] = w;
+    for (int q = 0; q < ng; ++q) {
+      w.h0 = q * mla::kMaxHeads;
+      piece_item[i * ng + q] = w;
+    }
   }
   // Group by pair, each pair's list in assignment order (longest first).
   std::vector<std::vector<int>> per(nc);
@@ -386,7 +398,7 @@ void build_schedule(mla_plan_s* p) {
 
 mla_status_t check_plan_args(int B, int H, const int32_t* seq_lens, int block_size,
                              int max_blocks) {
-  if (B < 1 || H < 1 || H > mla::kMaxHeads || !seq_lens || max_blocks < 1) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || H > mla::kMaxPlanHeads || !seq_lens || max_blocks < 1) return MLA_ERR_INVALID_ARG;
   if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
     return MLA_ERR_INVALID_ARG;
   const int64_t cap = static_cast<int64_t>(max_blocks) * block_size;
@@ -592,6 +604,14 @@ int mla_plan_num_splits(mla_plan_t p, int b) {
 int mla_plan_num_work_items(mla_plan_t p) { return p ? static_cast<int>(p->items.size()) : -1; }
 
 int mla_plan_num_clusters(mla_plan_t p) { return p ? p->num_clusters : -1; }
+
+int mla_plan_work_item_heads(mla_plan_t p, int i, int32_t* h_begin, int32_t* h_end) {
+  if (!p || i < 0 || i >= static_cast<int>(p->items.size())) return -1;
+  const WorkItem& w = p->items[i];
+  if (h_begin) *h_begin = w.h0;
+  if (h_end) *h_end = std::min(p->H, w.h0 + mla::kMaxHeads);
+  return 0;
+}
 
 int mla_plan_work_item(mla_plan_t p, int i, int32_t* b, int32_t* t0, int32_t* t1, int32_t* slot,
                        int32_t* cluster) {

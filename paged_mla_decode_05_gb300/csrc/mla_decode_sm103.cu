@@ -90,6 +90,12 @@ MLA_DEVI int tiles_of(const WorkItem& it) {
   return it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
 }
 
+// Query heads of an item's head group: heads [h0, h0 + heads_of) of the
+// request, at most 128 (the MMA M; fewer are padded inside the kernel).
+MLA_DEVI int heads_of(const DecodeParams& p, const WorkItem& it) {
+  return min(kMaxHeads, p.H - it.h0);
+}
+
 MLA_DEVI void report(const DecodeParams& p, uint32_t bits) {
   if (bits) atomicOr(p.err, bits);
 }
@@ -201,10 +207,12 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
         for (int nx = it + 1; nx < it1; ++nx) {
           const WorkItem wn = p.items[nx];
           if (tiles_of(wn) == 0) continue;
-          const uint16_t* qn = p.q_nope + static_cast<int64_t>(wn.b) * p.H * kDc;
-          const uint16_t* qp = p.q_pe + static_cast<int64_t>(wn.b) * p.H * kDr;
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qn), "r"(p.H * kDc * 2) : "memory");
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qp), "r"(p.H * kDr * 2) : "memory");
+          const int64_t qrow = static_cast<int64_t>(wn.b) * p.H + wn.h0;
+          const int nh = heads_of(p, wn);
+          const uint16_t* qn = p.q_nope + qrow * kDc;
+          const uint16_t* qp = p.q_pe + qrow * kDr;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qn), "r"(nh * kDc * 2) : "memory");
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(qp), "r"(nh * kDr * 2) : "memory");
           break;
         }
       }
@@ -364,13 +372,14 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
   if (!ok) report(p, 4u);
 }
 
-// Load Q rows of request b into tensor memory columns [0, 288): lane = head,
-// two bf16 per column. Rows at or past H are zero (in-kernel head padding).
+// Load the Q rows of item w (request w.b, heads w.h0 ...) into tensor memory
+// columns [0, 288): lane = head of the group, two bf16 per column. Lanes past
+// the group's heads are zero (in-kernel head padding).
 // The first three panels are loaded into registers first; then, when
 // wait_parity >= 0, the warp waits for that phase of q_free (the S MMAs of
 // the previous item's last tile are done) before it overwrites Q. Returns
 // false if that wait ran out of time.
-__device__ __noinline__ bool load_q(const DecodeParams& p, Ctrl* c, int b, int row,
+__device__ __noinline__ bool load_q(const DecodeParams& p, Ctrl* c, const WorkItem& w, int row,
                                     uint32_t trow, int wait_parity) {
   // The warp writes its 32-lane quarter of Q as two 16-lane halves in the
   // 16x256b fragment: a quad of threads reads 32 consecutive bytes of one head
@@ -378,10 +387,10 @@ __device__ __noinline__ bool load_q(const DecodeParams& p, Ctrl* c, int b, int r
   const int lane = row & 31;
   const int q0 = row - lane;                    // first head of this quarter
   const int g4 = lane >> 2, u = lane & 3;
-  const int64_t r0 = static_cast<int64_t>(b) * p.H + q0 + g4;
+  const int64_t r0 = static_cast<int64_t>(w.b) * p.H + w.h0 + q0 + g4;
   const uint2* qn = reinterpret_cast<const uint2*>(p.q_nope + r0 * kDc) + u;
   const uint2* qp = reinterpret_cast<const uint2*>(p.q_pe + r0 * kDr) + u;
-  const int nv = p.H - (q0 + g4);               // heads q0+g4+8m exist while 8m < nv
+  const int nv = heads_of(p, w) - (q0 + g4);    // heads q0+g4+8m exist while 8m < nv
   // Panels stream through a ring of three register buffers: panel cc + 3 is
   // requested as soon as panel cc is in tensor memory, so three panels are in
   // flight throughout. Each panel is announced on its own barrier (one arrival
@@ -441,7 +450,7 @@ MLA_DEVI void score_qloader(const DecodeParams& p, Ctrl* c, uint32_t tmem, int w
   for (int it = it0; it < it1; ++it) {
     if (tiles_of(p.items[it]) == 0) continue;
     const int wait_parity = n_items > 0 ? (n_items - 1) & 1 : -1;
-    if (!load_q(p, c, p.items[it].b, row, trow, wait_parity)) {
+    if (!load_q(p, c, p.items[it], row, trow, wait_parity)) {
       if (lane == 0) report(p, 4u);
       return;
     }
@@ -789,7 +798,6 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
                           int lane, int it0, int it1) {
   const int row = (warp & 3) * 32 + lane;
   const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-  const bool active = row < p.H;
   const bool elected = (warp == 2 && lane == 0);
   const uint8_t* recs = data + kNumVSlots * kVHalfBytes + kNumPBufs * kPBytes;
   int total = 0;
@@ -802,7 +810,8 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
     const int nt = tiles_of(w);
-    const int64_t orow = static_cast<int64_t>(w.b) * p.H + row;
+    const bool active = row < heads_of(p, w);
+    const int64_t orow = static_cast<int64_t>(w.b) * p.H + w.h0 + row;
     if (nt == 0) {  // empty request: out = 0, lse = -inf
       if (active && w.slot < 0) {
         uint4* o = reinterpret_cast<uint4*>(p.out + orow * kDc);
@@ -884,7 +893,7 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
     const bool to_out = w.slot < 0;
     uint16_t* out_row = (active && to_out) ? p.out + orow * kDc : nullptr;
     float* part_row = (active && !to_out)
-                          ? p.part_o + (static_cast<int64_t>(w.slot) * p.H + row) * kDc
+                          ? p.part_o + (static_cast<int64_t>(w.slot) * p.H + w.h0 + row) * kDc
                           : nullptr;
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
@@ -899,7 +908,7 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
     }
     if (active) {
       if (to_out) p.lse[orow] = lse_val;
-      else p.part_lse[static_cast<int64_t>(w.slot) * p.H + row] = lse_val;
+      else p.part_lse[static_cast<int64_t>(w.slot) * p.H + w.h0 + row] = lse_val;
     }
   }
   if (!ok) report(p, 4u);

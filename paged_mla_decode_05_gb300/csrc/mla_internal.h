@@ -12,7 +12,8 @@ namespace mla {
 constexpr int kDc = 512;                 // latent c_kv columns (= V width)
 constexpr int kDr = 64;                  // rope k_pe columns
 constexpr int kD = kDc + kDr;            // 576 bf16 per cached token row
-constexpr int kMaxHeads = 128;           // MMA M; fewer heads are padded inside the kernel
+constexpr int kMaxHeads = 128;           // MMA M: one head group; fewer heads are padded inside the kernel
+constexpr int kMaxPlanHeads = 1024;      // query heads per request: up to 8 head groups
 constexpr int kTile = 96;                // tokens per KV tile (MMA N of the score product)
 constexpr int kRowsSmallBox = 16;        // TMA box heights: 16 rows (block size 16) and
 constexpr int kRowsLargeBox = 32;        // 32 rows (block sizes >= 32), never crossing a page
@@ -73,7 +74,8 @@ struct WorkItem {
   int32_t t1;
   int32_t slot;
   int32_t seq_len;   // the plan's length of request b (checked against device seq_lens)
-  int32_t pad[3];
+  int32_t h0;        // first query head of the item's head group (a multiple of 128)
+  int32_t pad[2];
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 

@@ -39,18 +39,24 @@ def test_status_strings(m):
 
 
 def check_schedule(plan, lens, H, n_clusters):
+    """Every (request, head group) is covered exactly once by contiguous
+    whole-tile chunks; split chunks own partial slots (shared by the head
+    groups of one chunk); the workspace holds them."""
     items = plan.work_items()
+    heads = plan.work_item_heads()
     B = len(lens)
-    covered = {b: [] for b in range(B)}
-    slots = []
-    for (b, t0, t1, slot, cl) in items:
+    groups = [(g, min(H, g + 128)) for g in range(0, H, 128)]
+    covered = {(b, hg): [] for b in range(B) for hg in groups}
+    slots = set()
+    for (b, t0, t1, slot, cl), hg in zip(items, heads):
         assert 0 <= cl < n_clusters
+        assert hg in groups
         assert t0 % TILE == 0 and t0 <= t1 <= lens[b]
-        covered[b].append((t0, t1, slot))
+        covered[(b, hg)].append((t0, t1, slot))
         if slot >= 0:
-            slots.append(slot)
-    for b in range(B):
-        segs = sorted(covered[b])
+            slots.add(slot)
+    for (b, hg), segs in covered.items():
+        segs = sorted(segs)
         assert len(segs) == plan.num_splits(b)
         if lens[b] == 0:
             assert segs == [(0, 0, -1)]
@@ -61,7 +67,12 @@ def check_schedule(plan, lens, H, n_clusters):
         if len(segs) == 1:
             assert segs[0][2] == -1
         else:
-            assert all(s[2] >= 0 for s in segs)
+            assert all(sg[2] >= 0 for sg in segs)
+    # the head groups of one chunk share its slot
+    by_chunk = {}
+    for (b, t0, t1, slot, cl) in items:
+        by_chunk.setdefault((b, t0, t1), set()).add(slot)
+    assert all(len(v) == 1 for v in by_chunk.values())
     assert sorted(slots) == list(range(len(slots)))
     expect_ws = 0
     if slots:
@@ -97,6 +108,20 @@ def test_forced_splits(m, force):
         assert plan.num_splits(b) == max(1, min(force, int(tiles[b])))
 
 
+@pytest.mark.parametrize("H", [129, 256, 300, 1024])
+def test_head_groups_cover_every_head(m, H):
+    """H > 128: each chunk of each request is scheduled once per group of 128
+    heads (the last group holds the rest)."""
+    lens = np.array([5000, 96, 0, 1, 3000], dtype=np.int32)
+    plan = m.mla_decode_plan(5, H, lens, 32, 200, num_clusters=16, host_only=True)
+    check_schedule(plan, lens, H, 16)
+    ng = (H + 127) // 128
+    assert plan.num_work_items == ng * sum(plan.num_splits(b) for b in range(5))
+    forced = m.mla_decode_plan(5, H, lens, 32, 200, num_clusters=16, force_splits=3,
+                               host_only=True)
+    check_schedule(forced, lens, H, 16)
+
+
 def test_balance_with_few_pairs(m):
     rng = np.random.default_rng(0)
     lens = rng.integers(1, 4097, size=300).astype(np.int32)
@@ -108,7 +133,7 @@ def test_balance_with_few_pairs(m):
     assert load.max() <= 1.1 * load.mean()
 
 
-@pytest.mark.parametrize("bad", [dict(B=0), dict(H=0), dict(H=129), dict(bs=24), dict(bs=256),
+@pytest.mark.parametrize("bad", [dict(B=0), dict(H=0), dict(H=1025), dict(bs=24), dict(bs=256),
                                  dict(len=-1), dict(len=10**5)])
 def test_plan_rejects_bad_arguments(m, bad):
     B = bad.get("B", 2)

@@ -58,6 +58,17 @@ def test_head_counts(lib, oracle_mod, H):
     full_parity(oracle_mod, spec(f"h{H}", 3, H, 32, [1, 97, 300], seed=H))
 
 
+@pytest.mark.parametrize("H,splits", [(129, 0), (192, 2), (256, 0)])
+def test_head_groups_above_128(lib, oracle_mod, H, splits):
+    """More than 128 query heads: the plan runs each KV chunk once per group of
+    128 heads (the last group padded inside the kernel), every row against
+    the oracle, with and without split partials."""
+    w = spec(f"h{H}", 3, H, 32, [1, 700, 1300], seed=H)
+    _, _, plan = full_parity(oracle_mod, w, force_splits=splits)
+    heads = plan.work_item_heads()
+    assert {h for h, _ in heads} == set(range(0, H, 128))
+
+
 @pytest.mark.parametrize("bs", [16, 32, 64, 128])
 def test_block_sizes_ragged(lib, oracle_mod, bs):
     lens = [1, 15, 95, 96, 97, 191, 192, 193, 500]
@@ -242,7 +253,7 @@ def test_argument_errors(lib):
     with pytest.raises(m.MLAError) as e:
         m.mla_decode(plan, *args, -1.0, o, l, ws)          # sm_scale must be > 0
     assert e.value.status == 1
-    for bad in [dict(H=0), dict(H=129), dict(bs=48)]:
+    for bad in [dict(H=0), dict(H=1025), dict(bs=48)]:
         with pytest.raises(m.MLAError):
             m.mla_decode_plan(2, bad.get("H", 16), w["seq_lens"], bad.get("bs", 32),
                               int(w["max_blocks"]))
