@@ -28,7 +28,8 @@ struct mla_plan_s {
   int B = 0, H = 0, block_size = 0, max_blocks = 0;
   int device = -1;
   bool host_only = false;
-  int num_clusters = 0;
+  int num_clusters = 0;                  // CTA pairs the schedule may use
+  int num_launch = 0;                    // pairs that hold work items (launched)
   int force_splits = 0;
   std::vector<int32_t> seq_lens;
   std::vector<int32_t> splits;           // per request
@@ -36,6 +37,7 @@ struct mla_plan_s {
   std::vector<int32_t> item_cluster;     // parallel to items
   std::vector<int32_t> cluster_offsets;  // num_clusters + 1
   std::vector<CombineItem> combine;
+  int max_split = 0;                     // largest n_slots over the combine items
   int num_slots = 0;
   size_t workspace_bytes = 0;
   // Device copy of the schedule: [error word | items | offsets | combine].
@@ -93,7 +95,8 @@ mla_status_t prepare_device(int dev, int* clusters) {
   DeviceInfo& d = g_dev[dev];
   if (!d.prepared) {
     if (!device_is_sm103(dev)) return MLA_ERR_UNSUPPORTED_DEVICE;
-    if (mla::decode_prepare_device() != cudaSuccess) return MLA_ERR_CUDA;
+    if (mla::decode_prepare_device() != cudaSuccess || mla::combine_prepare_device() != cudaSuccess)
+      return MLA_ERR_CUDA;
     int n = 0;
     if (mla::decode_max_clusters(&n) != cudaSuccess || n <= 0) return MLA_ERR_CUDA;
     d.clusters = n;
@@ -343,6 +346,7 @@ void build_schedule(mla_plan_s* p) {
   std::vector<int> count(B, 0);
   for (const Piece& pc : best) count[pc.b]++;
   p->splits.assign(B, 0);
+  p->max_split = 0;
   std::vector<int> first_slot(B, -1);
   int slots = 0;
   p->combine.clear();
@@ -352,6 +356,7 @@ void build_schedule(mla_plan_s* p) {
       first_slot[b] = slots;
       p->combine.push_back({b, slots, count[b], 0});
       slots += count[b];
+      p->max_split = std::max(p->max_split, count[b]);
     }
   }
   // A split piece owns one partial slot, shared by its head groups (each
@@ -372,19 +377,23 @@ void build_schedule(mla_plan_s* p) {
     }
   }
   // Group by pair, each pair's list in assignment order (longest first).
+  // Pairs left without items are dropped, so only pairs with work launch.
   std::vector<std::vector<int>> per(nc);
   for (int i : order) per[owner[i]].push_back(i);
   p->items.clear();
   p->item_cluster.clear();
-  p->cluster_offsets.assign(nc + 1, 0);
+  p->cluster_offsets.clear();
   for (int c = 0; c < nc; ++c) {
-    p->cluster_offsets[c] = static_cast<int32_t>(p->items.size());
+    if (per[c].empty()) continue;
+    const int launched = static_cast<int>(p->cluster_offsets.size());
+    p->cluster_offsets.push_back(static_cast<int32_t>(p->items.size()));
     for (int i : per[c]) {
       p->items.push_back(piece_item[i]);
-      p->item_cluster.push_back(c);
+      p->item_cluster.push_back(launched);
     }
   }
-  p->cluster_offsets[nc] = static_cast<int32_t>(p->items.size());
+  p->num_launch = static_cast<int>(p->cluster_offsets.size());
+  p->cluster_offsets.push_back(static_cast<int32_t>(p->items.size()));
   p->num_slots = slots;
   const size_t o_bytes = static_cast<size_t>(slots) * p->H * mla::kDc * 4;
   const size_t l_bytes = static_cast<size_t>(slots) * p->H * 4;
@@ -603,7 +612,7 @@ int mla_plan_num_splits(mla_plan_t p, int b) {
 
 int mla_plan_num_work_items(mla_plan_t p) { return p ? static_cast<int>(p->items.size()) : -1; }
 
-int mla_plan_num_clusters(mla_plan_t p) { return p ? p->num_clusters : -1; }
+int mla_plan_num_clusters(mla_plan_t p) { return p ? p->num_launch : -1; }
 
 int mla_plan_work_item_heads(mla_plan_t p, int i, int32_t* h_begin, int32_t* h_end) {
   if (!p || i < 0 || i >= static_cast<int>(p->items.size())) return -1;
@@ -679,7 +688,7 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (mla::launch_decode(dp, p->num_clusters, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (mla::launch_decode(dp, p->num_launch, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (!p->combine.empty()) {
     mla::CombineParams cp;
     cp.items = reinterpret_cast<const CombineItem*>(p->d_buf + p->off_combine);
@@ -688,7 +697,8 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
     cp.out = dp.out;
     cp.lse = lse;
     cp.H = p->H;
-    if (mla::launch_combine(cp, static_cast<int>(p->combine.size()), s) != cudaSuccess)
+    if (mla::launch_combine(cp, static_cast<int>(p->combine.size()), p->max_split, s) !=
+        cudaSuccess)
       return MLA_ERR_CUDA;
   }
   return MLA_OK;
@@ -782,7 +792,7 @@ mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q
   dp.max_blocks = p->max_blocks;
   dp.num_blocks = num_blocks;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
-  if (mla::launch_decode(dp, p->num_clusters, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (mla::launch_decode(dp, p->num_launch, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (!p->combine.empty()) {
     mla::CombineParams cp;
     cp.items = reinterpret_cast<const CombineItem*>(scratch + p->off_combine);
@@ -791,7 +801,8 @@ mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q
     cp.out = dp.out;
     cp.lse = lse;
     cp.H = p->H;
-    if (mla::launch_combine(cp, static_cast<int>(p->combine.size()), s) != cudaSuccess)
+    if (mla::launch_combine(cp, static_cast<int>(p->combine.size()), p->max_split, s) !=
+        cudaSuccess)
       return MLA_ERR_CUDA;
   }
   return MLA_OK;

@@ -128,7 +128,10 @@ struct CombineParams {
 
 // Launchers (defined in the .cu files).
 cudaError_t launch_decode(const DecodeParams& p, int num_clusters, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams& p, int num_items, cudaStream_t stream);
+// max_slots: the largest n_slots of the combine items (at most 4096).
+cudaError_t launch_combine(const CombineParams& p, int num_items, int max_slots,
+                           cudaStream_t stream);
+cudaError_t combine_prepare_device();
 cudaError_t decode_max_clusters(int* num_clusters);
 cudaError_t decode_prepare_device();
 // One-warp kernel whose wait on a barrier nothing completes must time out
