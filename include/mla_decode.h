@@ -66,6 +66,13 @@ typedef struct {
   int host_only;      /* nonzero: build the schedule on the host only (no device upload,
                          no device query unless num_clusters == 0); such a plan can be
                          inspected but not passed to mla_decode */
+  int lengths_are_bounds; /* nonzero: seq_lens_host are upper bounds. The schedule (pairs,
+                         splits, workspace) is built for the bounds, and on every call the
+                         kernels read each request's length L from the device seq_lens
+                         (0 <= L <= bound; a larger L raises MLA_DEVERR_SEQLEN_MISMATCH and
+                         is clamped to the bound). The launch then does not depend on the
+                         lengths: one mla_decode captured in a CUDA graph can be replayed
+                         as the lengths change, with no plan update between replays. */
 } mla_plan_options_t;
 
 /*

@@ -38,7 +38,7 @@ class MLAError(RuntimeError):
 
 class PlanOptions(ctypes.Structure):
     _fields_ = [("num_clusters", ctypes.c_int), ("force_splits", ctypes.c_int),
-                ("host_only", ctypes.c_int)]
+                ("host_only", ctypes.c_int), ("lengths_are_bounds", ctypes.c_int)]
 
 
 def _load() -> ctypes.CDLL:
@@ -165,12 +165,18 @@ class Plan:
 
 
 def mla_decode_plan(B: int, H: int, seq_lens_host, block_size: int, max_blocks: int,
-                    num_clusters: int = 0, force_splits: int = 0, host_only: bool = False) -> Plan:
-    """Build the split-KV schedule (host-only; uploads a small work list)."""
+                    num_clusters: int = 0, force_splits: int = 0, host_only: bool = False,
+                    lengths_are_bounds: bool = False) -> Plan:
+    """Build the split-KV schedule (host-only; uploads a small work list).
+
+    With ``lengths_are_bounds`` the host lengths are upper bounds and every
+    decode reads the true lengths from the device ``seq_lens`` (a launch that
+    can be captured once in a CUDA graph and replayed as lengths change)."""
     lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
     if lens.shape != (B,):
         raise ValueError(f"seq_lens must have shape ({B},)")
-    opts = PlanOptions(int(num_clusters), int(force_splits), 1 if host_only else 0)
+    opts = PlanOptions(int(num_clusters), int(force_splits), 1 if host_only else 0,
+                       1 if lengths_are_bounds else 0)
     h = ctypes.c_void_p()
     _check(LIB.mla_decode_plan_ex(B, H, lens.ctypes.data_as(ctypes.c_void_p), block_size,
                                   max_blocks, ctypes.byref(opts), ctypes.byref(h)),

@@ -31,6 +31,7 @@ struct mla_plan_s {
   int num_clusters = 0;                  // CTA pairs the schedule may use
   int num_launch = 0;                    // pairs that hold work items (launched)
   int force_splits = 0;
+  bool lengths_are_bounds = false;       // seq_lens are upper bounds; kernels read the true ones
   std::vector<int32_t> seq_lens;
   std::vector<int32_t> splits;           // per request
   std::vector<WorkItem> items;           // grouped by CTA pair
@@ -557,6 +558,7 @@ mla_status_t mla_decode_plan_ex(int B, int H, const int32_t* seq_lens_host, int 
   p->max_blocks = max_blocks;
   p->host_only = o.host_only != 0;
   p->force_splits = o.force_splits;
+  p->lengths_are_bounds = o.lengths_are_bounds != 0;
   p->seq_lens.assign(seq_lens_host, seq_lens_host + B);
   if (!p->host_only || o.num_clusters == 0) {
     int dev = 0;
@@ -686,6 +688,7 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   dp.max_blocks = p->max_blocks;
   dp.num_blocks = num_blocks;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  dp.dynamic_lens = p->lengths_are_bounds ? 1 : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (mla::launch_decode(dp, p->num_launch, s) != cudaSuccess) return MLA_ERR_CUDA;
@@ -792,6 +795,7 @@ mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q
   dp.max_blocks = p->max_blocks;
   dp.num_blocks = num_blocks;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  dp.dynamic_lens = p->lengths_are_bounds ? 1 : 0;
   if (mla::launch_decode(dp, p->num_launch, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (!p->combine.empty()) {
     mla::CombineParams cp;

@@ -90,6 +90,15 @@ MLA_DEVI int tiles_of(const WorkItem& it) {
   return it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
 }
 
+// Work item i of the schedule. With lengths planned as upper bounds, its end
+// is clamped to the request's length read from the device on every call, so
+// one schedule (and one captured launch) serves any lengths up to the bounds.
+MLA_DEVI WorkItem item_at(const DecodeParams& p, int i) {
+  WorkItem w = p.items[i];
+  if (p.dynamic_lens) w.t1 = max(w.t0, min(w.t1, __ldg(&p.seq_lens[w.b])));
+  return w;
+}
+
 // Query heads of an item's head group: heads [h0, h0 + heads_of) of the
 // request, at most 128 (the MMA M; fewer are padded inside the kernel).
 MLA_DEVI int heads_of(const DecodeParams& p, const WorkItem& it) {
@@ -196,8 +205,11 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
   bool ok = true;
   const int n = pieces_per_tile(p.block_size);
   for (int it = it0; it < it1 && ok; ++it) {
-    const WorkItem w = p.items[it];
-    if (lane == 0 && __ldg(&p.seq_lens[w.b]) != w.seq_len) err |= 2u;  // MLA_DEVERR_SEQLEN_MISMATCH
+    const WorkItem w = item_at(p, it);
+    if (lane == 0) {   // MLA_DEVERR_SEQLEN_MISMATCH: not the planned length, or above the bound
+      const int len = __ldg(&p.seq_lens[w.b]);
+      if (p.dynamic_lens ? (len < 0 || len > w.seq_len) : len != w.seq_len) err |= 2u;
+    }
     PageWindow win;
     const int nt = tiles_of(w);
     for (int i = 0; i < nt && ok; ++i, ++g) {
@@ -205,7 +217,7 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
       // they are loaded (earlier, the streaming cache would evict them).
       if (lane == 0 && i == max(nt - kQPrefetchLead, 0)) {
         for (int nx = it + 1; nx < it1; ++nx) {
-          const WorkItem wn = p.items[nx];
+          const WorkItem wn = item_at(p, nx);
           if (tiles_of(wn) == 0) continue;
           const int64_t qrow = static_cast<int64_t>(wn.b) * p.H + wn.h0;
           const int nh = heads_of(p, wn);
@@ -261,7 +273,7 @@ MLA_DEVI void score_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0
   int g = 0;
   const int n = pieces_per_tile(p.block_size);
   for (int it = it0; it < it1; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = item_at(p, it);
     const int nt = tiles_of(w);
     PageWindow win;
     for (int i = 0; i < nt; ++i, ++g) {
@@ -316,7 +328,7 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
   bool ok = true;
   constexpr uint32_t idesc = kIdescS;
   for (int it = it0; it < it1 && ok; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = item_at(p, it);
     const int nt = tiles_of(w);
     if (nt == 0) continue;
     const uint32_t q_par = n_items & 1;
@@ -448,9 +460,9 @@ MLA_DEVI void score_qloader(const DecodeParams& p, Ctrl* c, uint32_t tmem, int w
   const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   int n_items = 0;
   for (int it = it0; it < it1; ++it) {
-    if (tiles_of(p.items[it]) == 0) continue;
+    if (tiles_of(item_at(p, it)) == 0) continue;
     const int wait_parity = n_items > 0 ? (n_items - 1) & 1 : -1;
-    if (!load_q(p, c, p.items[it], row, trow, wait_parity)) {
+    if (!load_q(p, c, item_at(p, it), row, trow, wait_parity)) {
       if (lane == 0) report(p, 4u);
       return;
     }
@@ -524,12 +536,12 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
   int g = 0;
   bool ok = true;
   int cur = it0;
-  while (cur < it1 && tiles_of(p.items[cur]) == 0) ++cur;
+  while (cur < it1 && tiles_of(item_at(p, cur)) == 0) ++cur;
   while (cur < it1 && ok) {
-    const WorkItem w = p.items[cur];
+    const WorkItem w = item_at(p, cur);
     const int nt = tiles_of(w);
     int nxt = cur + 1;
-    while (nxt < it1 && tiles_of(p.items[nxt]) == 0) ++nxt;
+    while (nxt < it1 && tiles_of(item_at(p, nxt)) == 0) ++nxt;
     float m_used = -INFINITY, l = 0.0f;
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
@@ -614,7 +626,7 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
   int h = 0;
   bool ok = true;
   for (int it = it0; it < it1 && ok; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = item_at(p, it);
     const int nt = tiles_of(w);
     PageWindow win;
     for (int i = 0; i < nt && ok; ++i) {
@@ -661,7 +673,7 @@ MLA_DEVI void out_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0, 
   volatile int32_t* seen = &c->p_seen;
   int g = 0;
   for (int it = it0; it < it1; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = item_at(p, it);
     const int nt = tiles_of(w);
     const int n_pages = (w.t1 + p.block_size - 1) / p.block_size;
     PageWindow win;
@@ -706,7 +718,7 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
   bool ok = true;
   uint8_t* pbufs = data + kNumVSlots * kVHalfBytes;
   for (int it = it0; it < it1 && ok; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = item_at(p, it);
     const int nt = tiles_of(w);
     if (nt == 0) continue;
     const int item = n_items++;
@@ -801,22 +813,24 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
   const bool elected = (warp == 2 && lane == 0);
   const uint8_t* recs = data + kNumVSlots * kVHalfBytes + kNumPBufs * kPBytes;
   int total = 0;
-  for (int it = it0; it < it1; ++it) total += tiles_of(p.items[it]);
+  for (int it = it0; it < it1; ++it) total += tiles_of(item_at(p, it));
   if (elected)
     for (int k = 0; k < kNumPBufs && k < total; ++k)
       mbar_arrive_expect_tx(smem_addr(&c->p_full[k]), kPMsgBytes);
   int g = 0, r = 0;
   bool ok = true;
   for (int it = it0; it < it1 && ok; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = item_at(p, it);
     const int nt = tiles_of(w);
     const bool active = row < heads_of(p, w);
     const int64_t orow = static_cast<int64_t>(w.b) * p.H + w.h0 + row;
-    if (nt == 0) {  // empty request: out = 0, lse = -inf
+    if (nt == 0) {  // no tokens: out = 0, lse = -inf (a split piece: an empty partial)
       if (active && w.slot < 0) {
         uint4* o = reinterpret_cast<uint4*>(p.out + orow * kDc);
         for (int e = 0; e < kDc / 8; ++e) o[e] = make_uint4(0u, 0u, 0u, 0u);
         p.lse[orow] = -INFINITY;
+      } else if (active) {
+        p.part_lse[static_cast<int64_t>(w.slot) * p.H + w.h0 + row] = -INFINITY;
       }
       continue;
     }

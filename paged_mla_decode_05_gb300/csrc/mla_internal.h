@@ -115,6 +115,7 @@ struct DecodeParams {
   int max_blocks;
   int64_t num_blocks;
   float scale_log2;               // sm_scale * log2(e)
+  int dynamic_lens;               // 1: planned lengths are upper bounds; items end at the device length
 };
 
 struct CombineParams {

@@ -306,3 +306,49 @@ def test_plan_update_growth_keeps_error_word_and_parity(lib, oracle_mod):
     ref_o, ref_l = oracle_mod.mla_decode(*oracle_args(w))
     assert_parity(out.float().cpu().numpy().astype(np.float64),
                   lse.cpu().numpy().astype(np.float64), ref_o, ref_l, "after growth")
+
+
+def test_graph_replay_with_length_bounds(lib, oracle_mod):
+    """A plan built for upper bounds on the lengths: one mla_decode captured in
+    a CUDA graph, replayed with three different device length vectors (no
+    plan update in between), each compared with the oracle. Lengths below a
+    split piece's start leave that piece empty (an empty partial)."""
+    import torch
+    m = lib
+    bounds = [1500, 700, 300, 2000, 96]
+    w = spec("bounds", 5, 32, 32, bounds, seed=23)
+    t = to_device(w)
+    plan = m.mla_decode_plan(5, 32, np.array(bounds, dtype=np.int32), 32, int(w["max_blocks"]),
+                             num_clusters=8, lengths_are_bounds=True)
+    assert any(plan.num_splits(b) > 1 for b in range(5))
+    out = torch.empty((5, 32, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((5, 32), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+    lens_dev = torch.tensor(bounds, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        m.mla_decode(plan, t["q_nope"], t["q_pe"], t["kv_cache"], t["block_table"], lens_dev,
+                     float(w["sm_scale"]), out, lse, ws, stream)     # warm-up outside capture
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            m.mla_decode(plan, t["q_nope"], t["q_pe"], t["kv_cache"], t["block_table"], lens_dev,
+                         float(w["sm_scale"]), out, lse, ws, stream)
+    for lens in ([1500, 700, 300, 2000, 96], [1, 650, 0, 1999, 95], [801, 96, 299, 40, 0]):
+        lens_dev.copy_(torch.tensor(lens, dtype=torch.int32))
+        out.fill_(float("nan"))
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        assert m.mla_check_device_error(plan, stream) == 0
+        w2 = dict(w)
+        w2["seq_lens"] = np.array(lens, dtype=np.int32)
+        ref_o, ref_l = oracle_mod.mla_decode(*oracle_args(w2))
+        assert_parity(out.float().cpu().numpy().astype(np.float64),
+                      lse.cpu().numpy().astype(np.float64), ref_o, ref_l, f"bounds replay {lens}")
+    # a length above its bound is reported (and clamped)
+    lens_dev.copy_(torch.tensor([1501, 700, 300, 2000, 96], dtype=torch.int32))
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    assert m.mla_check_device_error(plan, stream) == m.MLA_DEVERR_SEQLEN_MISMATCH
