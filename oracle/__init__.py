@@ -61,11 +61,14 @@ def _load():
         common = [i32, i32, p, p, p, i64, i32, p, i32, p, dbl]
         lib.oracle_mla_decode_rows.argtypes = common + [i64, p, p, p, p, i32]
         lib.oracle_mla_decode.argtypes = common + [p, p, i32]
+        lib.oracle_mla_decode_multi.argtypes = [i32, i32, i32, p, p, p, i64, i32, p, i32, p, dbl,
+                                                p, p, i32]
         lib.oracle_mla_partial.argtypes = common + [i32, i32, i64, i64, p, p]
         lib.oracle_mla_combine.argtypes = [i32, p, p, p, p]
         lib.oracle_mla_decode_bruteforce.argtypes = common + [p, p]
         lib.oracle_num_threads.argtypes = [i32]
-        for fn in (lib.oracle_mla_decode_rows, lib.oracle_mla_decode, lib.oracle_mla_partial,
+        for fn in (lib.oracle_mla_decode_rows, lib.oracle_mla_decode, lib.oracle_mla_decode_multi,
+                   lib.oracle_mla_partial,
                    lib.oracle_mla_combine, lib.oracle_mla_decode_bruteforce,
                    lib.oracle_num_threads):
             fn.restype = ctypes.c_int
@@ -118,6 +121,26 @@ def mla_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale, n_thread
     lse = np.empty((B, H), dtype=np.float64)
     _check(_load().oracle_mla_decode(*args, _ptr(out), _ptr(lse), int(n_threads)),
            "oracle_mla_decode")
+    del keep
+    return out, lse
+
+
+def mla_decode_multi(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale, n_threads: int = 0):
+    """Multi-token (speculative) decode: q_nope [B, q_len, H, 512], q_pe
+    [B, q_len, H, 64]; query token j of request b attends to its first
+    L - q_len + 1 + j tokens. Returns (out [B, q_len, H, 512], lse [B, q_len, H])."""
+    q_nope = np.ascontiguousarray(q_nope, dtype=np.uint16)
+    q_pe = np.ascontiguousarray(q_pe, dtype=np.uint16)
+    B, q_len, H, dc = q_nope.shape
+    assert dc == D_C and q_pe.shape == (B, q_len, H, D_R), (q_nope.shape, q_pe.shape)
+    args, keep = _common(q_nope.reshape(B, q_len * H, D_C), q_pe.reshape(B, q_len * H, D_R),
+                         kv_cache, block_table, seq_lens, sm_scale)
+    out = np.empty((B, q_len, H, D_C), dtype=np.float64)
+    lse = np.empty((B, q_len, H), dtype=np.float64)
+    (_, _, qn, qp, kv, nb, bs, bt, mb, sl, sc) = args
+    _check(_load().oracle_mla_decode_multi(B, q_len, H, qn, qp, kv, nb, bs, bt, mb, sl, sc,
+                                           _ptr(out), _ptr(lse), int(n_threads)),
+           "oracle_mla_decode_multi")
     del keep
     return out, lse
 

@@ -199,6 +199,44 @@ int oracle_mla_decode(int B, int H, const uint16_t* q_nope, const uint16_t* q_pe
                                 rh.data(), out, lse, n_threads);
 }
 
+// Multi-token decode (speculative decoding: q_len new tokens per request).
+// q_nope [B, q_len, H, 512], q_pe [B, q_len, H, 64]; the request's length L
+// counts the q_len new tokens, which are its last q_len tokens, so query
+// token j (0-based) attends causally to tokens t < L - q_len + 1 + j.
+// Writes out[B, q_len, H, 512] and lse[B, q_len, H]. Requires L == 0 (all
+// rows empty: out = 0, lse = -inf) or L >= q_len. The causal rule is the
+// reading taken where the pages only name speculative decoding.
+int oracle_mla_decode_multi(int B, int q_len, int H, const uint16_t* q_nope,
+                            const uint16_t* q_pe, const uint16_t* kv_cache, int64_t num_blocks,
+                            int block_size, const int32_t* block_table, int max_blocks,
+                            const int32_t* seq_lens, double sm_scale, double* out, double* lse,
+                            int n_threads) {
+  if (B < 0 || H < 1 || q_len < 1) return ORACLE_ERR_ARG;
+  // The request's q_len x H query rows, row j * H + h, share its cache.
+  Inputs in{B, q_len * H, q_nope, q_pe, kv_cache, num_blocks, block_size,
+            block_table, max_blocks, seq_lens, sm_scale};
+  if (!valid_shape(in)) return ORACLE_ERR_ARG;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens[b] != 0 && seq_lens[b] < q_len) return ORACLE_ERR_ARG;
+  set_threads(n_threads);
+  const int64_t n = static_cast<int64_t>(B) * q_len * H;
+  int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n; ++r) {
+    const int b = static_cast<int>(r / (static_cast<int64_t>(q_len) * H));
+    const int row = static_cast<int>(r % (static_cast<int64_t>(q_len) * H));   // j * H + h
+    const int j = row / H;
+    const int64_t L = seq_lens[b];
+    const int64_t Lj = L == 0 ? 0 : L - q_len + 1 + j;
+    const int rc = attend_range(in, b, row, 0, Lj, out + r * kDc, lse + r);
+    if (rc != ORACLE_OK) {
+#pragma omp critical
+      status = rc;
+    }
+  }
+  return status;
+}
+
 // Split-KV partial of one (b, h) over tokens [t0, t1): the normalised partial
 // output o[512] and that range's log-sum-exp. This is what one split of the
 // split-KV decode produces before the reduction step.
