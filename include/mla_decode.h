@@ -73,6 +73,13 @@ typedef struct {
                          is clamped to the bound). The launch then does not depend on the
                          lengths: one mla_decode captured in a CUDA graph can be replayed
                          as the lengths change, with no plan update between replays. */
+  int q_len;          /* query tokens per request (0 or 1: one; more: speculative decoding).
+                         The request's length L counts them as its last q_len tokens and
+                         query token j attends to its first L - q_len + 1 + j tokens (each
+                         L must be 0 or at least q_len). q_nope, q_pe, out and lse then have
+                         a q_len dimension after B: [B, q_len, H, ...]; the q_len * H query
+                         rows of a request share its latent KV and are processed as one
+                         request with q_len * H heads (at most 1024). */
 } mla_plan_options_t;
 
 /*
@@ -125,14 +132,16 @@ int mla_plan_num_clusters(mla_plan_t plan);       /* CTA pairs launched */
  * out/lse directly) and the CTA pair that runs it. */
 int mla_plan_work_item(mla_plan_t plan, int i, int32_t* b, int32_t* t0, int32_t* t1,
                        int32_t* slot, int32_t* cluster);
-/* Query heads [*h_begin, *h_end) of work item i: its head group (128 heads,
- * or the rest of H for the last group). */
+/* Query rows [*h_begin, *h_end) of work item i: its head group (128 rows, or
+ * the rest for the last group). A request's rows are its heads (j * H + h for
+ * query token j with several query tokens). */
 int mla_plan_work_item_heads(mla_plan_t plan, int i, int32_t* h_begin, int32_t* h_end);
 
 /*
  * mla_decode — one decode step over the paged latent cache.
  *
- *  q_nope       device bf16 [B, H, 512]   16-byte aligned
+ *  q_nope       device bf16 [B, H, 512]   16-byte aligned ([B, q_len, H, 512]
+ *               for a plan with q_len > 1; likewise q_pe, out and lse)
  *  q_pe         device bf16 [B, H, 64]    16-byte aligned
  *  kv_cache     device bf16 [num_blocks, block_size, 576]; each row is 512
  *               c_kv columns then 64 k_pe columns; 16-byte aligned

@@ -38,7 +38,8 @@ class MLAError(RuntimeError):
 
 class PlanOptions(ctypes.Structure):
     _fields_ = [("num_clusters", ctypes.c_int), ("force_splits", ctypes.c_int),
-                ("host_only", ctypes.c_int), ("lengths_are_bounds", ctypes.c_int)]
+                ("host_only", ctypes.c_int), ("lengths_are_bounds", ctypes.c_int),
+                ("q_len", ctypes.c_int)]
 
 
 def _load() -> ctypes.CDLL:
@@ -98,10 +99,16 @@ class Plan:
     """Owns an ``mla_plan_t``; freed on ``destroy()`` or garbage collection."""
 
     def __init__(self, handle: int, B: int, H: int, block_size: int, max_blocks: int,
-                 host_only: bool):
+                 host_only: bool, q_len: int = 1):
         self._h = ctypes.c_void_p(handle)
         self.B, self.H, self.block_size, self.max_blocks = B, H, block_size, max_blocks
         self.host_only = host_only
+        self.q_len = q_len
+
+    def q_shape(self, d: int):
+        """Shape of a per-query-row tensor with trailing dimension d (None: none)."""
+        lead = (self.B, self.H) if self.q_len == 1 else (self.B, self.q_len, self.H)
+        return lead if d is None else lead + (d,)
 
     @property
     def handle(self) -> ctypes.c_void_p:
@@ -166,22 +173,24 @@ class Plan:
 
 def mla_decode_plan(B: int, H: int, seq_lens_host, block_size: int, max_blocks: int,
                     num_clusters: int = 0, force_splits: int = 0, host_only: bool = False,
-                    lengths_are_bounds: bool = False) -> Plan:
+                    lengths_are_bounds: bool = False, q_len: int = 1) -> Plan:
     """Build the split-KV schedule (host-only; uploads a small work list).
 
     With ``lengths_are_bounds`` the host lengths are upper bounds and every
     decode reads the true lengths from the device ``seq_lens`` (a launch that
-    can be captured once in a CUDA graph and replayed as lengths change)."""
+    can be captured once in a CUDA graph and replayed as lengths change).
+    ``q_len`` > 1: several query tokens per request (speculative decoding);
+    query tensors and outputs then take the shape [B, q_len, H, ...]."""
     lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
     if lens.shape != (B,):
         raise ValueError(f"seq_lens must have shape ({B},)")
     opts = PlanOptions(int(num_clusters), int(force_splits), 1 if host_only else 0,
-                       1 if lengths_are_bounds else 0)
+                       1 if lengths_are_bounds else 0, int(q_len))
     h = ctypes.c_void_p()
     _check(LIB.mla_decode_plan_ex(B, H, lens.ctypes.data_as(ctypes.c_void_p), block_size,
                                   max_blocks, ctypes.byref(opts), ctypes.byref(h)),
            "mla_decode_plan")
-    return Plan(h.value, B, H, block_size, max_blocks, host_only)
+    return Plan(h.value, B, H, block_size, max_blocks, host_only, int(q_len))
 
 
 def _stream_ptr(stream) -> ctypes.c_void_p:
@@ -225,14 +234,14 @@ def mla_decode(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, sm_sca
         raise ValueError(f"kv_cache must have shape [num_blocks, {plan.block_size}, {D}]")
     nb = int(kv_cache.shape[0])
     args = [
-        _tensor(q_nope, torch.bfloat16, (B, H, D_C), "q_nope"),
-        _tensor(q_pe, torch.bfloat16, (B, H, D_R), "q_pe"),
+        _tensor(q_nope, torch.bfloat16, plan.q_shape(D_C), "q_nope"),
+        _tensor(q_pe, torch.bfloat16, plan.q_shape(D_R), "q_pe"),
         _tensor(kv_cache, torch.bfloat16, (nb, plan.block_size, D), "kv_cache"),
     ]
     bt = _tensor(block_table, torch.int32, (B, plan.max_blocks), "block_table")
     sl = _tensor(seq_lens, torch.int32, (B,), "seq_lens")
-    o = _tensor(out, torch.bfloat16, (B, H, D_C), "out")
-    l = _tensor(lse, torch.float32, (B, H), "lse")
+    o = _tensor(out, torch.bfloat16, plan.q_shape(D_C), "out")
+    l = _tensor(lse, torch.float32, plan.q_shape(None), "lse")
     if workspace is None:
         ws, ws_bytes = ctypes.c_void_p(0), 0
     else:
@@ -263,14 +272,14 @@ def mla_decode_no_alloc(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_len
         raise ValueError(f"kv_cache must have shape [num_blocks, {plan.block_size}, {D}]")
     nb = int(kv_cache.shape[0])
     args = [
-        _tensor(q_nope, torch.bfloat16, (B, H, D_C), "q_nope"),
-        _tensor(q_pe, torch.bfloat16, (B, H, D_R), "q_pe"),
+        _tensor(q_nope, torch.bfloat16, plan.q_shape(D_C), "q_nope"),
+        _tensor(q_pe, torch.bfloat16, plan.q_shape(D_R), "q_pe"),
         _tensor(kv_cache, torch.bfloat16, (nb, plan.block_size, D), "kv_cache"),
     ]
     bt = _tensor(block_table, torch.int32, (B, plan.max_blocks), "block_table")
     sl = _tensor(seq_lens, torch.int32, (B,), "seq_lens")
-    o = _tensor(out, torch.bfloat16, (B, H, D_C), "out")
-    l = _tensor(lse, torch.float32, (B, H), "lse")
+    o = _tensor(out, torch.bfloat16, plan.q_shape(D_C), "out")
+    l = _tensor(lse, torch.float32, plan.q_shape(None), "lse")
     eb = _tensor(err_bits, torch.int32, (1,), "err_bits")
     _check(LIB.mla_decode_no_alloc(plan.handle, args[0], args[1], args[2], nb, bt, sl,
                                    ctypes.c_float(sm_scale), o, l, eb, _stream_ptr(stream)),

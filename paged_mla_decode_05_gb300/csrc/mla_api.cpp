@@ -25,7 +25,10 @@ using mla::CombineItem;
 using mla::WorkItem;
 
 struct mla_plan_s {
+  // H: query rows per request (q_len * heads); the kernels and the schedule
+  // work in rows, heads and q_len are what the caller passed.
   int B = 0, H = 0, block_size = 0, max_blocks = 0;
+  int heads = 0, q_len = 1;
   int device = -1;
   bool host_only = false;
   int num_clusters = 0;                  // CTA pairs the schedule may use
@@ -407,14 +410,18 @@ void build_schedule(mla_plan_s* p) {
 }
 
 mla_status_t check_plan_args(int B, int H, const int32_t* seq_lens, int block_size,
-                             int max_blocks) {
-  if (B < 1 || H < 1 || H > mla::kMaxPlanHeads || !seq_lens || max_blocks < 1) return MLA_ERR_INVALID_ARG;
+                             int max_blocks, int q_len = 1) {
+  if (B < 1 || H < 1 || q_len < 1 || !seq_lens || max_blocks < 1) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(H) * q_len > mla::kMaxPlanHeads) return MLA_ERR_INVALID_ARG;
   if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
     return MLA_ERR_INVALID_ARG;
   const int64_t cap = static_cast<int64_t>(max_blocks) * block_size;
   if (cap >= (int64_t{1} << 30)) return MLA_ERR_INVALID_ARG;
-  for (int b = 0; b < B; ++b)
+  for (int b = 0; b < B; ++b) {
     if (seq_lens[b] < 0 || seq_lens[b] > cap) return MLA_ERR_INVALID_ARG;
+    // Several query tokens are the request's last tokens: it holds them all.
+    if (q_len > 1 && seq_lens[b] != 0 && seq_lens[b] < q_len) return MLA_ERR_INVALID_ARG;
+  }
   return MLA_OK;
 }
 
@@ -544,16 +551,20 @@ mla_status_t mla_decode_plan_ex(int B, int H, const int32_t* seq_lens_host, int 
                                 mla_plan_t* plan_out) {
   if (!plan_out) return MLA_ERR_INVALID_ARG;
   *plan_out = nullptr;
-  mla_status_t st = check_plan_args(B, H, seq_lens_host, block_size, max_blocks);
-  if (st != MLA_OK) return st;
   mla_plan_options_t o{};
   if (opts) o = *opts;
+  if (o.q_len < 0) return MLA_ERR_INVALID_ARG;
+  const int q_len = o.q_len > 0 ? o.q_len : 1;
+  mla_status_t st = check_plan_args(B, H, seq_lens_host, block_size, max_blocks, q_len);
+  if (st != MLA_OK) return st;
   if (o.num_clusters < 0 || o.force_splits < 0 || o.force_splits > kMaxForcedSplits)
     return MLA_ERR_INVALID_ARG;
   mla_plan_s* p = new (std::nothrow) mla_plan_s();
   if (!p) return MLA_ERR_INVALID_ARG;
   p->B = B;
-  p->H = H;
+  p->H = H * q_len;
+  p->heads = H;
+  p->q_len = q_len;
   p->block_size = block_size;
   p->max_blocks = max_blocks;
   p->host_only = o.host_only != 0;
@@ -594,7 +605,8 @@ mla_status_t mla_decode_plan(int B, int H, const int32_t* seq_lens_host, int blo
 
 mla_status_t mla_plan_update(mla_plan_t p, const int32_t* seq_lens_host, void* stream) {
   if (!p) return MLA_ERR_INVALID_ARG;
-  mla_status_t st = check_plan_args(p->B, p->H, seq_lens_host, p->block_size, p->max_blocks);
+  mla_status_t st =
+      check_plan_args(p->B, p->heads, seq_lens_host, p->block_size, p->max_blocks, p->q_len);
   if (st != MLA_OK) return st;
   if (!p->host_only) {
     int dev = -1;
@@ -684,6 +696,8 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   dp.cluster_offsets = reinterpret_cast<const int32_t*>(p->d_buf + p->off_offsets);
   dp.err = reinterpret_cast<uint32_t*>(p->d_buf);
   dp.H = p->H;
+  dp.q_len = p->q_len;
+  dp.heads = p->heads;
   dp.block_size = p->block_size;
   dp.max_blocks = p->max_blocks;
   dp.num_blocks = num_blocks;
@@ -791,6 +805,8 @@ mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q
   dp.cluster_offsets = reinterpret_cast<const int32_t*>(scratch + p->off_offsets);
   dp.err = err;
   dp.H = p->H;
+  dp.q_len = p->q_len;
+  dp.heads = p->heads;
   dp.block_size = p->block_size;
   dp.max_blocks = p->max_blocks;
   dp.num_blocks = num_blocks;

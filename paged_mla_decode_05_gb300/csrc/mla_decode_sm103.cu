@@ -95,8 +95,21 @@ MLA_DEVI int tiles_of(const WorkItem& it) {
 // one schedule (and one captured launch) serves any lengths up to the bounds.
 MLA_DEVI WorkItem item_at(const DecodeParams& p, int i) {
   WorkItem w = p.items[i];
-  if (p.dynamic_lens) w.t1 = max(w.t0, min(w.t1, __ldg(&p.seq_lens[w.b])));
+  w.len = w.seq_len;
+  if (p.dynamic_lens) {
+    w.len = max(0, min(w.seq_len, __ldg(&p.seq_lens[w.b])));
+    w.t1 = max(w.t0, min(w.t1, w.len));
+  }
   return w;
+}
+
+// End (exclusive) of the tokens that row `row` of item w attends to. With
+// several query tokens per request (row = j * heads + h of the request),
+// token j sees the request's first len - q_len + 1 + j tokens.
+MLA_DEVI int row_end(const DecodeParams& p, const WorkItem& w, int row) {
+  const int rr = w.h0 + row;
+  if (p.q_len <= 1 || rr >= p.H) return w.t1;
+  return min(w.t1, w.len - (p.q_len - 1) + rr / p.heads);
 }
 
 // Query heads of an item's head group: heads [h0, h0 + heads_of) of the
@@ -548,7 +561,8 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       const int k = g % kNumPBufs;
       const uint32_t ph = static_cast<uint32_t>(g / kNumPBufs) & 1u;   // P buffer use parity
       const uint32_t scol = trow + kTmemS0 + s * kTile;
-      const int valid = min(kTile, w.t1 - (w.t0 + i * kTile));
+      // Columns of this row's tile that it attends to (<= 0: none).
+      const int valid = min(kTile, row_end(p, w, row) - (w.t0 + i * kTile));
       if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->s_full[s]), (g >> 1) & 1))) {
         ok = false;
         break;
@@ -566,7 +580,7 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       tc_before_sync();
       mbar_arrive(smem_addr(&c->s_free[s]));
       if (row == 0) MLA_TRACE_AT(17, g);
-      if (valid < kTile) {   // the item's tail tile: columns past its end are -inf
+      if (valid < kTile) {   // columns past the row's end are -inf
 #pragma unroll
         for (int j = 0; j < kTile; ++j) r[j] = j < valid ? r[j] : 0xFF800000u;
       }
@@ -595,8 +609,9 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       }
       if (row == 0) MLA_TRACE_AT(5, g);
       const uint32_t bar = peer_pfull0 + k * 8;
-      l += softmax_tile(r, sl2x2, pack_f32x2(-m_used, -m_used), peer_pbuf0 + k * kPBytes + prow_off,
-                        bar);
+      // A row that has seen no token yet (m = -inf) writes p = 0.
+      const float mneg = m_used == -INFINITY ? 0.0f : -m_used;
+      l += softmax_tile(r, sl2x2, pack_f32x2(mneg, mneg), peer_pbuf0 + k * kPBytes + prow_off, bar);
       st_async_v4(peer_rec0 + (g % kNumRecSlots) * kRecBytes + row * 16, __float_as_uint(alpha),
                   __float_as_uint(l), __float_as_uint(m_used), 0u, bar);
       if (row == 0) MLA_TRACE_AT(6, g);
@@ -902,8 +917,10 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
       break;
     }
     tc_after_sync();
-    const float inv_l = 1.0f / l_fin;
-    const float lse_val = (m_fin + __log2f(l_fin)) * 0.69314718055994531f;
+    // A row without tokens in this item (possible with several query tokens
+    // per request) has l = 0: out = 0 and lse = -inf.
+    const float inv_l = l_fin > 0.0f ? 1.0f / l_fin : 0.0f;
+    const float lse_val = l_fin > 0.0f ? (m_fin + __log2f(l_fin)) * 0.69314718055994531f : -INFINITY;
     const bool to_out = w.slot < 0;
     uint16_t* out_row = (active && to_out) ? p.out + orow * kDc : nullptr;
     float* part_row = (active && !to_out)

@@ -74,8 +74,9 @@ struct WorkItem {
   int32_t t1;
   int32_t slot;
   int32_t seq_len;   // the plan's length of request b (checked against device seq_lens)
-  int32_t h0;        // first query head of the item's head group (a multiple of 128)
-  int32_t pad[2];
+  int32_t h0;        // first query row of the item's head group (a multiple of 128)
+  int32_t len;       // the request's length in this call (set on the device)
+  int32_t pad;
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 
@@ -110,7 +111,9 @@ struct DecodeParams {
   const WorkItem* items;          // grouped by CTA pair
   const int32_t* cluster_offsets; // [num_clusters + 1]
   uint32_t* err;                  // device error word
-  int H;
+  int H;                          // query rows per request: q_len * heads
+  int q_len;                      // query tokens per request (1: plain decode)
+  int heads;                      // query heads per token
   int block_size;
   int max_blocks;
   int64_t num_blocks;

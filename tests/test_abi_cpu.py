@@ -162,3 +162,22 @@ def test_selftest_argument_checks(m):
     bits = ctypes.c_uint32(7)
     assert lib.mla_selftest_wait_timeout(None, ctypes.byref(bits)) == 2   # UNSUPPORTED_DEVICE
     assert bits.value == 0
+
+
+@pytest.mark.parametrize("q_len,H", [(2, 16), (4, 16), (2, 128), (3, 100)])
+def test_multi_token_schedule(m, q_len, H):
+    """Several query tokens per request: the schedule covers the q_len * H
+    query rows of every request (in head groups of 128 rows)."""
+    lens = np.array([q_len, 700, 0, 2000, 97], dtype=np.int32)
+    plan = m.mla_decode_plan(5, H, lens, 32, 100, num_clusters=16, host_only=True, q_len=q_len)
+    check_schedule(plan, lens, q_len * H, 16)
+    assert plan.q_shape(512) == (5, q_len, H, 512)
+
+
+def test_multi_token_argument_checks(m):
+    with pytest.raises(m.MLAError):      # a request shorter than its query tokens
+        m.mla_decode_plan(2, 16, np.array([3, 100]), 32, 10, num_clusters=4, host_only=True,
+                          q_len=4)
+    with pytest.raises(m.MLAError):      # more than 1024 query rows per request
+        m.mla_decode_plan(2, 128, np.array([30, 100]), 32, 10, num_clusters=4, host_only=True,
+                          q_len=9)

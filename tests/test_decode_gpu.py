@@ -352,3 +352,61 @@ def test_graph_replay_with_length_bounds(lib, oracle_mod):
         g.replay()
     stream.synchronize()
     assert m.mla_check_device_error(plan, stream) == m.MLA_DEVERR_SEQLEN_MISMATCH
+
+
+def multi_spec(name, B, q_len, H, bs, lens, seed):
+    """A workload with q_len query tokens per request: the generator's draws
+    for q_len * H rows, viewed as [B, q_len, H, ...]."""
+    w = spec(name, B, q_len * H, bs, lens, seed)
+    w = dict(w)
+    w["q_len"], w["heads"] = q_len, H
+    return w
+
+
+def run_multi(oracle_mod, w, force_splits=0):
+    import torch
+    m = __import__("paged_mla_decode_05_gb300")
+    q_len, H, B = w["q_len"], w["heads"], int(w["B"])
+    t = to_device(w)
+    plan = m.mla_decode_plan(B, H, w["seq_lens"], int(w["block_size"]), int(w["max_blocks"]),
+                             force_splits=force_splits, q_len=q_len)
+    qn = t["q_nope"].view(B, q_len, H, 512)
+    qp = t["q_pe"].view(B, q_len, H, 64)
+    out = torch.full((B, q_len, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, q_len, H), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+    m.mla_decode(plan, qn, qp, t["kv_cache"], t["block_table"], t["seq_lens"],
+                 float(w["sm_scale"]), out, lse, ws)
+    assert m.mla_check_device_error(plan) == 0
+    ref_o, ref_l = oracle_mod.mla_decode_multi(
+        w["q_nope"].reshape(B, q_len, H, 512), w["q_pe"].reshape(B, q_len, H, 64), w["kv_cache"],
+        w["block_table"], w["seq_lens"], w["sm_scale"])
+    assert_parity(out.float().cpu().numpy().astype(np.float64),
+                  lse.cpu().numpy().astype(np.float64), ref_o, ref_l,
+                  f"{w['name']} q_len={q_len}")
+    return plan
+
+
+@pytest.mark.parametrize("q_len", [2, 4])
+def test_multi_token_v2lite_shape(lib, oracle_mod, q_len):
+    """Speculative decoding on the DeepSeek-V2-Lite shape (B=64, H=16,
+    lengths U{q_len..4096}, block size 64): every element against the oracle."""
+    lens = np.random.default_rng(40 + q_len).integers(q_len, 4096, size=64, endpoint=True)
+    run_multi(oracle_mod, multi_spec("v2lite_multi", 64, q_len, 16, 64, lens.tolist(), seed=q_len))
+
+
+@pytest.mark.parametrize("q_len", [2, 4])
+def test_multi_token_r1_shape(lib, oracle_mod, q_len):
+    """Speculative decoding on the DeepSeek-R1 shape (H=128: q_len * 128 query
+    rows per request in head groups of 128), lengths 1024 + U{0..2048}."""
+    lens = 1024 + np.random.default_rng(50 + q_len).integers(0, 2048, size=16, endpoint=True)
+    run_multi(oracle_mod, multi_spec("r1_multi", 16, q_len, 128, 32, lens.tolist(), seed=q_len))
+
+
+def test_multi_token_split_pieces_with_empty_rows(lib, oracle_mod):
+    """Forced splits put a piece of request 1 at tokens [576, 577), where the
+    first three of its four query tokens see no token: their partials are
+    empty (lse = -inf) and the combine must ignore them."""
+    w = multi_spec("multi_split", 3, 4, 16, 32, [4, 577, 300], seed=3)
+    plan = run_multi(oracle_mod, w, force_splits=7)
+    assert plan.num_splits(1) == 7
