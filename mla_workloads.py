@@ -27,6 +27,12 @@ fixed order):
      blocks (never -1, so a faulty reader sees sentinels instead of faulting);
   7. optionally ("peaky" rows) each valid token row is multiplied by 8 with
      probability 0.01 (exact in bf16).
+
+FP8 variant (``to_fp8``): the same workload with its cache stored as OCP E4M3
+bytes under one per-tensor scale, as an engine serving with an fp8 KV cache
+would hold it: byte = E4M3 round-to-nearest-even of (element / kv_scale),
+clipped to the largest finite magnitude 448, so the sentinels become +-448
+(standing for +-448 * kv_scale) and the N(0, 1) rows keep 4 significant bits.
 """
 from __future__ import annotations
 
@@ -202,6 +208,28 @@ def generate(spec: WorkloadSpec) -> Dict[str, object]:
     }
 
 
+FP8_KV_SCALE = 0.1            # per-tensor scale of the FP8 workloads (not a power of two)
+E4M3_MAX = 448.0
+
+
+def to_fp8(w: Dict[str, object], kv_scale: float = FP8_KV_SCALE) -> Dict[str, object]:
+    """The workload with its cache quantised to E4M3 bytes (see the recipe).
+
+    Adds ``kv_fp8`` (uint8, same shape as ``kv_cache``) and ``kv_scale``; the
+    bf16 ``kv_cache`` is dropped. Rounding uses torch's float8_e4m3fn cast
+    (round to nearest even) after clipping to +-448.
+    """
+    import torch
+    x = bf16_bits_to_f32(w["kv_cache"]) / np.float32(kv_scale)
+    np.clip(x, -E4M3_MAX, E4M3_MAX, out=x)
+    codes = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    out = {k: v for k, v in w.items() if k != "kv_cache"}
+    out["kv_fp8"] = np.ascontiguousarray(codes)
+    out["kv_scale"] = float(kv_scale)
+    out["name"] = f"{w['name']}_fp8"
+    return out
+
+
 def permute_blocks(w: Dict[str, object], seed: int) -> Dict[str, object]:
     """Same logical cache under a different physical block placement.
 
@@ -211,10 +239,11 @@ def permute_blocks(w: Dict[str, object], seed: int) -> Dict[str, object]:
     rng = np.random.Generator(np.random.PCG64(seed))
     nb = int(w["num_blocks"])
     pi = rng.permutation(nb).astype(np.int32)
-    kv = np.empty_like(w["kv_cache"])
-    kv[pi] = w["kv_cache"]
+    key = "kv_fp8" if "kv_fp8" in w else "kv_cache"
+    kv = np.empty_like(w[key])
+    kv[pi] = w[key]
     out = dict(w)
-    out["kv_cache"] = kv
+    out[key] = kv
     out["block_table"] = pi[w["block_table"]]
     out["spare_blocks"] = np.sort(pi[w["spare_blocks"]])
     return out
@@ -223,7 +252,7 @@ def permute_blocks(w: Dict[str, object], seed: int) -> Dict[str, object]:
 def expected_counts(w: Dict[str, object]) -> Dict[str, float]:
     """Algorithmic byte and flop counts of one decode call on this workload.
 
-    Bytes: KV rows read once (1152 B each), q_nope+q_pe, out (bf16), lse (fp32),
+    Bytes: KV rows read once (1152 B each, 576 B for an FP8 cache), q_nope+q_pe, out (bf16), lse (fp32),
     the block-table entries of used pages and the lengths. Flops: per token and
     real head, 2*576 for the score and 2*512 for the value product.
     """
@@ -231,7 +260,7 @@ def expected_counts(w: Dict[str, object]) -> Dict[str, float]:
     B, H, bs = int(w["B"]), int(w["H"]), int(w["block_size"])
     tokens = int(seq.sum())
     pages = int(((seq + bs - 1) // bs).sum())
-    kv_bytes = tokens * D * 2
+    kv_bytes = tokens * D * (1 if "kv_fp8" in w else 2)
     total = kv_bytes + B * H * D * 2 + B * H * D_C * 2 + 4 * B * H + 4 * pages + 4 * B
     flops = tokens * H * (2 * D + 2 * D_C)
     return {"tokens": tokens, "kv_bytes": float(kv_bytes), "bytes": float(total),

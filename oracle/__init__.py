@@ -66,8 +66,12 @@ def _load():
         lib.oracle_mla_partial.argtypes = common + [i32, i32, i64, i64, p, p]
         lib.oracle_mla_combine.argtypes = [i32, p, p, p, p]
         lib.oracle_mla_decode_bruteforce.argtypes = common + [p, p]
+        lib.oracle_mla_decode_fp8.argtypes = [i32, i32, i32, p, p, p, dbl, i64, i32, p, i32, p,
+                                              dbl, p, p, i32]
+        lib.oracle_e4m3_decode.argtypes = [i64, p, p]
         lib.oracle_num_threads.argtypes = [i32]
         for fn in (lib.oracle_mla_decode_rows, lib.oracle_mla_decode, lib.oracle_mla_decode_multi,
+                   lib.oracle_mla_decode_fp8, lib.oracle_e4m3_decode,
                    lib.oracle_mla_partial,
                    lib.oracle_mla_combine, lib.oracle_mla_decode_bruteforce,
                    lib.oracle_num_threads):
@@ -142,6 +146,44 @@ def mla_decode_multi(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale, n_
                                            _ptr(out), _ptr(lse), int(n_threads)),
            "oracle_mla_decode_multi")
     del keep
+    return out, lse
+
+
+def e4m3_decode(codes):
+    """OCP E4M3 bytes (any shape, uint8) -> float64 values of the same shape."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(codes.shape, dtype=np.float64)
+    _check(_load().oracle_e4m3_decode(codes.size, _ptr(codes), _ptr(out)), "oracle_e4m3_decode")
+    return out
+
+
+def mla_decode_fp8(q_nope, q_pe, kv_fp8, kv_scale, block_table, seq_lens, sm_scale,
+                   n_threads: int = 0):
+    """Decode over an FP8 latent cache: kv_fp8 uint8 [num_blocks, bs, 576] of
+    E4M3 bytes, element value kv_scale * e4m3(byte). q_nope [B, H, 512] (or
+    [B, q_len, H, 512] for multi-token queries, causal as in mla_decode_multi).
+    Returns (out, lse) shaped like the queries without the last axis / with 512."""
+    q_nope = np.ascontiguousarray(q_nope, dtype=np.uint16)
+    q_pe = np.ascontiguousarray(q_pe, dtype=np.uint16)
+    multi = q_nope.ndim == 4
+    if multi:
+        B, q_len, H, dc = q_nope.shape
+    else:
+        (B, H, dc), q_len = q_nope.shape, 1
+    assert dc == D_C and q_pe.shape == q_nope.shape[:-1] + (D_R,), (q_nope.shape, q_pe.shape)
+    kv_fp8 = np.ascontiguousarray(kv_fp8, dtype=np.uint8)
+    nb, bs, d = kv_fp8.shape
+    assert d == D, kv_fp8.shape
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    assert block_table.ndim == 2 and block_table.shape[0] == B and seq_lens.shape == (B,)
+    out = np.empty(q_nope.shape[:-1] + (D_C,), dtype=np.float64)
+    lse = np.empty(q_nope.shape[:-1], dtype=np.float64)
+    _check(_load().oracle_mla_decode_fp8(B, q_len, H, _ptr(q_nope), _ptr(q_pe), _ptr(kv_fp8),
+                                         float(kv_scale), nb, bs, _ptr(block_table),
+                                         block_table.shape[1], _ptr(seq_lens), float(sm_scale),
+                                         _ptr(out), _ptr(lse), int(n_threads)),
+           "oracle_mla_decode_fp8")
     return out, lse
 
 

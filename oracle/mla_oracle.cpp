@@ -23,6 +23,15 @@
 // 64 k_pe, V = c_kv) and the natural-log LSE are the readings written down in
 // the design notes; the pages print neither formulas nor tensor shapes.
 //
+// FP8 latent cache (oracle_mla_decode_fp8): each cached element is one byte
+// in the OCP 8-bit E4M3 format and stands for kv_scale * e4m3(byte); step 1
+// then reads that product, everything after it is unchanged. The pages name
+// only an "fp8" KV cache ("[Kernel][DSV4.1] Fuse MXFP8 wo_b GEMM with
+// sequence-parallel reduce-scatter" (vLLM PR #57428), serving command with
+// --kv-cache-dtype fp8; "Support DS conv-state layout in fused KDA decode
+// kernel" (vLLM PR #53396), E2E setup with an FP8 KV cache); the E4M3 format
+// and one per-tensor scale are the readings taken there.
+//
 // Edge conventions: L = 0 gives out = 0 and lse = -inf. A block id outside
 // [0, num_blocks) makes the call return ORACLE_ERR_BAD_BLOCK.
 //
@@ -59,36 +68,67 @@ inline double bf16_to_double(uint16_t bits) {
   return static_cast<double>(f);
 }
 
+// OCP 8-bit floating point, E4M3 variant: bit 7 sign, bits 6..3 exponent
+// with bias 7, bits 2..0 mantissa. Exponent field 0 holds the subnormals
+// (mantissa / 8) * 2^-6; S.1111.111 is NaN; there are no infinities, so
+// S.1111.110 = +-448 is the largest finite value.
+double e4m3_to_double(uint8_t byte) {
+  const int sign = byte >> 7;
+  const int e = (byte >> 3) & 0xF;
+  const int m = byte & 0x7;
+  if (e == 0xF && m == 0x7) return std::numeric_limits<double>::quiet_NaN();
+  const double mag = e == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
 struct Inputs {
   int B, H;
   const uint16_t* q_nope;     // [B, H, 512]
   const uint16_t* q_pe;       // [B, H, 64]
-  const uint16_t* kv_cache;   // [num_blocks, block_size, 576]
+  const uint16_t* kv_cache;   // [num_blocks, block_size, 576] bf16, or nullptr when kv_fp8 is set
   int64_t num_blocks;
   int block_size;
   const int32_t* block_table; // [B, max_blocks]
   int max_blocks;
   const int32_t* seq_lens;    // [B]
   double sm_scale;
+  const uint8_t* kv_fp8 = nullptr;   // [num_blocks, block_size, 576] E4M3 bytes
+  double kv_scale = 1.0;             // value = kv_scale * e4m3(byte)
 };
 
-// Step 1: address of cached row t of request b, or nullptr for a block id
-// that is out of range.
-const uint16_t* gather_row(const Inputs& in, int b, int64_t t) {
+// One gathered cache row; at(d) is the value of column d as a double.
+struct Row {
+  const uint16_t* b16 = nullptr;
+  const uint8_t* f8 = nullptr;
+  double scale = 1.0;
+  bool valid() const { return b16 != nullptr || f8 != nullptr; }
+  double at(int d) const { return f8 != nullptr ? scale * e4m3_to_double(f8[d]) : bf16_to_double(b16[d]); }
+};
+
+// Step 1: cached row t of request b (invalid for a block id out of range).
+Row gather_row(const Inputs& in, int b, int64_t t) {
   const int64_t page = t / in.block_size;
   const int64_t slot = t % in.block_size;
   const int32_t blk = in.block_table[static_cast<int64_t>(b) * in.max_blocks + page];
-  if (blk < 0 || blk >= in.num_blocks) return nullptr;
-  return in.kv_cache + (static_cast<int64_t>(blk) * in.block_size + slot) * kD;
+  Row r;
+  if (blk < 0 || blk >= in.num_blocks) return r;
+  const int64_t off = (static_cast<int64_t>(blk) * in.block_size + slot) * kD;
+  if (in.kv_fp8 != nullptr) {
+    r.f8 = in.kv_fp8 + off;
+    r.scale = in.kv_scale;
+  } else {
+    r.b16 = in.kv_cache + off;
+  }
+  return r;
 }
 
 // Step 2 for one token: the scaled score of head (b, h) against row.
-double score(const Inputs& in, int b, int h, const uint16_t* row) {
+double score(const Inputs& in, int b, int h, const Row& row) {
   const uint16_t* qn = in.q_nope + (static_cast<int64_t>(b) * in.H + h) * kDc;
   const uint16_t* qp = in.q_pe + (static_cast<int64_t>(b) * in.H + h) * kDr;
   double acc = 0.0;
-  for (int d = 0; d < kDc; ++d) acc += bf16_to_double(qn[d]) * bf16_to_double(row[d]);
-  for (int d = 0; d < kDr; ++d) acc += bf16_to_double(qp[d]) * bf16_to_double(row[kDc + d]);
+  for (int d = 0; d < kDc; ++d) acc += bf16_to_double(qn[d]) * row.at(d);
+  for (int d = 0; d < kDr; ++d) acc += bf16_to_double(qp[d]) * row.at(kDc + d);
   return in.sm_scale * acc;
 }
 
@@ -103,11 +143,11 @@ int attend_range(const Inputs& in, int b, int h, int64_t t0, int64_t t1,
     return ORACLE_OK;
   }
   std::vector<double> s(static_cast<size_t>(t1 - t0));
-  std::vector<const uint16_t*> rows(static_cast<size_t>(t1 - t0));
+  std::vector<Row> rows(static_cast<size_t>(t1 - t0));
   double m = -std::numeric_limits<double>::infinity();
   for (int64_t t = t0; t < t1; ++t) {
-    const uint16_t* row = gather_row(in, b, t);
-    if (row == nullptr) return ORACLE_ERR_BAD_BLOCK;
+    const Row row = gather_row(in, b, t);
+    if (!row.valid()) return ORACLE_ERR_BAD_BLOCK;
     rows[t - t0] = row;
     s[t - t0] = score(in, b, h, row);
     if (s[t - t0] > m) m = s[t - t0];
@@ -116,7 +156,7 @@ int attend_range(const Inputs& in, int b, int h, int64_t t0, int64_t t1,
   for (size_t i = 0; i < s.size(); ++i) {
     const double w = std::exp(s[i] - m);
     z += w;
-    for (int j = 0; j < kDc; ++j) out[j] += w * bf16_to_double(rows[i][j]);
+    for (int j = 0; j < kDc; ++j) out[j] += w * rows[i].at(j);
   }
   for (int j = 0; j < kDc; ++j) out[j] /= z;
   *lse = m + std::log(z);
@@ -143,6 +183,33 @@ int set_threads(int n_threads) {
   (void)n_threads;
   return 1;
 #endif
+}
+
+// Every query row of a decode whose requests carry q_len query tokens each:
+// in.H counts q_len * heads rows per request, row j * heads + h, and token j
+// attends to the first L - q_len + 1 + j cached tokens (all L for q_len = 1).
+int decode_causal(const Inputs& in, int q_len, double* out, double* lse, int n_threads) {
+  if (!valid_shape(in)) return ORACLE_ERR_ARG;
+  const int heads = in.H / q_len;
+  for (int b = 0; b < in.B; ++b)
+    if (in.seq_lens[b] != 0 && in.seq_lens[b] < q_len) return ORACLE_ERR_ARG;
+  set_threads(n_threads);
+  const int64_t n = static_cast<int64_t>(in.B) * in.H;
+  int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n; ++r) {
+    const int b = static_cast<int>(r / in.H);
+    const int row = static_cast<int>(r % in.H);   // j * heads + h
+    const int j = row / heads;
+    const int64_t L = in.seq_lens[b];
+    const int64_t Lj = L == 0 ? 0 : L - q_len + 1 + j;
+    const int rc = attend_range(in, b, row, 0, Lj, out + r * kDc, lse + r);
+    if (rc != ORACLE_OK) {
+#pragma omp critical
+      status = rc;
+    }
+  }
+  return status;
 }
 
 }  // namespace
@@ -215,26 +282,31 @@ int oracle_mla_decode_multi(int B, int q_len, int H, const uint16_t* q_nope,
   // The request's q_len x H query rows, row j * H + h, share its cache.
   Inputs in{B, q_len * H, q_nope, q_pe, kv_cache, num_blocks, block_size,
             block_table, max_blocks, seq_lens, sm_scale};
-  if (!valid_shape(in)) return ORACLE_ERR_ARG;
-  for (int b = 0; b < B; ++b)
-    if (seq_lens[b] != 0 && seq_lens[b] < q_len) return ORACLE_ERR_ARG;
-  set_threads(n_threads);
-  const int64_t n = static_cast<int64_t>(B) * q_len * H;
-  int status = ORACLE_OK;
-#pragma omp parallel for schedule(dynamic, 1)
-  for (int64_t r = 0; r < n; ++r) {
-    const int b = static_cast<int>(r / (static_cast<int64_t>(q_len) * H));
-    const int row = static_cast<int>(r % (static_cast<int64_t>(q_len) * H));   // j * H + h
-    const int j = row / H;
-    const int64_t L = seq_lens[b];
-    const int64_t Lj = L == 0 ? 0 : L - q_len + 1 + j;
-    const int rc = attend_range(in, b, row, 0, Lj, out + r * kDc, lse + r);
-    if (rc != ORACLE_OK) {
-#pragma omp critical
-      status = rc;
-    }
-  }
-  return status;
+  return decode_causal(in, q_len, out, lse, n_threads);
+}
+
+// The same decode over an FP8 latent cache: kv_fp8 holds E4M3 bytes
+// [num_blocks, block_size, 576] and element (blk, slot, d) stands for
+// kv_scale * e4m3(kv_fp8[blk, slot, d]). q_len = 1 is the ordinary decode
+// (q [B, H, ...], out [B, H, 512], lse [B, H]); q_len > 1 follows the
+// causal rule of oracle_mla_decode_multi.
+int oracle_mla_decode_fp8(int B, int q_len, int H, const uint16_t* q_nope, const uint16_t* q_pe,
+                          const uint8_t* kv_fp8, double kv_scale, int64_t num_blocks,
+                          int block_size, const int32_t* block_table, int max_blocks,
+                          const int32_t* seq_lens, double sm_scale, double* out, double* lse,
+                          int n_threads) {
+  if (B < 0 || H < 1 || q_len < 1 || kv_fp8 == nullptr || !std::isfinite(kv_scale))
+    return ORACLE_ERR_ARG;
+  Inputs in{B, q_len * H, q_nope, q_pe, nullptr, num_blocks, block_size,
+            block_table, max_blocks, seq_lens, sm_scale, kv_fp8, kv_scale};
+  return decode_causal(in, q_len, out, lse, n_threads);
+}
+
+// E4M3 bytes -> doubles, element by element (NaN for the two NaN codes).
+int oracle_e4m3_decode(int64_t n, const uint8_t* bytes, double* out) {
+  if (n < 0) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(bytes[i]);
+  return ORACLE_OK;
 }
 
 // Split-KV partial of one (b, h) over tokens [t0, t1): the normalised partial
