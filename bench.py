@@ -10,7 +10,10 @@ in HBM; the cache alone is ten times the 129 MB L2, so no flush is needed
 between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config NAME]
+                    [--config NAME] [--kv bf16|fp8]
+
+``--kv fp8`` runs the same workload over an FP8 (E4M3, per-tensor scale)
+cache through ``mla_decode_fp8`` (576 bytes per cached token).
 
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
 same workload on the host cores (the slow baseline). Under torchrun (N > 1)
@@ -42,7 +45,9 @@ UNIT = "us/call"
 DEFAULT_CONFIG = "r1_b512_h128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_SRC = os.path.join(ROOT, "paged_mla_decode_05_gb300", "csrc", "mla_decode_sm103.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_r1_b512_h128_traffic.txt")
+TRAFFIC_FILES = {"bf16": os.path.join(ROOT, "profiles", "decode_r1_b512_h128_traffic.txt"),
+                 "fp8": os.path.join(ROOT, "profiles", "decode_r1_b512_h128_fp8_traffic.txt")}
+FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor throughput (4.5 / 2.25 PFLOP/s)
 L2_BYTES = 129 * 1024 * 1024      # GB300 L2
 FLUSH_BYTES = 512 * 1024 * 1024   # written between steps when the cache is near the L2 size
 
@@ -100,13 +105,14 @@ def source_digest() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    if not os.path.exists(TRAFFIC_FILE):
+def recorded_traffic(config: str, kv: str):
+    """DRAM bytes per decode launch of the default workload from the committed
+    ncu summary, if it was taken on the current kernel source (else None)."""
+    path = TRAFFIC_FILES[kv]
+    if config != DEFAULT_CONFIG or not os.path.exists(path):
         return None
     vals = {}
-    with open(TRAFFIC_FILE) as f:
+    with open(path) as f:
         for line in f:
             if ":" in line:
                 k, v = line.split(":", 1)
@@ -175,10 +181,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def load_workload(name: str, kv: str):
+    """The seeded workload, with its cache converted to E4M3 for kv == "fp8"."""
+    w = wl.generate(wl.WORKLOADS_BY_NAME[name])
+    return wl.to_fp8(w) if kv == "fp8" else w
+
+
+def cache_of(w):
+    return w["kv_fp8"] if "kv_fp8" in w else w["kv_cache"]
+
+
 def workload_config(spec, w, counts, world):
     """The config block both arms report for a workload (identical keys)."""
-    cache_bytes = int(w["kv_cache"].nbytes)
-    return {"workload": spec.name, "B": int(w["B"]), "H": int(w["H"]),
+    cache_bytes = int(cache_of(w).nbytes)
+    fp8 = "kv_fp8" in w
+    return {"workload": spec.name + ("_fp8" if fp8 else ""), "B": int(w["B"]), "H": int(w["H"]),
+            "kv_cache": (f"fp8 e4m3, per-tensor scale {w['kv_scale']}" if fp8 else "bf16"),
             "block_size": int(w["block_size"]),
             "seq_lens": "1024+U{0..2048}" if spec.name.startswith("r1_") else spec.description,
             "tokens": counts["tokens"], "num_blocks": int(w["num_blocks"]),
@@ -202,15 +220,17 @@ def bench_ours(args, world, rank, local):
 
     spec = wl.WORKLOADS_BY_NAME[args.config]
     t0 = time.time()
-    w = wl.generate(spec)
-    log(f"[bench] generated {spec.name} in {time.time() - t0:.1f}s")
+    w = load_workload(args.config, args.kv)
+    fp8 = args.kv == "fp8"
+    log(f"[bench] generated {spec.name} ({args.kv} cache) in {time.time() - t0:.1f}s")
     counts = wl.expected_counts(w)
     B, H, bs = w["B"], w["H"], w["block_size"]
 
     def bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
-    q_nope, q_pe, kv = bf16(w["q_nope"]), bf16(w["q_pe"]), bf16(w["kv_cache"])
+    q_nope, q_pe = bf16(w["q_nope"]), bf16(w["q_pe"])
+    kv = torch.from_numpy(w["kv_fp8"]).to(dev) if fp8 else bf16(w["kv_cache"])
     table = torch.from_numpy(w["block_table"]).to(dev)
     lens = torch.from_numpy(w["seq_lens"]).to(dev)
     plan = m.mla_decode_plan(B, H, w["seq_lens"], bs, int(w["max_blocks"]))
@@ -221,7 +241,11 @@ def bench_ours(args, world, rank, local):
     stream = torch.cuda.current_stream()
 
     def step():
-        m.mla_decode(plan, q_nope, q_pe, kv, table, lens, w["sm_scale"], out, lse, ws, stream)
+        if fp8:
+            m.mla_decode_fp8(plan, q_nope, q_pe, kv, w["kv_scale"], table, lens, w["sm_scale"], out,
+                             lse, ws, stream)
+        else:
+            m.mla_decode(plan, q_nope, q_pe, kv, table, lens, w["sm_scale"], out, lse, ws, stream)
 
     for _ in range(args.warmup):
         step()
@@ -231,7 +255,7 @@ def bench_ours(args, world, rank, local):
     # A cache several times the L2 size leaves no reuse between steps; a
     # smaller one gets L2 flushed (a write larger than L2) before every step,
     # outside the timed events of that step.
-    cache_bytes = int(w["kv_cache"].nbytes)
+    cache_bytes = int(cache_of(w).nbytes)
     flush = None
     if cache_bytes < 4 * L2_BYTES:
         flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -331,12 +355,18 @@ def bench_ours(args, world, rank, local):
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     t_bytes_us = counts["bytes"] / (hbm * 1e9) * 1e6
-    t_flops_us = counts["flops"] / (tf * 1e12) * 1e6
+    # FLOPs at the dense bf16 peak (the roofline_fraction below); the bound
+    # itself takes the contraction's own dtype: e4m3 for an FP8 cache.
+    t_flops_bf16_us = counts["flops"] / (tf * 1e12) * 1e6
+    tf_own = tf * (FP8_OVER_BF16 if fp8 else 1.0)
+    t_flops_us = counts["flops"] / (tf_own * 1e12) * 1e6
     # Dominant kernel: the decode kernel. Without a split the step is exactly
     # that one launch, so the step time is its duration.
     dominant_us = us if launches_per_step == 1 else None
-    achieved = counts["bytes"] / (ms_per_step * 1e-3) / 1e9
-    traffic = recorded_traffic()
+    hbm_bound = t_bytes_us >= t_flops_us
+    achieved = (counts["bytes"] / (ms_per_step * 1e-3) / 1e9 if hbm_bound
+                else counts["flops"] / (ms_per_step * 1e-3) / 1e12)
+    traffic = recorded_traffic(args.config, args.kv)
     result = {
         "metric": METRIC,
         "value": round(us, 2),
@@ -348,9 +378,12 @@ def bench_ours(args, world, rank, local):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 latent cache and queries, sentinel-filled spare "
-                "blocks and tail slots)",
+        "dtype": "e4m3" if fp8 else "bf16",
+        "data": ("synthetic (seeded N(0,1) latent cache quantised to E4M3 with scale "
+                 f"{w['kv_scale']}, bf16 queries, sentinel-filled spare blocks and tail slots)"
+                 if fp8 else
+                 "synthetic (seeded N(0,1) bf16 latent cache and queries, sentinel-filled spare "
+                 "blocks and tail slots)"),
         "config": workload_config(spec, w, counts, world),
         "plan": {"cta_pairs": plan.num_clusters, "work_items": plan.num_work_items,
                  "split_requests": int(sum(plan.num_splits(b) > 1 for b in range(B)))},
@@ -358,17 +391,20 @@ def bench_ours(args, world, rank, local):
         "alg_bytes_per_call": counts["bytes"],
         "alg_flops_per_call": counts["flops"],
         "roofline": {
-            "bound": "hbm" if t_bytes_us >= t_flops_us else "tensor",
+            "bound": "hbm" if hbm_bound else "tensor",
             "achieved": round(achieved, 1),
-            "peak": hbm,
-            "unit": "GB/s",
-            "frac": round(achieved / hbm, 4),
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                           else "fallback 6.8 TB/s",
+            "peak": hbm if hbm_bound else tf_own,
+            "unit": "GB/s" if hbm_bound else "TFLOP/s",
+            "frac": round(achieved / (hbm if hbm_bound else tf_own), 4),
+            "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if hbm_bound else
+                            f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops"
+                            + (" x 2, the nominal fp8/bf16 ratio)" if fp8 else ")"))
+                           if peak_kind == "measured" else "fallback 6.8 TB/s, 1.9 PFLOP/s",
             "traffic": traffic,
             "t_bytes_us": round(t_bytes_us, 2),
             "t_flops_us": round(t_flops_us, 2),
-            "roofline_fraction": round(max(t_bytes_us, t_flops_us) / us, 4),
+            "t_flops_bf16_us": round(t_flops_bf16_us, 2),
+            "roofline_fraction": round(max(t_bytes_us, t_flops_bf16_us) / us, 4),
             "dominant_kernel": "mla_decode_kernel",
             "dominant_kernel_us": round(dominant_us, 2) if dominant_us else None,
         },
@@ -388,57 +424,70 @@ def bench_ours(args, world, rank, local):
 
 # ------------------------------------------------------------- CPU oracle leg
 
+def oracle_call(oracle, w, reqs=None):
+    """The oracle on requests `reqs` (all when None) of workload w."""
+    sel = slice(None) if reqs is None else np.asarray(reqs)
+    qn, qp = w["q_nope"][sel], w["q_pe"][sel]
+    bt, sl = w["block_table"][sel], w["seq_lens"][sel]
+    if "kv_fp8" in w:
+        return oracle.mla_decode_fp8(qn, qp, w["kv_fp8"], w["kv_scale"], bt, sl, w["sm_scale"])
+    return oracle.mla_decode(qn, qp, w["kv_cache"], bt, sl, w["sm_scale"])
+
+
+def sample_requests(rng, seq, n):
+    """n random requests with at least one token (all of them if fewer)."""
+    nz = np.nonzero(seq > 0)[0]
+    return np.sort(rng.permutation(nz)[:max(1, min(n, nz.size))])
+
+
 def cpu_baseline(w, budget_s: float):
-    """The fp64 oracle as it stands, on a bounded sample of (request, head)
-    rows of the same workload, scaled to one full call."""
+    """The fp64 oracle as it stands, on a bounded random sample of the
+    workload's requests (all their heads), scaled to one full call by the
+    sample's share of the tokens."""
     import oracle
     oracle.build()
     B, H = int(w["B"]), int(w["H"])
     cores = oracle.num_threads(0)
-    rng = np.random.default_rng(123)
-    order = rng.permutation(B * H)
-    args = (w["q_nope"], w["q_pe"], w["kv_cache"], w["block_table"], w["seq_lens"], w["sm_scale"])
-    n = min(B * H, max(cores * 4, 64))
-    t0 = time.perf_counter()
-    rows = order[:n]
-    oracle.mla_decode_rows(*args, rows // H, rows % H)
-    pilot = time.perf_counter() - t0
-    n2 = int(min(B * H, max(n, n * budget_s / max(pilot, 1e-6))))
-    rows = order[:n2]
-    t0 = time.perf_counter()
-    oracle.mla_decode_rows(*args, rows // H, rows % H)
-    dt = time.perf_counter() - t0
     seq = np.asarray(w["seq_lens"], dtype=np.int64)
-    frac_tokens = seq[rows // H].sum() / (seq.sum() * H)
-    per_call_s = dt / frac_tokens
+    rng = np.random.default_rng(123)
+    reqs = sample_requests(rng, seq, max(1, cores // max(1, H // 16)))
+    t0 = time.perf_counter()
+    oracle_call(oracle, w, reqs)
+    pilot = time.perf_counter() - t0
+    n2 = int(min(B, max(reqs.size, reqs.size * budget_s / max(pilot, 1e-6))))
+    reqs = sample_requests(rng, seq, n2)
+    t0 = time.perf_counter()
+    oracle_call(oracle, w, reqs)
+    dt = time.perf_counter() - t0
+    share = seq[reqs].sum() / seq.sum()
+    per_call_s = dt / share
     return {"value": round(per_call_s * 1e6, 1), "unit": UNIT, "cores": int(cores), "kind": "oracle",
-            "sample": f"{n2} of {B * H} (request, head) rows, {dt:.1f} s, scaled by token share "
-                      f"{frac_tokens:.4f}"}
+            "sample": f"{reqs.size} of {B} requests (all {H} heads each), {dt:.1f} s, scaled by "
+                      f"token share {share:.4f}"}
 
 
 def bench_reference(args, world, rank, local):
-    """--impl reference: the oracle on the host cores, each step a bounded sample."""
+    """--impl reference: the oracle on the host cores, each step the whole
+    workload when the run fits the time budget, else a bounded sample."""
     if world > 1:
         init_dist(world, "gloo")
         if rank != 0:
             return None
     spec = wl.WORKLOADS_BY_NAME[args.config]
-    w = wl.generate(spec)
+    w = load_workload(args.config, args.kv)
     import oracle
     oracle.build()
     B, H = int(w["B"]), int(w["H"])
     cores = oracle.num_threads(0)
     seq = np.asarray(w["seq_lens"], dtype=np.int64)
-    args_o = (w["q_nope"], w["q_pe"], w["kv_cache"], w["block_table"], w["seq_lens"], w["sm_scale"])
     rng = np.random.default_rng(7)
     total_steps = args.warmup + args.steps
-    # Pilot: time a small random sample of rows to size the steps.
-    pilot_rows = rng.permutation(B * H)[:max(cores * 2, 32)]
+    # Pilot: a few requests, to size the steps.
+    pilot = sample_requests(rng, seq, max(1, cores // max(1, H // 16)))
     t0 = time.perf_counter()
-    oracle.mla_decode_rows(*args_o, pilot_rows // H, pilot_rows % H)
+    oracle_call(oracle, w, pilot)
     pilot_s = time.perf_counter() - t0
-    pilot_share = seq[pilot_rows // H].sum() / (seq.sum() * H)
-    full_est_s = pilot_s / max(pilot_share, 1e-12)
+    full_est_s = pilot_s / max(seq[pilot].sum() / max(seq.sum(), 1), 1e-12)
     budget_s = 240.0
     full = total_steps * full_est_s <= budget_s
     times = []
@@ -446,26 +495,24 @@ def bench_reference(args, world, rank, local):
         # Every step is one whole call of the oracle on the workload.
         for s in range(total_steps):
             t0 = time.perf_counter()
-            oracle.mla_decode(*args_o)
+            oracle_call(oracle, w)
             dt = time.perf_counter() - t0
             if s >= args.warmup:
                 times.append(dt)
-        sample = f"the full workload every step ({B * H} (request, head) rows)"
+        sample = f"the full workload every step ({B} requests x {H} heads)"
     else:
-        # Each step: a fixed-size random sample of rows sized so the run stays
-        # within the budget, scaled by its token share to one call.
-        n_rows = int(max(16, min(B * H, (budget_s / max(total_steps, 1)) / max(full_est_s, 1e-9)
-                                 * B * H)))
+        # Each step: a random sample of requests sized so the run stays within
+        # the budget, scaled by its token share to one call.
+        n_req = int(max(1, min(B, (budget_s / max(total_steps, 1)) / max(full_est_s, 1e-9) * B)))
         for s in range(total_steps):
-            rows = rng.permutation(B * H)[:n_rows]
+            reqs = sample_requests(rng, seq, n_req)
             t0 = time.perf_counter()
-            oracle.mla_decode_rows(*args_o, rows // H, rows % H)
+            oracle_call(oracle, w, reqs)
             dt = time.perf_counter() - t0
             if s >= args.warmup:
-                share = seq[rows // H].sum() / (seq.sum() * H)
-                times.append(dt / share)
-        sample = (f"{n_rows} random (request, head) rows per step, scaled by token share to one "
-                  "full call (the full call would not fit the run's time budget)")
+                times.append(dt / (seq[reqs].sum() / seq.sum()))
+        sample = (f"{n_req} random requests (all {H} heads) per step, scaled by token share to "
+                  "one full call (the full call would not fit the run's time budget)")
     us = statistics.mean(times) * 1e6
     return {
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
@@ -488,6 +535,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.WORKLOADS_BY_NAME))
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="cache element type (fp8: E4M3 with a per-tensor scale)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)

@@ -172,6 +172,34 @@ mla_status_t mla_decode(mla_plan_t plan, const void* q_nope, const void* q_pe,
                         const int32_t* seq_lens, float sm_scale, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * mla_decode_fp8 — mla_decode over an FP8 latent cache, the "fp8 KV cache"
+ * the pages' deployments serve with ("[Kernel][DSV4.1] Fuse MXFP8 wo_b GEMM
+ * with sequence-parallel reduce-scatter" (vLLM PR #57428), serving command
+ * with --kv-cache-dtype fp8; "Support DS conv-state layout in fused KDA
+ * decode kernel" (vLLM PR #53396), E2E setup). The pages name the cache type
+ * only; the element format and the scale below are the readings taken.
+ *
+ *  kv_cache_fp8 device uint8 [num_blocks, block_size, 576], 16-byte aligned:
+ *               OCP E4M3 bytes (sign, 4 exponent bits with bias 7, 3
+ *               mantissa bits; no infinities, S.1111.111 is NaN), same row
+ *               layout as the bf16 cache (512 c_kv then 64 k_pe columns)
+ *  kv_scale     per-tensor scale, finite and > 0: element (blk, slot, d)
+ *               stands for kv_scale * e4m3(kv_cache_fp8[blk][slot][d])
+ *
+ * Every other argument, the plan (any plan mla_decode accepts), the outputs
+ * and the errors are those of mla_decode; MLA_ERR_INVALID_ARG also for a bad
+ * kv_scale. Computation: K and V are multiplied in 8-bit on the tensor core;
+ * q (bf16) and the softmax weights enter those products as two E4M3 terms
+ * each, about the 8 significant bits of bf16, and the cache scale is applied
+ * in fp32. Reads 576 bytes per cached token instead of 1152.
+ */
+mla_status_t mla_decode_fp8(mla_plan_t plan, const void* q_nope, const void* q_pe,
+                            const void* kv_cache_fp8, float kv_scale, int64_t num_blocks,
+                            const int32_t* block_table, const int32_t* seq_lens, float sm_scale,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* Bytes of device memory behind mla_decode_no_alloc (32 MiB). */
 #define MLA_NO_ALLOC_SCRATCH_BYTES (((size_t)32) << 20)
 
@@ -185,8 +213,8 @@ mla_status_t mla_decode(mla_plan_t plan, const void* q_nope, const void* q_pe,
  * pageable host memory, and such a copy may hold the calling thread until
  * the driver has staged it; it does not wait for the device.)
  *
- * Same computation, kernels and argument rules as mla_decode, with three
- * differences:
+ * Same computation, kernels and argument rules as mla_decode (bf16 cache),
+ * with three differences:
  *  - No workspace argument. The split partials and a copy of the plan's work
  *    list live in one fixed array of MLA_NO_ALLOC_SCRATCH_BYTES inside the
  *    library's device image. Every GPU that loads the library holds it until

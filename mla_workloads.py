@@ -220,11 +220,15 @@ def to_fp8(w: Dict[str, object], kv_scale: float = FP8_KV_SCALE) -> Dict[str, ob
     (round to nearest even) after clipping to +-448.
     """
     import torch
-    x = bf16_bits_to_f32(w["kv_cache"]) / np.float32(kv_scale)
-    np.clip(x, -E4M3_MAX, E4M3_MAX, out=x)
-    codes = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    src = w["kv_cache"].reshape(-1)
+    codes = np.empty(src.shape, dtype=np.uint8)
+    step = 1 << 24
+    for s in range(0, src.size, step):   # in chunks: the full cache is ~650M elements
+        x = bf16_bits_to_f32(src[s:s + step]) / np.float32(kv_scale)
+        np.clip(x, -E4M3_MAX, E4M3_MAX, out=x)
+        codes[s:s + step] = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     out = {k: v for k, v in w.items() if k != "kv_cache"}
-    out["kv_fp8"] = np.ascontiguousarray(codes)
+    out["kv_fp8"] = codes.reshape(w["kv_cache"].shape)
     out["kv_scale"] = float(kv_scale)
     out["name"] = f"{w['name']}_fp8"
     return out

@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
         "mla_plan_work_item": (i32, [p, i32, p, p, p, p, p]),
         "mla_plan_work_item_heads": (i32, [p, i32, p, p]),
         "mla_decode": (i32, [p, p, p, p, i64, p, p, ctypes.c_float, p, p, p, sz, p]),
+        "mla_decode_fp8": (i32, [p, p, p, p, ctypes.c_float, i64, p, p, ctypes.c_float, p, p, p,
+                                 sz, p]),
         "mla_decode_no_alloc": (i32, [p, p, p, p, i64, p, p, ctypes.c_float, p, p, p, p]),
         "mla_check_device_error": (i32, [p, p, ctypes.POINTER(u32)]),
         "mla_plan_destroy": (None, [p]),
@@ -252,6 +254,45 @@ def mla_decode(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, sm_sca
     _check(LIB.mla_decode(plan.handle, args[0], args[1], args[2], nb, bt, sl,
                           ctypes.c_float(sm_scale), o, l, ws, ws_bytes, _stream_ptr(stream)),
            "mla_decode")
+
+
+def mla_decode_fp8(plan: Plan, q_nope, q_pe, kv_cache_fp8, kv_scale: float, block_table,
+                   seq_lens, sm_scale: float, out, lse, workspace=None, stream=None):
+    """Enqueue one decode over an FP8 (E4M3) latent cache (see mla_decode_fp8
+    in include/mla_decode.h).
+
+    kv_cache_fp8 is a CUDA uint8 tensor [num_blocks, block_size, 576] of E4M3
+    bytes (a float8_e4m3fn tensor viewed as uint8 is accepted too); element
+    values are kv_scale * e4m3(byte). Everything else as ``mla_decode``.
+    """
+    import torch
+    B, H = plan.B, plan.H
+    if getattr(torch, "float8_e4m3fn", None) is not None and kv_cache_fp8.dtype == torch.float8_e4m3fn:
+        kv_cache_fp8 = kv_cache_fp8.view(torch.uint8)
+    if (kv_cache_fp8.dim() != 3 or kv_cache_fp8.shape[1] != plan.block_size
+            or kv_cache_fp8.shape[2] != D):
+        raise ValueError(f"kv_cache_fp8 must have shape [num_blocks, {plan.block_size}, {D}]")
+    nb = int(kv_cache_fp8.shape[0])
+    args = [
+        _tensor(q_nope, torch.bfloat16, plan.q_shape(D_C), "q_nope"),
+        _tensor(q_pe, torch.bfloat16, plan.q_shape(D_R), "q_pe"),
+        _tensor(kv_cache_fp8, torch.uint8, (nb, plan.block_size, D), "kv_cache_fp8"),
+    ]
+    bt = _tensor(block_table, torch.int32, (B, plan.max_blocks), "block_table")
+    sl = _tensor(seq_lens, torch.int32, (B,), "seq_lens")
+    o = _tensor(out, torch.bfloat16, plan.q_shape(D_C), "out")
+    l = _tensor(lse, torch.float32, plan.q_shape(None), "lse")
+    if workspace is None:
+        ws, ws_bytes = ctypes.c_void_p(0), 0
+    else:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws = ctypes.c_void_p(workspace.data_ptr())
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(LIB.mla_decode_fp8(plan.handle, args[0], args[1], args[2], ctypes.c_float(kv_scale), nb,
+                              bt, sl, ctypes.c_float(sm_scale), o, l, ws, ws_bytes,
+                              _stream_ptr(stream)),
+           "mla_decode_fp8")
 
 
 def mla_decode_no_alloc(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens,

@@ -56,6 +56,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         obj = os.path.join(BUILD, src + ".o")
         objs.append(obj)
         extra = ["-Xptxas", "-v"] if verbose and src.endswith(".cu") else []
+        if src.endswith(".cu"):
+            # No register may spill: the roles read tensor memory with
+            # asynchronous loads whose destination registers must stay put
+            # until the wait, which a spill between the two would break.
+            extra += ["-Xptxas", "--warn-on-spills", "-Xptxas", "--warning-as-error"]
         cmds.append(common + extra + ["-c", os.path.join(CSRC, src), "-o", obj])
 
     def run(cmd):

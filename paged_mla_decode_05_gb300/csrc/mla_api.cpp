@@ -65,6 +65,7 @@ struct mla_plan_s {
   CUtensorMap tmap_v32;
   const void* tmap_ptr = nullptr;
   int64_t tmap_blocks = -1;
+  int tmap_fp8 = -1;
 };
 
 namespace {
@@ -504,41 +505,75 @@ void free_plan(mla_plan_s* p) {
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 // Tensor maps of the cache at kv_cache, kept in the plan until the cache
-// pointer or pool size changes. The cache is viewed as a 4-D tensor
-// {64 columns, 8 rows, 9 panels, row groups of 8} with strides of 1152 B
-// (row), 128 B (panel) and 9216 B (row group), so one box brings a run of
-// 16 or 32 rows across several panels and lands as [row group][panel]
-// [8 rows][128 B] (128-byte swizzle, zero fill outside the pool). Boxes:
-// 2 or min(block_size, 32)/8 row groups; 9 panels (K: all 576 columns) or 4
-// panels (one half of V).
-mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_blocks) {
-  if (p->tmap_ptr == kv_cache && p->tmap_blocks == num_blocks) return MLA_OK;
+// pointer, pool size or element type changes.
+// bf16: the cache is viewed as a 4-D tensor {64 columns, 8 rows, 9 panels,
+// row groups of 8} with strides of 1152 B (row), 128 B (panel) and 9216 B
+// (row group), so one box brings a run of 16 or 32 rows across several
+// panels and lands as [row group][panel][8 rows][128 B] (128-byte swizzle,
+// zero fill outside the pool). Boxes: 2 or min(block_size, 32)/8 row groups;
+// 9 panels (K: all 576 columns) or 4 panels (one half of V).
+// FP8: columns 0..511 as {128 columns, 8 rows, 4 panels, row groups}
+// (strides 576, 128, 4608 B; 128-byte swizzle), the K and V boxes; columns
+// 512..575 as {64 columns, 8 rows, row groups} (strides 576, 4608 B; 64-byte
+// swizzle), the rope boxes. Splitting the row keeps every box inside it: a
+// 128-column view of the rope columns would read 64 bytes past each row,
+// and past the pool's end on its last row.
+mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_blocks, bool fp8) {
+  if (p->tmap_ptr == kv_cache && p->tmap_blocks == num_blocks && p->tmap_fp8 == (fp8 ? 1 : 0))
+    return MLA_OK;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return MLA_ERR_CUDA;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(mla::kPanelCols), 8,
-                              static_cast<cuuint64_t>(mla::kNumPanels),
-                              static_cast<cuuint64_t>(num_blocks) * p->block_size / 8};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(mla::kD) * 2,
-                                 static_cast<cuuint64_t>(mla::kPanelCols) * 2,
-                                 static_cast<cuuint64_t>(mla::kD) * 2 * 8};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUtensorMap* maps[4] = {&p->tmap_k16, &p->tmap_k32, &p->tmap_v16, &p->tmap_v32};
+  p->tmap_ptr = nullptr;
+  const cuuint64_t groups = static_cast<cuuint64_t>(num_blocks) * p->block_size / 8;
   const int large = std::min(p->block_size, mla::kRowsLargeBox);
-  const int groups[4] = {mla::kRowsSmallBox / 8, large / 8, mla::kRowsSmallBox / 8, large / 8};
-  const int panels[4] = {mla::kNumPanels, mla::kNumPanels, mla::kVHalfPanels, mla::kVHalfPanels};
-  for (int i = 0; i < 4; ++i) {
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(mla::kPanelCols), 8,
-                               static_cast<cuuint32_t>(panels[i]),
-                               static_cast<cuuint32_t>(groups[i])};
-    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), dims,
-            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-      p->tmap_ptr = nullptr;
-      return MLA_ERR_INVALID_ARG;
+  const cuuint32_t g_small = mla::kRowsSmallBox / 8, g_large = static_cast<cuuint32_t>(large / 8);
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (!fp8) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(mla::kPanelCols), 8,
+                                static_cast<cuuint64_t>(mla::kNumPanels), groups};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(mla::kD) * 2,
+                                   static_cast<cuuint64_t>(mla::kPanelCols) * 2,
+                                   static_cast<cuuint64_t>(mla::kD) * 2 * 8};
+    CUtensorMap* maps[4] = {&p->tmap_k16, &p->tmap_k32, &p->tmap_v16, &p->tmap_v32};
+    const cuuint32_t box_groups[4] = {g_small, g_large, g_small, g_large};
+    const int panels[4] = {mla::kNumPanels, mla::kNumPanels, mla::kVHalfPanels, mla::kVHalfPanels};
+    for (int i = 0; i < 4; ++i) {
+      const cuuint32_t box[4] = {static_cast<cuuint32_t>(mla::kPanelCols), 8,
+                                 static_cast<cuuint32_t>(panels[i]), box_groups[i]};
+      if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), dims,
+              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MLA_ERR_INVALID_ARG;
+    }
+  } else {
+    const cuuint64_t dims[4] = {128, 8, static_cast<cuuint64_t>(mla::kF8Panels), groups};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(mla::kD), 128,
+                                   static_cast<cuuint64_t>(mla::kD) * 8};
+    CUtensorMap* maps[2] = {&p->tmap_k16, &p->tmap_k32};
+    const cuuint32_t box_groups[2] = {g_small, g_large};
+    for (int i = 0; i < 2; ++i) {
+      const cuuint32_t box[4] = {128, 8, static_cast<cuuint32_t>(mla::kF8Panels), box_groups[i]};
+      if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(kv_cache), dims,
+              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MLA_ERR_INVALID_ARG;
+    }
+    const cuuint64_t rdims[3] = {static_cast<cuuint64_t>(mla::kDr), 8, groups};
+    const cuuint64_t rstrides[2] = {static_cast<cuuint64_t>(mla::kD),
+                                    static_cast<cuuint64_t>(mla::kD) * 8};
+    CUtensorMap* rmaps[2] = {&p->tmap_v16, &p->tmap_v32};
+    void* rope = const_cast<uint8_t*>(static_cast<const uint8_t*>(kv_cache) + mla::kDc);
+    for (int i = 0; i < 2; ++i) {
+      const cuuint32_t box[3] = {static_cast<cuuint32_t>(mla::kDr), 8, box_groups[i]};
+      if (enc(rmaps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, rope, rdims, rstrides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MLA_ERR_INVALID_ARG;
     }
   }
   p->tmap_ptr = kv_cache;
   p->tmap_blocks = num_blocks;
+  p->tmap_fp8 = fp8 ? 1 : 0;
   return MLA_OK;
 }
 
@@ -648,11 +683,18 @@ int mla_plan_work_item(mla_plan_t p, int i, int32_t* b, int32_t* t0, int32_t* t1
   return 0;
 }
 
-mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, const void* kv_cache,
-                        int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
-                        float sm_scale, void* out, float* lse, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// mla_decode and mla_decode_fp8: the same launches on a bf16 (fp8 = false)
+// or an E4M3 cache with per-tensor scale kv_scale.
+mla_status_t decode_impl(mla_plan_t p, const void* q_nope, const void* q_pe, const void* kv_cache,
+                         bool fp8, float kv_scale, int64_t num_blocks, const int32_t* block_table,
+                         const int32_t* seq_lens, float sm_scale, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream) {
   if (!p || p->host_only) return MLA_ERR_INVALID_ARG;
+  if (fp8 && (!(kv_scale > 0.0f) || !std::isfinite(kv_scale))) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !lse)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
@@ -671,7 +713,7 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   mla_status_t st = prepare_device(dev, nullptr);
   if (st != MLA_OK) return st;
 
-  st = refresh_kv_maps(p, kv_cache, num_blocks);
+  st = refresh_kv_maps(p, kv_cache, num_blocks, fp8);
   if (st != MLA_OK) return st;
 
   mla::DecodeParams dp;
@@ -703,6 +745,8 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
   dp.num_blocks = num_blocks;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
   dp.dynamic_lens = p->lengths_are_bounds ? 1 : 0;
+  dp.kv_fp8 = fp8 ? 1 : 0;
+  dp.kv_scale = fp8 ? kv_scale : 1.0f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (mla::launch_decode(dp, p->num_launch, s) != cudaSuccess) return MLA_ERR_CUDA;
@@ -719,6 +763,27 @@ mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, cons
       return MLA_ERR_CUDA;
   }
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode(mla_plan_t p, const void* q_nope, const void* q_pe, const void* kv_cache,
+                        int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                        float sm_scale, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  return decode_impl(p, q_nope, q_pe, kv_cache, false, 1.0f, num_blocks, block_table, seq_lens,
+                     sm_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+mla_status_t mla_decode_fp8(mla_plan_t p, const void* q_nope, const void* q_pe,
+                            const void* kv_cache_fp8, float kv_scale, int64_t num_blocks,
+                            const int32_t* block_table, const int32_t* seq_lens, float sm_scale,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  return decode_impl(p, q_nope, q_pe, kv_cache_fp8, true, kv_scale, num_blocks, block_table,
+                     seq_lens, sm_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 // The allocation-free variant: the workspace and the device copy of the work
@@ -762,7 +827,7 @@ mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q
   if (st != MLA_OK) return st;
   uint8_t* scratch = nullptr;
   if (mla::no_alloc_scratch(dev, &scratch) != cudaSuccess) return MLA_ERR_CUDA;
-  st = refresh_kv_maps(p, kv_cache, num_blocks);
+  st = refresh_kv_maps(p, kv_cache, num_blocks, false);
   if (st != MLA_OK) return st;
 
   // The caller's error word is the only state that must start at zero: the

@@ -13,23 +13,29 @@
 // Design (GB300-first; the pages' kernels are prior art, not the blueprint):
 // one 2-CTA cluster per work list, with split roles, because the fp32 output
 // accumulator of 128 heads x 512 columns fills a whole SM's tensor memory:
-//  * score CTA (cluster rank 0): streams 80-token KV tiles (all 576 columns)
-//    into two 90 KB shared-memory stages, one 4-D TMA box per page piece (a
-//    page-aligned run of 32 or 16 rows across all 9 panels; per-SM TMA cost
-//    is per box, so few large boxes keep up with HBM). The 4-D view lands
-//    every 8-row swizzle atom of the tile at a fixed offset whichever page it
-//    came from, so one MMA can span the whole tile. Q [128 heads x 576] stays
-//    in tensor memory; S = Q.K^T runs on tcgen05 (M = 128 heads, A from
-//    tensor memory) from two issuer threads, each taking part of the tile's
-//    rows. The fp32 online softmax (one thread per head row, one pass per
-//    tile with a lazy rescale) stages P (bf16) and the per-row rescale record
-//    in shared memory and ships each tile to the output CTA with one bulk
-//    copy into its shared memory.
+//  * score CTA (cluster rank 0): streams 96-token KV tiles (all 576 columns)
+//    into shared-memory stages, one TMA box per page piece (a page-aligned
+//    run of 32 or 16 rows; per-SM TMA cost is per box, so few large boxes
+//    keep up with HBM). The 4-D view lands every 8-row swizzle atom of the
+//    tile at a fixed offset whichever page it came from, so one MMA spans the
+//    whole tile. Q [128 heads x 576] stays in tensor memory (four loader
+//    warps replace it between items); S = Q.K^T runs on tcgen05 (M = 128
+//    heads, N = 96, A from tensor memory) from one issuer thread. The fp32
+//    online softmax (one thread per head row, one pass per tile with a lazy
+//    rescale) writes P and the per-row rescale record straight into the
+//    output CTA's shared memory with asynchronous remote stores.
 //  * output CTA (rank 1): holds O [128 x 512] fp32 in tensor memory, streams
-//    V half-tiles (256 columns) into a 4-slot ring with 4-D TMA boxes (L2
-//    hits: the score CTA just read the same lines), issues O += P.V with
-//    tcgen05 (N = 256), applies the rescale when the softmax max moved, and
-//    writes the normalised output.
+//    V into a 3-slot ring with TMA (L2 hits: the score CTA just read the
+//    same lines), issues O += P.V with tcgen05 (N = 256), applies the
+//    rescale when the softmax maximum moved, and writes the normalised
+//    output.
+// FP8 (E4M3) cache, the template's second instance: K and V are read as
+// bytes (576 per token, half the bf16 traffic) and multiplied on the tensor
+// core in kind::f8f6f4. Q and P, which are not 8-bit quantities, enter the
+// MMAs as two E4M3 terms each (hi + lo, about 8 significant bits, as bf16
+// has), so each product is two MMAs; Q carries a per-row power-of-two scale
+// and the per-tensor cache scale is applied in fp32 to the scores and the
+// output.
 // Heads below 128 are padded inside the kernel: zero Q rows in tensor memory
 // and zero P rows in shared memory, never stored.
 #include <cuda_runtime.h>
@@ -45,8 +51,8 @@ constexpr int kQPrefetchLead = 4;   // tiles before an item's end: L2 prefetch o
 // Control block: identical offsets in both CTAs of the pair, so a barrier can
 // be addressed in the peer by offset (mapa, multicast commit).
 struct Ctrl {
-  uint64_t kv_full[kNumStages];   // score: all pieces of a stage landed (TMA bytes)
-  uint64_t kv_empty[kNumStages];  // score: S MMAs done reading the stage
+  uint64_t kv_full[kF8NumStages];   // score: all pieces of a stage landed (TMA bytes)
+  uint64_t kv_empty[kF8NumStages];  // score: S MMAs done reading the stage
   uint64_t s_full[2];             // score: S tile in tensor memory
   uint64_t s_free[2];             // score: softmax copied S out
   uint64_t q_ready[kNumPanels];   // score: Q of the next item in tensor memory, per panel
@@ -64,27 +70,30 @@ struct Ctrl {
   uint64_t o_ready[kNumPBufs];
   uint64_t o_done[2];             // output: P.V of tile g complete (alternating)
   uint64_t o_drained[2];          // output: epilogue has read O columns [256h, 256h+256) of an item
+  uint64_t qs_ready[kF8QScaleSlots];  // score (FP8): the Q row scales of an item are in their slot
   uint32_t tmem_base;
   int32_t p_seen;                 // output: P tiles received so far (paces the prefetcher)
-  int32_t k_issued;               // score: K tiles whose TMA loads are issued (paces the prefetcher)
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTile, 0, 0);   // K-major A and B
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);    // V is MN-major
-constexpr float kRescaleThreshold = 8.0f;                        // log2 units
+constexpr uint32_t kIdescS8 = idesc_e4m3_f32(128, kTile, 0, 0);  // FP8: same shapes
+constexpr uint32_t kIdescPV8 = idesc_e4m3_f32(128, 256, 0, 1);
 constexpr uint32_t kFullMask = 0xffffffffu;
-#ifndef PF_TILES
-#define PF_TILES 4
-#endif
-constexpr int kPrefetchTiles = PF_TILES;   // output prefetcher: distance ahead of received P (tiles)
-#ifndef PF_MODE
-#define PF_MODE 0
-#endif
-#ifndef PF_DIST
-#define PF_DIST 4
-#endif
-constexpr int kPfDist = PF_DIST;    // score prefetcher: tiles ahead of the TMA producer
+constexpr int kPrefetchTiles = 4;   // output prefetcher: distance ahead of received P (tiles)
+
+// Lazy rescale threshold (log2 units): the running row maximum moves only
+// when a tile's maximum exceeds it by more than this. bf16 P takes p up to
+// 2^8. The FP8 path stores P as two E4M3 terms and scales it by
+// 2^kF8PShift, so p * 2^kF8PShift <= 2^(threshold + shift) = 256 stays below
+// E4M3's 448 while the smallest p kept (E4M3's 2^-9 subnormal step) is
+// 2^-13 of the running maximum's weight.
+template <bool F8> __host__ __device__ constexpr float rescale_threshold() { return F8 ? 4.0f : 8.0f; }
+constexpr float kF8PShift = 4.0f;
+
+template <bool F8> __host__ __device__ constexpr int num_stages() { return F8 ? kF8NumStages : kNumStages; }
+template <bool F8> __host__ __device__ constexpr int stage_bytes() { return F8 ? kF8StageBytes : kStageBytes; }
 
 MLA_DEVI int tiles_of(const WorkItem& it) {
   return it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
@@ -120,10 +129,6 @@ MLA_DEVI int heads_of(const DecodeParams& p, const WorkItem& it) {
 
 MLA_DEVI void report(const DecodeParams& p, uint32_t bits) {
   if (bits) atomicOr(p.err, bits);
-}
-
-MLA_DEVI void named_barrier_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
 
 // Optional timeline instrumentation (compiled only with -DMLA_TRACE): each
@@ -206,17 +211,23 @@ MLA_DEVI bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
 
 // ------------------------------------------------------------ score CTA roles
 
-// TMA producer warp: each 80-token tile into stage g % 2, one 4-D box per
-// page piece (all 9 panels), lane j loading piece j. The stage layout
-// [row group][panel][8 rows][128 B] does not depend on how the tile is cut
-// into pieces; one barrier per stage counts the bytes of all pieces.
+// TMA producer warp: each 96-token tile into stage g % stages, one 4-D box
+// per page piece, lane j loading piece j. bf16: one box of all 9 panels. FP8:
+// lanes 0..15 load the 512 c_kv columns (4 panels) and lanes 16..31 the 64
+// rope columns of the same pieces. The stage layout does not depend on how
+// the tile is cut into pieces; one barrier per stage counts the bytes of all
+// pieces.
+template <bool F8>
 MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int lane, int it0,
                              int it1) {
+  constexpr int NS = num_stages<F8>();
+  constexpr int SB = stage_bytes<F8>();
   uint32_t err = 0;
   const uint64_t policy = policy_evict_normal();
   int g = 0;
   bool ok = true;
   const int n = pieces_per_tile(p.block_size);
+  const int j = F8 ? (lane & 15) : lane;   // this lane's piece
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = item_at(p, it);
     if (lane == 0) {   // MLA_DEVERR_SEQLEN_MISMATCH: not the planned length, or above the bound
@@ -241,105 +252,61 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
           break;
         }
       }
-      const int s = g & 1;
+      const int s = g % NS;
       const int tile_t0 = w.t0 + i * kTile;
       int r0, large;
-      piece_shape(p.block_size, lane < n ? lane : 0, r0, large);
+      piece_shape(p.block_size, j < n ? j : 0, r0, large);
       window_cover(p, w, tile_t0, win, lane);
       const int y = cache_row(p, w, tile_t0 + r0, win, err);   // a multiple of 8
       MLA_TRACE_AT(0, g);
-      if (g >= kNumStages &&
-          !warp_wait(smem_addr(&c->kv_empty[s]), ((g >> 1) - 1) & 1, lane)) {
+      if (g >= NS && !warp_wait(smem_addr(&c->kv_empty[s]), ((g / NS) - 1) & 1, lane)) {
         ok = false;
         break;
       }
       const uint32_t full = smem_addr(&c->kv_full[s]);
-      if (lane == 0) mbar_arrive_expect_tx(full, kStageBytes);
+      if (lane == 0) mbar_arrive_expect_tx(full, SB);
       __syncwarp();
-      if (lane < n)
-        tma_load_4d(smem_addr(data + s * kStageBytes + (r0 >> 3) * kKGroupBytes),
-                    large ? static_cast<const void*>(&p.tmap_k32)
-                          : static_cast<const void*>(&p.tmap_k16),
-                    0, 0, 0, y >> 3, full, policy);
-      if (lane == 0) {
-        MLA_TRACE_AT(26, g);
-        *reinterpret_cast<volatile int32_t*>(&c->k_issued) = g + 1;
+      uint8_t* stage = data + s * SB;
+      if (!F8) {
+        if (lane < n)
+          tma_load_4d(smem_addr(stage + (r0 >> 3) * kKGroupBytes),
+                      large ? static_cast<const void*>(&p.tmap_k32)
+                            : static_cast<const void*>(&p.tmap_k16),
+                      0, 0, 0, y >> 3, full, policy);
+      } else if (j < n) {
+        if (lane < 16)
+          tma_load_4d(smem_addr(stage + (r0 >> 3) * kF8NopeGroupBytes),
+                      large ? static_cast<const void*>(&p.tmap_k32)
+                            : static_cast<const void*>(&p.tmap_k16),
+                      0, 0, 0, y >> 3, full, policy);
+        else
+          tma_load_3d(smem_addr(stage + kF8NopeBytes + (r0 >> 3) * kF8RopeGroupBytes),
+                      large ? static_cast<const void*>(&p.tmap_v32)
+                            : static_cast<const void*>(&p.tmap_v16),
+                      0, 0, y >> 3, full, policy);
       }
+      if (lane == 0) MLA_TRACE_AT(26, g);
     }
   }
-  // Release the prefetcher whatever happened (it paces itself on this count).
-  if (lane == 0) *reinterpret_cast<volatile int32_t*>(&c->k_issued) = 0x7fffffff;
   if (!ok) err |= 4u;
   err = __reduce_or_sync(kFullMask, err);
   if (lane == 0) report(p, err);
 }
 
-// L2 prefetch warp of the score CTA: walks the pair's tiles kPfDist ahead of
-// the tiles whose loads the TMA producer has issued and prefetches each tile's
-// cache rows into L2, so the producer's loads find them there. The rows of a
-// tile are page-aligned runs (the same pieces the producer loads), each a
-// contiguous range of whole 1152-byte rows.
-MLA_DEVI void score_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0, int it1) {
-  const char* cache = reinterpret_cast<const char*>(p.kv_cache);
-  volatile int32_t* issued = &c->k_issued;
-  uint32_t err = 0;
-  int g = 0;
-  const int n = pieces_per_tile(p.block_size);
-  for (int it = it0; it < it1; ++it) {
-    const WorkItem w = item_at(p, it);
-    const int nt = tiles_of(w);
-    PageWindow win;
-    for (int i = 0; i < nt; ++i, ++g) {
-      int ahead_ok = 1;
-      if (lane == 0) {
-        const long long t0 = clock64();
-        while (*issued < g - kPfDist + 1) {
-          if (clock64() - t0 > kWaitLimitCycles) { ahead_ok = 0; break; }
-          __nanosleep(256);
-        }
-      }
-      if (!__shfl_sync(kFullMask, ahead_ok, 0)) return;
-      const int tile_t0 = w.t0 + i * kTile;
-      window_cover(p, w, tile_t0, win, lane);
-#if PF_MODE == 2
-      // One bulk prefetch per piece (lane j: piece j).
-      int r0, large;
-      piece_shape(p.block_size, lane < n ? lane : 0, r0, large);
-      const int y = cache_row(p, w, tile_t0 + r0, win, err);
-      const int rows = min(large ? kRowsLargeBox : kRowsSmallBox, w.t1 - (tile_t0 + r0));
-      if (lane < n && rows > 0 && y < static_cast<int>(p.num_blocks * p.block_size))
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                     :: "l"(cache + static_cast<int64_t>(y) * (kD * 2)), "r"(rows * kD * 2) : "memory");
-#else
-      // Per-line prefetches: the warp walks each piece's 128-byte lines.
-      for (int j = 0; j < n; ++j) {
-        int r0, large;
-        piece_shape(p.block_size, j, r0, large);
-        const int y = cache_row(p, w, tile_t0 + r0, win, err);
-        const int rows = min(large ? kRowsLargeBox : kRowsSmallBox, w.t1 - (tile_t0 + r0));
-        if (rows <= 0 || y >= static_cast<int>(p.num_blocks * p.block_size)) continue;
-        const char* base = cache + static_cast<int64_t>(y) * (kD * 2);
-        for (int ln = lane; ln < rows * (kD * 2 / 128); ln += 32)
-          asm volatile("prefetch.global.L2 [%0];" :: "l"(base + ln * 128));
-      }
-#endif
-    }
-  }
-  (void)err;   // bad block ids are reported by the producer
-}
-
-// S MMA issuer: S[g%2] = Q . K^T over the 576 columns, 36 k-steps of 16 with
-// N = 80 (the whole tile: its 8-row atoms are kKGroupBytes apart in the
-// stage whichever pages they came from). The steady-state loop is fully
-// unrolled: one thread issues one MMA every ~50 cycles at best.
-#ifndef S_ISSUERS
-#define S_ISSUERS 1
-#endif
+// S MMA issuer: S[g%2] = Q . K^T over the 576 columns with N = 96 (the
+// whole tile: its 8-row atoms sit at fixed offsets in the stage whichever
+// pages they came from). bf16: 36 k-steps of 16 columns. FP8: 18 k-steps of
+// 32 columns, each issued twice, for the hi and the lo terms of Q (both in
+// tensor memory) against the same K columns. An item's first tile follows
+// its Q into tensor memory panel by panel; later tiles issue the fully
+// unrolled sequence (one thread issues one MMA every ~45 cycles at best).
+template <bool F8>
 MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
-                        int it1, int sel) {
+                        int it1) {
+  constexpr int NS = num_stages<F8>();
+  constexpr int SB = stage_bytes<F8>();
   int g = 0, n_items = 0;
   bool ok = true;
-  constexpr uint32_t idesc = kIdescS;
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = item_at(p, it);
     const int nt = tiles_of(w);
@@ -347,49 +314,78 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
     const uint32_t q_par = n_items & 1;
     ++n_items;
     for (int i = 0; i < nt; ++i, ++g) {
-      if (S_ISSUERS > 1 && (g & 1) != sel) continue;   // the other issuer's tile
-      const int s = g & 1;
-      // With two issuers, the one taking an item's second tile makes sure
-      // all of Q is in tensor memory (its last panel barrier completes last).
-      if (S_ISSUERS > 1 && i == 1 && !mbar_wait(smem_addr(&c->q_ready[kNumPanels - 1]), q_par)) {
-        ok = false;
-        break;
-      }
-      if (g >= 2 && !mbar_wait(smem_addr(&c->s_free[s]), ((g >> 1) - 1) & 1)) { ok = false; break; }
+      const int s = g % NS;    // KV stage
+      const int sb = g & 1;    // S buffer
+      if (g >= 2 && !mbar_wait(smem_addr(&c->s_free[sb]), ((g >> 1) - 1) & 1)) { ok = false; break; }
       MLA_TRACE_AT(2, g);
-      if (!mbar_wait(smem_addr(&c->kv_full[s]), (g >> 1) & 1)) { ok = false; break; }
+      if (!mbar_wait(smem_addr(&c->kv_full[s]), (g / NS) & 1)) { ok = false; break; }
       MLA_TRACE_AT(1, g);
       tc_after_sync();
-      const uint32_t d = tmem + kTmemS0 + s * kTile;
-      // Descriptor of panel 0 (8-row atoms kKGroupBytes apart); later k-steps
-      // only move the start-address field (low word, 16-byte units, never
-      // carries out): +1 KB per panel, +32 B per k-step.
-      const uint64_t bp = smem_desc(smem_addr(data + s * kStageBytes), 16, kKGroupBytes);
-      const uint32_t hi = static_cast<uint32_t>(bp >> 32);
-      uint32_t blo = static_cast<uint32_t>(bp);
-      uint32_t a = tmem + kTmemQ;
-      if (i == 0) {
-        // First tile of an item: its Q arrives panel by panel.
+      const uint32_t d = tmem + kTmemS0 + sb * kTile;
+      const uint32_t a = tmem + kTmemQ;
+      uint8_t* stage = data + s * SB;
+      if (!F8) {
+        // Descriptor of panel 0 (8-row atoms kKGroupBytes apart); later
+        // k-steps only move the start-address field (low word, 16-byte units,
+        // never carries out): +1 KB per panel, +32 B per k-step.
+        const uint64_t bp = smem_desc(smem_addr(stage), 16, kKGroupBytes);
+        const uint32_t hi = static_cast<uint32_t>(bp >> 32);
+        const uint32_t blo = static_cast<uint32_t>(bp);
+        if (i == 0) {
 #pragma unroll 1
-        for (int pc = 0; pc < kNumPanels; ++pc, a += 32, blo += kAtomBytes / 16) {
-          if (!mbar_wait(smem_addr(&c->q_ready[pc]), q_par)) { ok = false; break; }
-          tc_after_sync();
+          for (int pc = 0; pc < kNumPanels; ++pc) {
+            if (!mbar_wait(smem_addr(&c->q_ready[pc]), q_par)) { ok = false; break; }
+            tc_after_sync();
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            mma_ts(d, a + q * 8, (static_cast<uint64_t>(hi) << 32) | (blo + q * 2), idesc,
-                   (pc > 0 || q > 0) ? 1u : 0u);
+            for (int q = 0; q < 4; ++q)
+              mma_ts(d, a + pc * 32 + q * 8,
+                     (static_cast<uint64_t>(hi) << 32) | (blo + pc * (kAtomBytes / 16) + q * 2),
+                     kIdescS, (pc > 0 || q > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+        } else {
+#pragma unroll
+          for (int kq = 0; kq < kNumPanels * 4; ++kq)   // panel kq/4, 32 bytes per k-step
+            mma_ts(d, a + kq * 8,
+                   (static_cast<uint64_t>(hi) << 32) | (blo + (kq >> 2) * (kAtomBytes / 16) + (kq & 3) * 2),
+                   kIdescS, kq > 0 ? 1u : 0u);
         }
-        if (!ok) break;
       } else {
+        // c_kv columns: 128-byte panels 1 KB apart, 8-row groups
+        // kF8NopeGroupBytes apart, 32 bytes per k-step; rope columns: one
+        // 64-byte-swizzled panel, 8-row groups kF8RopeGroupBytes apart.
+        const uint64_t kn = smem_desc(smem_addr(stage), 16, kF8NopeGroupBytes);
+        const uint64_t kr = smem_desc(smem_addr(stage + kF8NopeBytes), 16, kF8RopeGroupBytes,
+                                      kLayoutSw64);
+        auto kdesc = [&](int ks) -> uint64_t {
+          return ks < 16 ? kn + static_cast<uint64_t>((ks >> 2) * (kAtomBytes / 16) + (ks & 3) * 2)
+                         : kr + static_cast<uint64_t>((ks - 16) * 2);
+        };
+        if (i == 0) {
+          // Q arrives two k-steps (64 columns, hi and lo) per barrier.
+#pragma unroll 1
+          for (int pc = 0; pc < kNumPanels; ++pc) {
+            if (!mbar_wait(smem_addr(&c->q_ready[pc]), q_par)) { ok = false; break; }
+            tc_after_sync();
 #pragma unroll
-        for (int kq = 0; kq < kNumPanels * 4; ++kq)   // panel kq/4, 32 bytes per k-step
-          mma_ts(d, a + kq * 8,
-                 (static_cast<uint64_t>(hi) << 32) | (blo + (kq >> 2) * (kAtomBytes / 16) + (kq & 3) * 2),
-                 idesc, kq > 0 ? 1u : 0u);
+            for (int q = 0; q < 2; ++q) {
+              const int ks = 2 * pc + q;
+              mma_ts_f8(d, a + ks * 8, kdesc(ks), kIdescS8, ks > 0 ? 1u : 0u);
+              mma_ts_f8(d, a + kF8QLoCol + ks * 8, kdesc(ks), kIdescS8, 1u);
+            }
+          }
+          if (!ok) break;
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < kD / 32; ++ks) {
+            mma_ts_f8(d, a + ks * 8, kdesc(ks), kIdescS8, ks > 0 ? 1u : 0u);
+            mma_ts_f8(d, a + kF8QLoCol + ks * 8, kdesc(ks), kIdescS8, 1u);
+          }
+        }
       }
       MLA_TRACE_AT(24, g);
       tc_commit(smem_addr(&c->kv_empty[s]));
-      tc_commit(smem_addr(&c->s_full[s]));
+      tc_commit(smem_addr(&c->s_full[sb]));
       if (i == nt - 1) tc_commit(smem_addr(&c->q_free));   // Q may now be replaced
       MLA_TRACE_AT(3, g);
     }
@@ -461,21 +457,109 @@ __device__ __noinline__ bool load_q(const DecodeParams& p, Ctrl* c, const WorkIt
   return true;
 }
 
+// FP8 path: Q of item w as two E4M3 terms per element in tensor memory, hi
+// codes in columns [0, 144) and lo codes in [144, 288) of lane `row`, with a
+// per-row power-of-two scale: q = 2^k (hi + lo), where 2^k puts max|q| of
+// the row in [128, 256). A bf16 q has 8 significant bits, so hi + lo holds it
+// exactly unless |q| < 2^-9 max|q| (then the error is below 2^-17 max|q|).
+// Each thread handles its own row: a first pass over the row finds max|q|
+// (as the largest bf16 magnitude pattern, whose order is that of the
+// values), writes 2^k into qscale (the ring slot of this item) and arrives on
+// qs_ready[slot]; then, when wait_parity >= 0, the warp waits on q_free and
+// converts the row 32 columns at a time, announcing each 64 columns (both
+// terms) on q_ready. Rows past the group's heads are zero.
+__device__ __noinline__ bool load_q_f8(const DecodeParams& p, Ctrl* c, float* qscale,
+                                       const WorkItem& w, int row, uint32_t trow,
+                                       int wait_parity, int slot) {
+  const int lane = row & 31;
+  const bool active = row < heads_of(p, w);
+  const int64_t r = static_cast<int64_t>(w.b) * p.H + w.h0 + (active ? row : 0);
+  const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + r * kDc);   // 64 x 16 B
+  const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + r * kDr);     // 8 x 16 B
+  auto chunk = [&](int j) -> uint4 {   // 16-byte piece j < 72 of the row
+    return active ? __ldg(j < kDc / 8 ? qn + j : qp + (j - kDc / 8)) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  uint32_t mx = 0;
+#pragma unroll 8
+  for (int j = 0; j < kD / 8; ++j) {
+    const uint4 v = chunk(j);
+    mx = __vmaxu2(mx, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                               __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+  }
+  mx = max(mx & 0xFFFFu, mx >> 16);
+  // Biased exponent E of max|q| (clamped so 2^k and 2^-k are normal fp32):
+  // max|q| / 2^k lies in [128, 256) for k = E - 134.
+  const int E = min(254, max(8, static_cast<int>(mx >> 7)));
+  const float inv_s = __uint_as_float(static_cast<uint32_t>(261 - E) << 23);   // 2^-k
+  qscale[slot * kMaxHeads + row] = __uint_as_float(static_cast<uint32_t>(E - 7) << 23);   // 2^k
+  mbar_arrive(smem_addr(&c->qs_ready[slot]));
+  if (wait_parity >= 0) {
+    if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->q_free), static_cast<uint32_t>(wait_parity))))
+      return false;
+    tc_after_sync();
+  }
+  const uint64_t is2 = pack_f32x2(inv_s, inv_s);
+  uint4 nxt[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) nxt[e] = chunk(e);
+#pragma unroll 1
+  for (int cc = 0; cc < kD / 32; ++cc) {   // 32 columns: four 16-byte pieces
+    uint4 v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = nxt[e];
+    if (cc + 1 < kD / 32) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) nxt[e] = chunk(4 * (cc + 1) + e);
+    }
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t wd[4] = {v[e].x, v[e].y, v[e].z, v[e].w};
+#pragma unroll
+      for (int k = 0; k < 4; k += 2) {
+        // bf16 pairs (2 elements per word) -> fp32, scaled by 2^-k (exact).
+        const uint32_t a = split_e4m3x2(mul_f32x2(pack_b32x2(wd[k] << 16, wd[k] & 0xFFFF0000u), is2));
+        const uint32_t b =
+            split_e4m3x2(mul_f32x2(pack_b32x2(wd[k + 1] << 16, wd[k + 1] & 0xFFFF0000u), is2));
+        hw[2 * e + k / 2] = (a & 0xFFFFu) | (b << 16);
+        lw[2 * e + k / 2] = (a >> 16) | (b & 0xFFFF0000u);
+      }
+    }
+    tmem_st8(trow + kTmemQ + cc * 8, hw);
+    tmem_st8(trow + kTmemQ + kF8QLoCol + cc * 8, lw);
+    // tcgen05.st reads its source registers asynchronously: complete the
+    // stores before the next chunk reuses hw and lw.
+    tmem_wait_st();
+    if (cc & 1) {
+      tc_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&c->q_ready[cc >> 1]));
+    }
+  }
+  return true;
+}
+
 // Q loader warps (one per tensor-memory lane quadrant): the Q of each of the
 // pair's items in turn, so the softmax warps never stop for it. Each call
-// loads the next item's first Q panels into registers right after the
-// previous Q is written, then waits on q_free for the S MMAs of the previous
-// item's last tile (phase j - 1 for the j-th non-empty item: the barrier
-// cannot run ahead, since item j's last tile needs this Q first).
-MLA_DEVI void score_qloader(const DecodeParams& p, Ctrl* c, uint32_t tmem, int warp, int lane,
-                            int it0, int it1) {
+// reads the next item's Q right after the previous Q is written (bf16: its
+// first panels into registers; FP8: the row maxima and scales), then waits
+// on q_free for the S MMAs of the previous item's last tile (phase j - 1 for
+// the j-th non-empty item: the barrier cannot run ahead, since item j's last
+// tile needs this Q first).
+template <bool F8>
+MLA_DEVI void score_qloader(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem,
+                            int warp, int lane, int it0, int it1) {
   const int row = (warp & 3) * 32 + lane;
   const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  float* qscale = reinterpret_cast<float*>(data + kF8NumStages * kF8StageBytes);
   int n_items = 0;
   for (int it = it0; it < it1; ++it) {
     if (tiles_of(item_at(p, it)) == 0) continue;
     const int wait_parity = n_items > 0 ? (n_items - 1) & 1 : -1;
-    if (!load_q(p, c, item_at(p, it), row, trow, wait_parity)) {
+    const bool ok = F8 ? load_q_f8(p, c, qscale, item_at(p, it), row, trow, wait_parity,
+                                   n_items % kF8QScaleSlots)
+                       : load_q(p, c, item_at(p, it), row, trow, wait_parity);
+    if (!ok) {
       if (lane == 0) report(p, 4u);
       return;
     }
@@ -510,6 +594,43 @@ MLA_DEVI float softmax_tile(const uint32_t (&r)[kTile], uint64_t sl2x2, uint64_t
   return ls0 + ls1;
 }
 
+// FP8 path: the same pass with p' = 2^(s * c - m') stored as two E4M3 terms
+// (split_e4m3x2): 16-token chunks of hi codes into core-matrix columns 0..5
+// of the row and the matching lo codes into columns 6..11. The p' values of
+// a chunk replace its scores in r (the role's register budget has no room
+// for a second copy). Returns the row sum of the p' values (fp32, before the
+// split).
+MLA_DEVI float softmax_tile_f8(uint32_t (&r)[kTile], uint64_t c2, uint64_t negm2,
+                               uint32_t p_dst, uint32_t peer_bar) {
+  uint64_t ls2 = pack_f32x2(0.0f, 0.0f);
+#pragma unroll
+  for (int q = 0; q < kTile / 16; ++q) {
+#pragma unroll
+    for (int j = 16 * q; j < 16 * q + 16; j += 2) {
+      float d0, d1;
+      unpack_f32x2(fma_f32x2(pack_b32x2(r[j], r[j + 1]), c2, negm2), d0, d1);
+      const float e0 = fast_exp2(d0);
+      const float e1 = fast_exp2(d1);
+      ls2 = add_f32x2(ls2, pack_f32x2(e0, e1));
+      r[j] = __float_as_uint(e0);
+      r[j + 1] = __float_as_uint(e1);
+    }
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+      const uint32_t a = split_e4m3x2(pack_b32x2(r[16 * q + j], r[16 * q + j + 1]));
+      const uint32_t b = split_e4m3x2(pack_b32x2(r[16 * q + j + 2], r[16 * q + j + 3]));
+      hw[j / 4] = (a & 0xFFFFu) | (b << 16);
+      lw[j / 4] = (a >> 16) | (b & 0xFFFF0000u);
+    }
+    st_async_v4(p_dst + q * 128, hw[0], hw[1], hw[2], hw[3], peer_bar);
+    st_async_v4(p_dst + (kTile / 16) * 128 + q * 128, lw[0], lw[1], lw[2], lw[3], peer_bar);
+  }
+  float ls0, ls1;
+  unpack_f32x2(ls2, ls0, ls1);
+  return ls0 + ls1;
+}
+
 // Largest of a tile's 96 raw scores.
 MLA_DEVI float tile_max(const uint32_t (&r)[kTile]) {
   float m0 = __uint_as_float(r[0]), m1 = __uint_as_float(r[1]), m2 = __uint_as_float(r[2]);
@@ -528,16 +649,26 @@ MLA_DEVI float tile_max(const uint32_t (&r)[kTile]) {
 // own (no barrier between the four warps per tile). Per tile: the 96 scores
 // are read from tensor memory with one wait, the S buffer is released at
 // once, the running row maximum m moves only when the tile's maximum exceeds
-// it by more than kRescaleThreshold (log2 units; always on an item's first
+// it by more than rescale_threshold (log2 units; always on an item's first
 // tile), and one pass writes P and the row record {alpha, l, m} into the
 // output CTA with remote stores.
+//
+// FP8 path: the raw scores carry the row's Q scale 2^k and the cache scale,
+// so the multiplier is c = sm_scale * log2(e) * kv_scale * 2^k (2^k read
+// from the Q loaders' ring slot of the item on its first tile, before the S
+// buffer is released: the loaders reuse a slot four items later, after the
+// S MMAs of a later tile, which wait for that release). P is shipped as
+// p' = p * 2^kF8PShift, and the record's m is m - kF8PShift, so that
+// lse = m + log2(l) and out = O / l hold unchanged.
+template <bool F8>
 MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem,
                             int warp, int lane, int it0, int it1) {
   const int row = (warp & 3) * 32 + lane;
   const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const bool elected = (warp == 2 && lane == 0);
   const float sl2 = p.scale_log2;
-  const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+  float c_row = sl2;
+  int n_items = 0;
   // Peer (output CTA) P buffers, record ring and p_full barriers.
   const uint32_t peer_pbuf0 = map_to_rank(smem_addr(data + kNumVSlots * kVHalfBytes), 1);
   const uint32_t peer_rec0 =
@@ -556,6 +687,7 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
     int nxt = cur + 1;
     while (nxt < it1 && tiles_of(item_at(p, nxt)) == 0) ++nxt;
     float m_used = -INFINITY, l = 0.0f;
+    const int item = n_items++;
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
       const int k = g % kNumPBufs;
@@ -576,6 +708,22 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < kTile; j += 8) reg_fence8(&r[j]);
+      if (F8 && i == 0) {
+        const int slot = item % kF8QScaleSlots;
+        if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->qs_ready[slot]),
+                                             (item / kF8QScaleSlots) & 1))) {
+          ok = false;
+          break;
+        }
+        // (a 32-bit shared-memory address keeps this path within the
+        // register budget of the role)
+        float qs;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qs)
+                     : "r"(smem_addr(data) + kF8NumStages * kF8StageBytes +
+                           (slot * kMaxHeads + row) * 4)
+                     : "memory");
+        c_row = sl2 * p.kv_scale * qs;
+      }
       // The scores are in registers: the S buffer may take tile g + 2.
       tc_before_sync();
       mbar_arrive(smem_addr(&c->s_free[s]));
@@ -585,11 +733,11 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
         for (int j = 0; j < kTile; ++j) r[j] = j < valid ? r[j] : 0xFF800000u;
       }
       // Lazy rescale: keep the running maximum unless the tile's maximum lies
-      // more than kRescaleThreshold above it (always on an item's first tile,
+      // more than the threshold above it (always on an item's first tile,
       // where m is -inf); P rescaled by alpha then reaches the output CTA.
-      const float m_tile = tile_max(r) * sl2;
+      const float m_tile = tile_max(r) * c_row;
       float alpha = 1.0f;
-      if (m_tile > m_used + kRescaleThreshold) {
+      if (m_tile > m_used + rescale_threshold<F8>()) {
         alpha = fast_exp2(m_used - m_tile);   // 0 on an item's first tile
         l *= alpha;
         m_used = m_tile;
@@ -610,10 +758,15 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       if (row == 0) MLA_TRACE_AT(5, g);
       const uint32_t bar = peer_pfull0 + k * 8;
       // A row that has seen no token yet (m = -inf) writes p = 0.
-      const float mneg = m_used == -INFINITY ? 0.0f : -m_used;
-      l += softmax_tile(r, sl2x2, pack_f32x2(mneg, mneg), peer_pbuf0 + k * kPBytes + prow_off, bar);
+      const float m_eff = F8 ? m_used - kF8PShift : m_used;
+      const float mneg = m_used == -INFINITY ? 0.0f : -m_eff;
+      const uint64_t c2 = pack_f32x2(c_row, c_row);
+      if (F8)
+        l += softmax_tile_f8(r, c2, pack_f32x2(mneg, mneg), peer_pbuf0 + k * kPBytes + prow_off, bar);
+      else
+        l += softmax_tile(r, c2, pack_f32x2(mneg, mneg), peer_pbuf0 + k * kPBytes + prow_off, bar);
       st_async_v4(peer_rec0 + (g % kNumRecSlots) * kRecBytes + row * 16, __float_as_uint(alpha),
-                  __float_as_uint(l), __float_as_uint(m_used), 0u, bar);
+                  __float_as_uint(l), __float_as_uint(m_eff), 0u, bar);
       if (row == 0) MLA_TRACE_AT(6, g);
     }
     cur = nxt;
@@ -633,9 +786,13 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
 
 // ----------------------------------------------------------- output CTA roles
 
-// TMA producer warp: V half-tiles (4 panels = 256 columns) into a 4-slot ring.
+// TMA producer warp of the output CTA: V into a ring of kNumVSlots 48 KB
+// slots. bf16: each tile as two half-tiles of 256 columns (4 panels); FP8:
+// each tile's 512 columns in one slot.
+template <bool F8>
 MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int lane, int it0,
                            int it1) {
+  constexpr int kParts = F8 ? 1 : 2;   // slots per tile
   uint32_t err = 0;
   const uint64_t policy = policy_evict_first();   // last use of these lines
   int h = 0;
@@ -651,23 +808,29 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
       piece_shape(p.block_size, lane < n ? lane : 0, r0, large);
       window_cover(p, w, tile_t0, win, lane);
       const int y = cache_row(p, w, tile_t0 + r0, win, err);
-      for (int half = 0; half < 2; ++half, ++h) {
+      for (int half = 0; half < kParts; ++half, ++h) {
         const int v = h % kNumVSlots;
         if (h >= kNumVSlots &&
             !warp_wait(smem_addr(&c->v_empty[v]), ((h / kNumVSlots) - 1) & 1, lane)) {
           ok = false;
           break;
         }
-        MLA_TRACE_AT(8 + half, h >> 1);
+        MLA_TRACE_AT(8 + half, h / kParts);
         const uint32_t full = smem_addr(&c->v_full[v]);
         if (lane == 0) mbar_arrive_expect_tx(full, kVHalfBytes);
         __syncwarp();
-        // One warp instruction: lane j loads piece j (4 panels of this half).
+        // One warp instruction: lane j loads piece j.
         if (lane < n) {
-          tma_load_4d(smem_addr(data + v * kVHalfBytes) + (r0 >> 3) * kVGroupBytes,
-                      large ? static_cast<const void*>(&p.tmap_v32)
-                            : static_cast<const void*>(&p.tmap_v16),
-                      0, 0, half * kVHalfPanels, y >> 3, full, policy);
+          if (F8)
+            tma_load_4d(smem_addr(data + v * kVHalfBytes) + (r0 >> 3) * kF8NopeGroupBytes,
+                        large ? static_cast<const void*>(&p.tmap_k32)
+                              : static_cast<const void*>(&p.tmap_k16),
+                        0, 0, 0, y >> 3, full, policy);
+          else
+            tma_load_4d(smem_addr(data + v * kVHalfBytes) + (r0 >> 3) * kVGroupBytes,
+                        large ? static_cast<const void*>(&p.tmap_v32)
+                              : static_cast<const void*>(&p.tmap_v16),
+                        0, 0, half * kVHalfPanels, y >> 3, full, policy);
         }
       }
     }
@@ -681,10 +844,11 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
 // ahead of the P tiles received so far and issues per-line L2 prefetches
 // (load/store path) for the cache pages of those tiles, so the score CTA's
 // TMA loads find them in L2. Pages are contiguous blocks of block_size x
-// 1152 bytes; each page is prefetched once per item.
+// row bytes (1152 bf16, 576 FP8); each page is prefetched once per item.
 MLA_DEVI void out_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0, int it1) {
   const char* cache = reinterpret_cast<const char*>(p.kv_cache);
-  const int lines = p.block_size * (kD * 2 / 128);
+  const int row_bytes = p.kv_fp8 ? kD : kD * 2;
+  const int lines = p.block_size * row_bytes / 128;   // block sizes are multiples of 16
   volatile int32_t* seen = &c->p_seen;
   int g = 0;
   for (int it = it0; it < it1; ++it) {
@@ -715,7 +879,7 @@ MLA_DEVI void out_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0, 
         }
         const int blk = __shfl_sync(kFullMask, win.val, page - win.base);
         if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) continue;
-        const char* base = cache + static_cast<int64_t>(blk) * p.block_size * (kD * 2);
+        const char* base = cache + static_cast<int64_t>(blk) * p.block_size * row_bytes;
         for (int ln = lane; ln < lines; ln += 32)
           asm volatile("prefetch.global.L2 [%0];" :: "l"(base + ln * 128));
       }
@@ -727,6 +891,10 @@ MLA_DEVI void out_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0, 
 // An item's first tile overwrites O, so it waits for P itself (no rescale is
 // due) and, per half, for the epilogue of the previous item to have read
 // those columns; later tiles wait for the correction warps' o_ready.
+//
+// FP8 path: one V slot per tile; per 256-column half, the hi and the lo terms
+// of P each take 3 k-steps of 32 tokens (6 MMAs with N = 256).
+template <bool F8>
 MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
                       int it1) {
   int g = 0, h = 0, r = 0, n_items = 0;
@@ -760,22 +928,50 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
       a0 |= static_cast<uint64_t>(128 >> 4) << 16;
       a0 |= static_cast<uint64_t>(kPGroupBytes >> 4) << 32;
       a0 |= static_cast<uint64_t>(1) << 46;
-      for (int half = 0; half < 2; ++half, ++h) {
-        const int v = h % kNumVSlots;
-        if (i == 0 && item > 0 &&
-            !mbar_wait(smem_addr(&c->o_drained[half]), (item - 1) & 1)) { ok = false; break; }
-        if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
-        MLA_TRACE_AT(11 + half, g);
-        tc_after_sync();
-        // V half: MN-major, 128-byte swizzle; 64-column panels 1 KB apart
-        // (LBO), 8-token row groups kVGroupBytes apart (SBO); a k-step of 16
-        // tokens is two row groups.
-        const uint64_t b0 = smem_desc(smem_addr(data + v * kVHalfBytes), kAtomBytes, kVGroupBytes);
+      if (!F8) {
+        for (int half = 0; half < 2; ++half, ++h) {
+          const int v = h % kNumVSlots;
+          if (i == 0 && item > 0 &&
+              !mbar_wait(smem_addr(&c->o_drained[half]), (item - 1) & 1)) { ok = false; break; }
+          if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
+          MLA_TRACE_AT(11 + half, g);
+          tc_after_sync();
+          // V half: MN-major, 128-byte swizzle; 64-column panels 1 KB apart
+          // (LBO), 8-token row groups kVGroupBytes apart (SBO); a k-step of
+          // 16 tokens is two row groups.
+          const uint64_t b0 = smem_desc(smem_addr(data + v * kVHalfBytes), kAtomBytes, kVGroupBytes);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t ad = a0 + static_cast<uint64_t>((kk * 256) >> 4);
-          const uint64_t bd = b0 + static_cast<uint64_t>((kk * 2 * kVGroupBytes) >> 4);
-          mma_ss(tmem + half * 256, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t ad = a0 + static_cast<uint64_t>((kk * 256) >> 4);
+            const uint64_t bd = b0 + static_cast<uint64_t>((kk * 2 * kVGroupBytes) >> 4);
+            mma_ss(tmem + half * 256, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_addr(&c->v_empty[v]));
+        }
+      } else {
+        const int v = h % kNumVSlots;
+        if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
+        ++h;
+        tc_after_sync();
+        // V tile: MN-major, 128-byte swizzle; 128-column panels 1 KB apart
+        // (LBO), 8-token row groups kF8NopeGroupBytes apart (SBO); a k-step
+        // of 32 tokens is four row groups, a 256-column half two panels.
+        // P: hi codes in core-matrix columns 0..5, lo codes in 6..11.
+        const uint64_t b0 = smem_desc(smem_addr(data + v * kVHalfBytes), kAtomBytes, kF8NopeGroupBytes);
+        for (int half = 0; half < 2; ++half) {
+          if (i == 0 && item > 0 &&
+              !mbar_wait(smem_addr(&c->o_drained[half]), (item - 1) & 1)) { ok = false; break; }
+          MLA_TRACE_AT(11 + half, g);
+          tc_after_sync();
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < kTile / 32; ++kk) {
+              const uint64_t ad = a0 + static_cast<uint64_t>((part * (kTile / 16) * 128 + kk * 256) >> 4);
+              const uint64_t bd =
+                  b0 + static_cast<uint64_t>((half * 2 * kAtomBytes + kk * 4 * kF8NopeGroupBytes) >> 4);
+              mma_ss_f8(tmem + half * 256, ad, bd, kIdescPV8, (i > 0 || part > 0 || kk > 0) ? 1u : 0u);
+            }
         }
         tc_commit(smem_addr(&c->v_empty[v]));
       }
@@ -821,6 +1017,7 @@ MLA_DEVI void drain64(const DecodeParams& p, uint32_t taddr, float inv_l, bool t
 // land on p_full, which the elected thread arms two tiles ahead (one phase per
 // tile and buffer), so the MMA warp can also wait on it for an item's first
 // tile while these warps are still in the previous item's epilogue.
+template <bool F8>
 MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int warp,
                           int lane, int it0, int it1) {
   const int row = (warp & 3) * 32 + lane;
@@ -918,8 +1115,9 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
     }
     tc_after_sync();
     // A row without tokens in this item (possible with several query tokens
-    // per request) has l = 0: out = 0 and lse = -inf.
-    const float inv_l = l_fin > 0.0f ? 1.0f / l_fin : 0.0f;
+    // per request) has l = 0: out = 0 and lse = -inf. An FP8 cache's scale
+    // multiplies V here (and K through the softmax multiplier).
+    const float inv_l = l_fin > 0.0f ? (F8 ? p.kv_scale : 1.0f) / l_fin : 0.0f;
     const float lse_val = l_fin > 0.0f ? (m_fin + __log2f(l_fin)) * 0.69314718055994531f : -INFINITY;
     const bool to_out = w.slot < 0;
     uint16_t* out_row = (active && to_out) ? p.out + orow * kDc : nullptr;
@@ -945,6 +1143,7 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
   if (!ok) report(p, 4u);
 }
 
+template <bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -960,7 +1159,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNumStages; ++s) {
+    for (int s = 0; s < num_stages<F8>(); ++s) {
       mbar_init(smem_addr(&c->kv_full[s]), 1);
       mbar_init(smem_addr(&c->kv_empty[s]), 1);
     }
@@ -981,8 +1180,8 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->v_full[v]), 1);
       mbar_init(smem_addr(&c->v_empty[v]), 1);
     }
+    for (int j = 0; j < kF8QScaleSlots; ++j) mbar_init(smem_addr(&c->qs_ready[j]), 128);
     c->p_seen = 0;
-    c->k_issued = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -1003,38 +1202,24 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
 
   if (rank == 0) {
     if (warp == 0) {
-      score_producer(p, c, data, lane, it0, it1);
+      score_producer<F8>(p, c, data, lane, it0, it1);
     } else if (warp == 1) {
-      if (lane == 0) score_mma(p, c, data, tmem, it0, it1, 0);
+      if (lane == 0) score_mma<F8>(p, c, data, tmem, it0, it1);
     } else if (warp < 6) {
-      score_softmax(p, c, data, tmem, warp, lane, it0, it1);
+      score_softmax<F8>(p, c, data, tmem, warp, lane, it0, it1);
+    } else if (warp >= 8) {
+      score_qloader<F8>(p, c, data, tmem, warp, lane, it0, it1);
     }
-#if S_ISSUERS > 1
-    else if (warp == 7) {
-      if (lane == 0) score_mma(p, c, data, tmem, it0, it1, 1);
-    }
-#endif
-    else if (warp >= 8) {
-      score_qloader(p, c, tmem, warp, lane, it0, it1);
-    }
-#if PF_MODE != 0
-    else if (warp == 6) {
-      score_prefetcher(p, c, lane, it0, it1);
-    }
-#endif
   } else {
     if (warp == 0) {
-      out_producer(p, c, data, lane, it0, it1);
+      out_producer<F8>(p, c, data, lane, it0, it1);
     } else if (warp == 1) {
-      if (lane == 0) out_mma(p, c, data, tmem, it0, it1);
+      if (lane == 0) out_mma<F8>(p, c, data, tmem, it0, it1);
     } else if (warp < 6) {
-      out_correct(p, c, data, tmem, warp, lane, it0, it1);
-    }
-#if PF_MODE == 0
-    else if (warp == 6) {
+      out_correct<F8>(p, c, data, tmem, warp, lane, it0, it1);
+    } else if (warp == 6) {
       out_prefetcher(p, c, lane, it0, it1);
     }
-#endif
   }
   __syncwarp();
   tc_before_sync();
@@ -1054,7 +1239,10 @@ extern "C" cudaError_t mla_trace_set_buffer(void* dev_ptr) {
 #endif
 
 cudaError_t decode_prepare_device() {
-  return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemBytes);
 }
 
@@ -1072,11 +1260,15 @@ cudaError_t decode_max_clusters(int* num_clusters) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(num_clusters, mla_decode_kernel, &cfg);
+  // Both instantiations share the launch shape and shared-memory size.
+  return cudaOccupancyMaxActiveClusters(num_clusters, mla_decode_kernel<false>, &cfg);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int num_clusters, cudaStream_t stream) {
-  mla_decode_kernel<<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1), kSmemBytes, stream>>>(p);
+  if (p.kv_fp8)
+    mla_decode_kernel<true><<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1), kSmemBytes, stream>>>(p);
+  else
+    mla_decode_kernel<false><<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1), kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -51,6 +51,27 @@ constexpr int kPMsgBytes = kPBytes + kRecBytes;        // 26 KB of remote stores
 // of kNumRecSlots, so a record outlives the reuse of its P buffer.
 constexpr int kNumRecSlots = 4;
 static_assert(kNumRecSlots >= kNumPBufs + 1, "a record must outlive the reuse of its P buffer");
+// FP8 (E4M3) cache: 576-byte rows. Score stage: columns 0..511 as
+// [row group (12)][panel (4)][8 rows][128 B] with the 128-byte swizzle, then
+// columns 512..575 as [row group (12)][8 rows][64 B] with the 64-byte
+// swizzle (two TMA boxes per page piece, so no box reads past a row's end).
+// The output CTA loads the same 512-column layout as one V tile per slot.
+constexpr int kF8Panels = 4;                                  // 128-column panels of c_kv
+constexpr int kF8NopeGroupBytes = kF8Panels * 8 * 128;        // 4096: row-group stride
+constexpr int kF8NopeBytes = kTile / 8 * kF8NopeGroupBytes;   // 48 KB
+constexpr int kF8RopeGroupBytes = 8 * 64;                     // 512
+constexpr int kF8RopeBytes = kTile / 8 * kF8RopeGroupBytes;   // 6 KB
+constexpr int kF8StageBytes = kF8NopeBytes + kF8RopeBytes;    // 54 KB
+constexpr int kF8NumStages = 4;                               // score CTA: KV tiles in flight
+// Per-row scales of the FP8 Q split (Q = 2^k_row (hi + lo)): a ring of
+// kF8QScaleSlots items, 128 fp32 each, written by the Q loaders.
+constexpr int kF8QScaleSlots = 4;
+constexpr int kF8ScoreDataBytes = kF8NumStages * kF8StageBytes + kF8QScaleSlots * kMaxHeads * 4;
+static_assert(kF8NopeBytes == 48 * 1024, "an FP8 V tile fills one V slot");
+// Q in tensor memory for the FP8 path: hi codes in columns [0, 144), lo
+// codes in [144, 288), four E4M3 values per 32-bit column.
+constexpr int kF8QLoCol = kD / 4;        // 144
+
 constexpr int kThreads = 384;            // 12 warps per CTA
 constexpr int kTmemCols = 512;
 // Score CTA TMEM columns: Q (576 bf16 packed in pairs) then two S buffers.
@@ -62,7 +83,8 @@ constexpr int kCtrlBytes = 1024;
 constexpr int kScoreDataBytes = kNumStages * kStageBytes;                            // 216 KB
 constexpr int kOutDataBytes =
     kNumVSlots * kVHalfBytes + kNumPBufs * kPBytes + kNumRecSlots * kRecBytes;      // 200 KB
-constexpr int kDataBytes = kScoreDataBytes > kOutDataBytes ? kScoreDataBytes : kOutDataBytes;
+constexpr int kDataBytes0 = kScoreDataBytes > kOutDataBytes ? kScoreDataBytes : kOutDataBytes;
+constexpr int kDataBytes = kDataBytes0 > kF8ScoreDataBytes ? kDataBytes0 : kF8ScoreDataBytes;
 constexpr int kSmemBytes = kCtrlBytes + kDataBytes + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -89,12 +111,17 @@ struct CombineItem {
 };
 
 struct DecodeParams {
-  // 4-D views of the cache {64 columns, 8 rows, 9 panels, row groups of 8}
+  // bf16 cache: 4-D views {64 columns, 8 rows, 9 panels, row groups of 8}
   // (strides: row 1152 B, panel 128 B, row group 9216 B). One box brings a
   // page-aligned run of 16 or 32 rows (2 or 4 row groups) across several
   // 64-column panels and lands in shared memory as [row group][panel][8 rows]
   // [128 B] with the 128-byte swizzle: every 8-row x 128-byte atom of a tile
   // sits at (row group * panels + panel) * 1 KB, whichever page it came from.
+  // FP8 cache: tmap_k16/k32 view columns 0..511 as {128 columns, 8 rows,
+  // 4 panels, row groups} (strides 576, 128, 4608 B; boxes {128, 8, 4, 2|4},
+  // 128-byte swizzle), used for K by the score CTA and for V by the output
+  // CTA; tmap_v16/v32 view columns 512..575 as {64 columns, 8 rows, row
+  // groups} (strides 576, 4608 B; boxes {64, 8, 2|4}, 64-byte swizzle).
   CUtensorMap tmap_k16;           // box {64, 8, 9, 2}: all 576 columns
   CUtensorMap tmap_k32;           // box {64, 8, 9, 4} (block_size >= 32)
   CUtensorMap tmap_v16;           // box {64, 8, 4, 2}: one 256-column half of V
@@ -119,6 +146,8 @@ struct DecodeParams {
   int64_t num_blocks;
   float scale_log2;               // sm_scale * log2(e)
   int dynamic_lens;               // 1: planned lengths are upper bounds; items end at the device length
+  int kv_fp8;                     // 1: the cache holds E4M3 bytes [num_blocks, bs, 576]
+  float kv_scale;                 // FP8 cache: element value = kv_scale * e4m3(byte)
 };
 
 struct CombineParams {

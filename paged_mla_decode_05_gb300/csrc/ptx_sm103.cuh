@@ -128,6 +128,14 @@ MLA_DEVI void tma_load_4d(uint32_t dst, const void* tmap, int x, int y, int z, i
       " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy) : "memory");
 }
+// 3-D tiled TMA load, same conventions.
+MLA_DEVI void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar,
+                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy) : "memory");
+}
 MLA_DEVI uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -181,6 +189,21 @@ MLA_DEVI void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t
                      uint32_t accumulate) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// The same two forms with kind::f8f6f4 (8-bit A and B, fp32 accumulator);
+// the operand formats come from the instruction descriptor.
+MLA_DEVI void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                        uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+               :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+MLA_DEVI void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                        uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
                :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
@@ -241,15 +264,26 @@ MLA_DEVI void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+MLA_DEVI void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                  "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 // Shared-memory matrix descriptor of a tcgen05 operand: start address,
 // leading and stride byte offsets (16-byte units), fixed version bit 46 and
 // the swizzle mode in bits 61-63 (2 = 128-byte swizzle).
-MLA_DEVI uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+constexpr uint32_t kLayoutSw128 = 2;   // 128-byte swizzle
+constexpr uint32_t kLayoutSw64 = 4;    // 64-byte swizzle
+MLA_DEVI uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                            uint32_t layout = kLayoutSw128) {
   uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
   d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(layout) << 61;
   return d;
 }
 
@@ -261,6 +295,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
          (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0
+// in bits 7-9 and 10-12) and an fp32 accumulator; other fields as above.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn_major,
+                                                      int b_mn_major) {
+  return (1u << 4) | (static_cast<uint32_t>(a_mn_major) << 15) |
+         (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Two fp32 values to E4M3 (round to nearest even, saturating to +-448):
+// `lo` in bits 0-7, `hi` in bits 8-15.
+MLA_DEVI uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // fp32 exp2 on the special function unit (relative error about 2^-22).
@@ -295,6 +346,41 @@ MLA_DEVI uint64_t add_f32x2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+MLA_DEVI uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+MLA_DEVI uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Two-term E4M3 representation of a pair of fp32 values x (|x| <= 448):
+// x ~ hi + lo. hi keeps the leading 4 significant bits of x, rounded half
+// away from zero by an integer add on the fp32 bit pattern (the carry may
+// move the exponent, which is the correct rounding); lo = x - hi is exact in
+// fp32 and |lo| is at most half a unit of hi's last bit. (Integer rounding,
+// not Dekker's fp32 splitting: a compiler that contracts that multiply and
+// subtract into one fma makes hi = x.) Where hi lies in E4M3's normal range
+// (|hi| >= 2^-6) it converts exactly, and hi + lo carries about 8
+// significant bits of x (relative error at most 2^-8 when lo is normal too;
+// exact for a bf16 x). Returns the two codes of hi in bits 0-15 and those of
+// lo in bits 16-31, element 0 of the pair in the low byte of each.
+MLA_DEVI float round_4_significant_bits(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x00080000u) & 0xFFF00000u);
+}
+MLA_DEVI uint32_t split_e4m3x2(uint64_t x2) {
+  float x0, x1;
+  unpack_f32x2(x2, x0, x1);
+  const float h0 = round_4_significant_bits(x0);
+  const float h1 = round_4_significant_bits(x1);
+  float l0, l1;
+  unpack_f32x2(sub_f32x2(x2, pack_f32x2(h0, h1)), l0, l1);
+  return cvt_e4m3x2(h0, h1) | (cvt_e4m3x2(l0, l1) << 16);
+}
+
 // Three-input fp32 maximum (sm_100+).
 MLA_DEVI float max3f(float a, float b, float c) {
   float d;

@@ -3,8 +3,10 @@ with the oracle under the parity tolerance.
 
 Tolerance (fixed for this method): |out - ref| <= 2e-2 + 2e-2 |ref| per
 element, |lse - ref| <= 5e-3, every value finite. The kernels round P to bf16
-before P.V and round out to bf16 (relative 2^-9), which the bound covers with
-room to spare.
+(FP8 cache: two E4M3 terms, about as fine) before P.V and round out to bf16
+(relative 2^-9), which the bound covers with room to spare. The FP8 oracle
+reads the same E4M3 bytes exactly, so the cache's own quantisation is not
+part of the error.
 """
 import numpy as np
 
@@ -22,13 +24,35 @@ def to_device(w):
     def bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
-    return {
+    t = {
         "q_nope": bf16(w["q_nope"]),
         "q_pe": bf16(w["q_pe"]),
-        "kv_cache": bf16(w["kv_cache"]),
         "block_table": torch.from_numpy(np.ascontiguousarray(w["block_table"])).to(dev),
         "seq_lens": torch.from_numpy(np.ascontiguousarray(w["seq_lens"])).to(dev),
     }
+    if "kv_fp8" in w:   # FP8 workload (mla_workloads.to_fp8): E4M3 bytes
+        t["kv_fp8"] = torch.from_numpy(np.ascontiguousarray(w["kv_fp8"])).to(dev)
+    else:
+        t["kv_cache"] = bf16(w["kv_cache"])
+    return t
+
+
+def decode_into(m, plan, w, t, qn, qp, out, lse, ws):
+    """mla_decode, or mla_decode_fp8 for an FP8 workload."""
+    if "kv_fp8" in w:
+        m.mla_decode_fp8(plan, qn, qp, t["kv_fp8"], float(w["kv_scale"]), t["block_table"],
+                         t["seq_lens"], float(w["sm_scale"]), out, lse, ws)
+    else:
+        m.mla_decode(plan, qn, qp, t["kv_cache"], t["block_table"], t["seq_lens"],
+                     float(w["sm_scale"]), out, lse, ws)
+
+
+def oracle_ref(oracle_mod, w):
+    """The oracle's (out, lse) for a bf16 or an FP8 workload."""
+    if "kv_fp8" in w:
+        return oracle_mod.mla_decode_fp8(w["q_nope"], w["q_pe"], w["kv_fp8"], w["kv_scale"],
+                                         w["block_table"], w["seq_lens"], w["sm_scale"])
+    return oracle_mod.mla_decode(*oracle_args(w))
 
 
 def run_library(w, force_splits=0, num_clusters=0, dev_tensors=None, check_errors=True):
@@ -44,8 +68,7 @@ def run_library(w, force_splits=0, num_clusters=0, dev_tensors=None, check_error
     ws = None
     if plan.workspace_bytes:
         ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
-    m.mla_decode(plan, t["q_nope"], t["q_pe"], t["kv_cache"], t["block_table"], t["seq_lens"],
-                 float(w["sm_scale"]), out, lse, ws)
+    decode_into(m, plan, w, t, t["q_nope"], t["q_pe"], out, lse, ws)
     bits = m.mla_check_device_error(plan)
     if check_errors:
         assert bits == 0, f"device error bits {bits}"
