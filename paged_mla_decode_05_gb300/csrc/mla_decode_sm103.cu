@@ -61,14 +61,20 @@ struct Ctrl {
   uint64_t v_full[kNumVSlots];    // output: V half landed
   uint64_t v_empty[kNumVSlots];   // output: P.V done reading the V half
   uint64_t p_full[kNumPBufs];     // output: P tile and row record landed (copy bytes)
-  // output: O rescaled for a non-first tile of an item. 128 arrivals (the
-  // four correction warps, which run independently) per phase; a warp can be
-  // up to kNumPBufs - 1 such tiles ahead of another (it needs P of its tile,
-  // shipped after P.V of the tile kNumPBufs earlier), so the ring has
+  // output: the correction warps have taken tile g (and rescaled O if due).
+  // 128 arrivals (the four correction warps, which run independently) per
+  // phase, one phase per tile; a warp can be up to kNumPBufs - 1 tiles ahead
+  // of another (it needs P of its tile, shipped after P.V of the tile
+  // kNumPBufs earlier, which waited for every warp), so the ring has
   // kNumPBufs barriers and an early arrival never lands in a phase that a
   // slower warp has not completed.
   uint64_t o_ready[kNumPBufs];
-  uint64_t o_done[2];             // output: P.V of tile g complete (alternating)
+  // output: P.V of tile g complete, ring of kNumPBufs. A waiter for tile t
+  // always knows that P.V of tile t - kNumPBufs is complete (the correction
+  // warps hold P of tile t + 1, or of t itself in the epilogue, which the
+  // peer shipped after that P.V), and P.V of tile t + kNumPBufs cannot be
+  // (it waits for them), so o_done[t % kNumPBufs] is in tile t's phase.
+  uint64_t o_done[kNumPBufs];
   uint64_t o_drained[2];          // output: epilogue has read O columns [256h, 256h+256) of an item
   uint64_t qs_ready[kF8QScaleSlots];  // score (FP8): the Q row scales of an item are in their slot
   uint32_t tmem_base;
@@ -910,12 +916,14 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
       // P of this tile arrived through the peer's remote stores, counted on
       // p_full[k]: this thread acquires that phase itself (cluster scope)
       // for every tile, so the stores are visible to it before the proxy
-      // fence below. A non-first tile also waits for the correction warps.
+      // fence below. Every tile also waits for all correction warps to have
+      // taken it (o_ready; on an item's first tile there is nothing to
+      // rescale, but the wait keeps every correction warp within the P ring:
+      // P of tile g + kNumPBufs, the next phase of p_full[k], can then not
+      // arrive before each of them has seen this phase).
       if (!mbar_wait_cluster(smem_addr(&c->p_full[k]), (g / kNumPBufs) & 1)) { ok = false; break; }
-      if (i > 0) {
-        if (!mbar_wait(smem_addr(&c->o_ready[r % kNumPBufs]), (r / kNumPBufs) & 1)) { ok = false; break; }
-        ++r;
-      }
+      if (!mbar_wait(smem_addr(&c->o_ready[r % kNumPBufs]), (r / kNumPBufs) & 1)) { ok = false; break; }
+      ++r;
       MLA_TRACE_AT(10, g);
       tc_after_sync();
       // P arrived through remote stores (generic proxy); make them visible to
@@ -976,7 +984,7 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
         tc_commit(smem_addr(&c->v_empty[v]));
       }
       if (!ok) break;
-      tc_commit(smem_addr(&c->o_done[g & 1]));
+      tc_commit(smem_addr(&c->o_done[g % kNumPBufs]));
       tc_commit_multicast(smem_addr(&c->p_empty[k]), static_cast<uint16_t>(0x1));
       MLA_TRACE_AT(13, g);
     }
@@ -1063,40 +1071,37 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
       // The record of tile g stays in its slot until tile g + kNumRecSlots,
       // which the peer ships after P.V of tile g + kNumRecSlots - kNumPBufs
       // (at least g + 1) has completed. That P.V waited for these warps to
-      // pass its tile (o_ready) or, for an item's first tile, for the
-      // previous item's epilogue, which follows all its tiles: either way
-      // after this read of tile g.
+      // pass its tile (o_ready), after this read of tile g.
       const float4 rec = reinterpret_cast<const float4*>(recs + (g % kNumRecSlots) * kRecBytes)[row];
       const float alpha = active ? rec.x : 1.0f;
       const float lv = rec.y;
       const float mv = rec.z;
-      if (i > 0) {
-        if (__any_sync(kFullMask, alpha != 1.0f)) {
-          if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
-            ok = false;
-            break;
-          }
-          tc_after_sync();
-          // tcgen05.st reads its source registers asynchronously: each store
-          // completes (wait::st) before the next load may reuse them.
-#pragma unroll 1
-          for (int cc = 0; cc < kDc / 32; ++cc) {
-            uint32_t rr[32];
-            tmem_ld32(trow + cc * 32, rr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) reg_fence8(&rr[j]);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
-            tmem_st32(trow + cc * 32, rr);
-            tmem_wait_st();
-          }
+      // A non-first tile rescales O when the softmax maximum moved.
+      if (i > 0 && __any_sync(kFullMask, alpha != 1.0f)) {
+        if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) % kNumPBufs]), ((g - 1) / kNumPBufs) & 1))) {
+          ok = false;
+          break;
         }
-        tc_before_sync();
-        mbar_arrive(smem_addr(&c->o_ready[r % kNumPBufs]));
-        ++r;
+        tc_after_sync();
+        // tcgen05.st reads its source registers asynchronously: each store
+        // completes (wait::st) before the next load may reuse them.
+#pragma unroll 1
+        for (int cc = 0; cc < kDc / 32; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(trow + cc * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) reg_fence8(&rr[j]);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+          tmem_st32(trow + cc * 32, rr);
+          tmem_wait_st();
+        }
       }
-      // The next phase of this buffer is P of tile g + 2.
+      tc_before_sync();
+      mbar_arrive(smem_addr(&c->o_ready[r % kNumPBufs]));
+      ++r;
+      // The next phase of this buffer is P of tile g + kNumPBufs.
       if (elected && g + kNumPBufs < total)
         mbar_arrive_expect_tx(smem_addr(&c->p_full[k]), kPMsgBytes);
       if (row == 0) MLA_TRACE_AT(15, g);
@@ -1109,7 +1114,7 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
     // Epilogue: O / l -> out (bf16) or the split partial (fp32), one
     // 256-column half at a time; each half is released to the next item's
     // first P.V as soon as it has been read.
-    if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1))) {
+    if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->o_done[(g - 1) % kNumPBufs]), ((g - 1) / kNumPBufs) & 1))) {
       ok = false;
       break;
     }
@@ -1163,11 +1168,13 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->kv_full[s]), 1);
       mbar_init(smem_addr(&c->kv_empty[s]), 1);
     }
-    for (int j = 0; j < kNumPBufs; ++j) mbar_init(smem_addr(&c->o_ready[j]), 128);
+    for (int j = 0; j < kNumPBufs; ++j) {
+      mbar_init(smem_addr(&c->o_ready[j]), 128);
+      mbar_init(smem_addr(&c->o_done[j]), 1);
+    }
     for (int j = 0; j < 2; ++j) {
       mbar_init(smem_addr(&c->s_full[j]), 1);
       mbar_init(smem_addr(&c->s_free[j]), 128);
-      mbar_init(smem_addr(&c->o_done[j]), 1);
       mbar_init(smem_addr(&c->o_drained[j]), 128);
     }
     for (int j = 0; j < kNumPanels; ++j) mbar_init(smem_addr(&c->q_ready[j]), 4);

@@ -32,11 +32,8 @@ constexpr int kKGroupBytes = kNumPanels * kAtomBytes;    // 9216: row-group stri
 constexpr int kVGroupBytes = kVHalfPanels * kAtomBytes;  // 4096: row-group stride of a V slot
 constexpr int kNumStages = 2;            // score CTA: KV tiles in flight
 constexpr int kNumVSlots = 3;            // output CTA: V half-tiles in flight
-// P tiles in flight (output CTA buffers). Three would let the correction
-// warps run three tiles ahead of the P.V completions, which measured faster
-// on B=512 but gave nondeterministic wrong outputs on the peaky long-context
-// workload (cause not found), so the design stays at two.
-constexpr int kNumPBufs = 2;
+// P tiles in flight (output CTA buffers).
+constexpr int kNumPBufs = 3;
 // P [128 rows x 96 tokens] bf16 in the no-swizzle K-major layout of 8-row x
 // 16-byte core matrices: [row/8][token/8][row%8][16 B]; K-adjacent cores are
 // 128 B apart, row groups 1536 B apart. The score CTA's softmax threads write
