@@ -482,13 +482,19 @@ def bench_reference(args, world, rank, local):
     seq = np.asarray(w["seq_lens"], dtype=np.int64)
     rng = np.random.default_rng(7)
     total_steps = args.warmup + args.steps
-    # Pilot: a few requests, to size the steps.
+    # Pilot: a few requests, to size the steps; when that puts one whole call
+    # under 20 s, one whole call times it directly (a small sample runs below
+    # the oracle's full parallel rate and overestimates it).
     pilot = sample_requests(rng, seq, max(1, cores // max(1, H // 16)))
     t0 = time.perf_counter()
     oracle_call(oracle, w, pilot)
     pilot_s = time.perf_counter() - t0
     full_est_s = pilot_s / max(seq[pilot].sum() / max(seq.sum(), 1), 1e-12)
-    budget_s = 240.0
+    if full_est_s < 20.0:
+        t0 = time.perf_counter()
+        oracle_call(oracle, w)
+        full_est_s = time.perf_counter() - t0
+    budget_s = 300.0
     full = total_steps * full_est_s <= budget_s
     times = []
     if full:

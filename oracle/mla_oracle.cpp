@@ -96,13 +96,19 @@ struct Inputs {
   double kv_scale = 1.0;             // value = kv_scale * e4m3(byte)
 };
 
-// One gathered cache row; at(d) is the value of column d as a double.
+// One gathered cache row (bf16 or FP8). values(dst, n) writes the values of
+// its first n columns as doubles: the element type is decided once per row.
 struct Row {
   const uint16_t* b16 = nullptr;
   const uint8_t* f8 = nullptr;
   double scale = 1.0;
   bool valid() const { return b16 != nullptr || f8 != nullptr; }
-  double at(int d) const { return f8 != nullptr ? scale * e4m3_to_double(f8[d]) : bf16_to_double(b16[d]); }
+  void values(double* dst, int n) const {
+    if (f8 != nullptr)
+      for (int d = 0; d < n; ++d) dst[d] = scale * e4m3_to_double(f8[d]);
+    else
+      for (int d = 0; d < n; ++d) dst[d] = bf16_to_double(b16[d]);
+  }
 };
 
 // Step 1: cached row t of request b (invalid for a block id out of range).
@@ -126,9 +132,11 @@ Row gather_row(const Inputs& in, int b, int64_t t) {
 double score(const Inputs& in, int b, int h, const Row& row) {
   const uint16_t* qn = in.q_nope + (static_cast<int64_t>(b) * in.H + h) * kDc;
   const uint16_t* qp = in.q_pe + (static_cast<int64_t>(b) * in.H + h) * kDr;
+  double k[kD];
+  row.values(k, kD);
   double acc = 0.0;
-  for (int d = 0; d < kDc; ++d) acc += bf16_to_double(qn[d]) * row.at(d);
-  for (int d = 0; d < kDr; ++d) acc += bf16_to_double(qp[d]) * row.at(kDc + d);
+  for (int d = 0; d < kDc; ++d) acc += bf16_to_double(qn[d]) * k[d];
+  for (int d = 0; d < kDr; ++d) acc += bf16_to_double(qp[d]) * k[kDc + d];
   return in.sm_scale * acc;
 }
 
@@ -156,7 +164,9 @@ int attend_range(const Inputs& in, int b, int h, int64_t t0, int64_t t1,
   for (size_t i = 0; i < s.size(); ++i) {
     const double w = std::exp(s[i] - m);
     z += w;
-    for (int j = 0; j < kDc; ++j) out[j] += w * rows[i].at(j);
+    double v[kDc];
+    rows[i].values(v, kDc);
+    for (int j = 0; j < kDc; ++j) out[j] += w * v[j];
   }
   for (int j = 0; j < kDc; ++j) out[j] /= z;
   *lse = m + std::log(z);
