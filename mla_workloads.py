@@ -117,6 +117,16 @@ WORKLOADS: List[WorkloadSpec] = [
 ]
 WORKLOADS_BY_NAME: Dict[str, WorkloadSpec] = {w.name: w for w in WORKLOADS}
 
+# Sparse (top-k) decode: a long-context R1-shaped batch in which every request
+# attends to 2048 of its tokens (the token selection itself happens upstream).
+SPARSE_TOPK = 2048
+SPARSE_WORKLOADS: Dict[str, WorkloadSpec] = {
+    "sparse_r1_b64_h128": WorkloadSpec(
+        "sparse_r1_b64_h128", B=64, H=128, block_size=64, seed=6,
+        seq_lens=_uniform_lens(64, 8192, 16384), max_len=16384, pool=_pool_125,
+        description="B=64, H=128, L=8192+U{0..8192}, bs=64, top-2048 selection per request"),
+}
+
 
 def custom_spec(name: str, B: int, H: int, block_size: int, seq_lens: Sequence[int],
                 seed: int, spare_blocks: int = 4, peaky_fraction: float = 0.0,
@@ -231,6 +241,36 @@ def to_fp8(w: Dict[str, object], kv_scale: float = FP8_KV_SCALE) -> Dict[str, ob
     out["kv_fp8"] = codes.reshape(w["kv_cache"].shape)
     out["kv_scale"] = float(kv_scale)
     out["name"] = f"{w['name']}_fp8"
+    return out
+
+
+def with_topk(w: Dict[str, object], topk: int, seed: int,
+              mixed_padding: bool = False) -> Dict[str, object]:
+    """Adds ``topk_indices`` (int32 [B, topk]) to a workload: for each request,
+    min(topk, L) distinct token positions drawn uniformly without replacement,
+    in random order, the remaining entries padding (-1 at the end). With
+    ``mixed_padding`` the padding entries are -1 or L + k (k < 7) at random and
+    the whole row is shuffled, so padding sits between selected tokens. Draws
+    come from ``numpy.random.PCG64(seed)``."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = np.asarray(w["seq_lens"], dtype=np.int64)
+    B = lens.shape[0]
+    idx = np.full((B, topk), -1, dtype=np.int32)
+    for b in range(B):
+        L = int(lens[b])
+        n = min(topk, L)
+        row = np.full(topk, -1, dtype=np.int64)
+        if n > 0:
+            row[:n] = rng.choice(L, size=n, replace=False)
+        if mixed_padding:
+            if n < topk:
+                pads = rng.integers(0, 2, size=topk - n)
+                row[n:] = np.where(pads == 0, -1, L + rng.integers(0, 7, size=topk - n))
+            row = row[rng.permutation(topk)]
+        idx[b] = row.astype(np.int32)
+    out = dict(w)
+    out["topk_indices"] = idx
+    out["topk"] = topk
     return out
 
 

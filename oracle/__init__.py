@@ -69,6 +69,9 @@ def _load():
         lib.oracle_mla_decode_fp8.argtypes = [i32, i32, i32, p, p, p, dbl, i64, i32, p, i32, p,
                                               dbl, p, p, i32]
         lib.oracle_e4m3_decode.argtypes = [i64, p, p]
+        lib.oracle_mla_decode_sparse.argtypes = [i32, i32, p, p, p, i64, i32, p, i32, p, p, i32,
+                                                 dbl, p, p, i32]
+        lib.oracle_mla_decode_sparse.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = [i32]
         for fn in (lib.oracle_mla_decode_rows, lib.oracle_mla_decode, lib.oracle_mla_decode_multi,
                    lib.oracle_mla_decode_fp8, lib.oracle_e4m3_decode,
@@ -145,6 +148,24 @@ def mla_decode_multi(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale, n_
     _check(_load().oracle_mla_decode_multi(B, q_len, H, qn, qp, kv, nb, bs, bt, mb, sl, sc,
                                            _ptr(out), _ptr(lse), int(n_threads)),
            "oracle_mla_decode_multi")
+    del keep
+    return out, lse
+
+
+def mla_decode_sparse(q_nope, q_pe, kv_cache, block_table, seq_lens, topk_indices, sm_scale,
+                      n_threads: int = 0):
+    """Sparse decode: request b attends to the tokens topk_indices[b] (int32
+    [B, topk]; entries outside [0, L) are padding). Returns (out, lse) float64."""
+    args, keep = _common(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale)
+    B, H = args[0], args[1]
+    idx = np.ascontiguousarray(topk_indices, dtype=np.int32)
+    assert idx.ndim == 2 and idx.shape[0] == B, idx.shape
+    out = np.empty((B, H, D_C), dtype=np.float64)
+    lse = np.empty((B, H), dtype=np.float64)
+    (_, _, qn, qp, kv, nb, bs, bt, mb, sl, sc) = args
+    _check(_load().oracle_mla_decode_sparse(B, H, qn, qp, kv, nb, bs, bt, mb, sl, _ptr(idx),
+                                            idx.shape[1], sc, _ptr(out), _ptr(lse),
+                                            int(n_threads)), "oracle_mla_decode_sparse")
     del keep
     return out, lse
 

@@ -140,25 +140,25 @@ double score(const Inputs& in, int b, int h, const Row& row) {
   return in.sm_scale * acc;
 }
 
-// Steps 1-4 over the token range [t0, t1) of request b for head h. Writes the
-// normalised output (out[512]) and the range's log-sum-exp. An empty range
-// gives zeros and -inf.
-int attend_range(const Inputs& in, int b, int h, int64_t t0, int64_t t1,
-                 double* out, double* lse) {
+// Steps 1-4 over the listed tokens of request b for head h (each entry
+// attended once, in any order). Writes the normalised output (out[512]) and
+// the log-sum-exp of the list. An empty list gives zeros and -inf.
+int attend_tokens(const Inputs& in, int b, int h, const std::vector<int64_t>& tokens,
+                  double* out, double* lse) {
   for (int j = 0; j < kDc; ++j) out[j] = 0.0;
-  if (t1 <= t0) {
+  if (tokens.empty()) {
     *lse = -std::numeric_limits<double>::infinity();
     return ORACLE_OK;
   }
-  std::vector<double> s(static_cast<size_t>(t1 - t0));
-  std::vector<Row> rows(static_cast<size_t>(t1 - t0));
+  std::vector<double> s(tokens.size());
+  std::vector<Row> rows(tokens.size());
   double m = -std::numeric_limits<double>::infinity();
-  for (int64_t t = t0; t < t1; ++t) {
-    const Row row = gather_row(in, b, t);
+  for (size_t i = 0; i < tokens.size(); ++i) {
+    const Row row = gather_row(in, b, tokens[i]);
     if (!row.valid()) return ORACLE_ERR_BAD_BLOCK;
-    rows[t - t0] = row;
-    s[t - t0] = score(in, b, h, row);
-    if (s[t - t0] > m) m = s[t - t0];
+    rows[i] = row;
+    s[i] = score(in, b, h, row);
+    if (s[i] > m) m = s[i];
   }
   double z = 0.0;
   for (size_t i = 0; i < s.size(); ++i) {
@@ -171,6 +171,14 @@ int attend_range(const Inputs& in, int b, int h, int64_t t0, int64_t t1,
   for (int j = 0; j < kDc; ++j) out[j] /= z;
   *lse = m + std::log(z);
   return ORACLE_OK;
+}
+
+// The same over the token range [t0, t1).
+int attend_range(const Inputs& in, int b, int h, int64_t t0, int64_t t1,
+                 double* out, double* lse) {
+  std::vector<int64_t> tokens;
+  for (int64_t t = t0; t < t1; ++t) tokens.push_back(t);
+  return attend_tokens(in, b, h, tokens, out, lse);
 }
 
 bool valid_shape(const Inputs& in) {
@@ -310,6 +318,43 @@ int oracle_mla_decode_fp8(int B, int q_len, int H, const uint16_t* q_nope, const
   Inputs in{B, q_len * H, q_nope, q_pe, nullptr, num_blocks, block_size,
             block_table, max_blocks, seq_lens, sm_scale, kv_fp8, kv_scale};
   return decode_causal(in, q_len, out, lse, n_threads);
+}
+
+// Sparse decode (top-k token selection): request b attends only to the
+// tokens listed in topk_indices[b][0..topk), logical positions in its
+// sequence shared by all its heads; an entry outside [0, L) is padding and is
+// skipped, and an entry listed twice is attended twice. q, out and lse are
+// shaped as in oracle_mla_decode. The pages name a sparse MLA backend only;
+// the list form, the padding rule and the shared selection are the readings
+// taken there.
+int oracle_mla_decode_sparse(int B, int H, const uint16_t* q_nope, const uint16_t* q_pe,
+                             const uint16_t* kv_cache, int64_t num_blocks, int block_size,
+                             const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                             const int32_t* topk_indices, int topk, double sm_scale, double* out,
+                             double* lse, int n_threads) {
+  if (B < 0 || H < 1 || topk < 0 || (topk > 0 && topk_indices == nullptr)) return ORACLE_ERR_ARG;
+  Inputs in{B, H, q_nope, q_pe, kv_cache, num_blocks, block_size,
+            block_table, max_blocks, seq_lens, sm_scale};
+  if (!valid_shape(in)) return ORACLE_ERR_ARG;
+  set_threads(n_threads);
+  const int64_t n = static_cast<int64_t>(B) * H;
+  int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n; ++r) {
+    const int b = static_cast<int>(r / H);
+    const int h = static_cast<int>(r % H);
+    std::vector<int64_t> tokens;
+    for (int i = 0; i < topk; ++i) {
+      const int64_t t = topk_indices[static_cast<int64_t>(b) * topk + i];
+      if (t >= 0 && t < seq_lens[b]) tokens.push_back(t);
+    }
+    const int rc = attend_tokens(in, b, h, tokens, out + r * kDc, lse + r);
+    if (rc != ORACLE_OK) {
+#pragma omp critical
+      status = rc;
+    }
+  }
+  return status;
 }
 
 // E4M3 bytes -> doubles, element by element (NaN for the two NaN codes).
