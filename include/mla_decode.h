@@ -200,6 +200,62 @@ mla_status_t mla_decode_fp8(mla_plan_t plan, const void* q_nope, const void* q_p
                             void* out, float* lse, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/*
+ * Sparse (top-k) decode: each request attends only to a selected list of its
+ * tokens, the "FlashInfer sparse MLA" attention backend named by "[Kernel]
+ * [DSV4.1] Fuse MXFP8 wo_b GEMM with sequence-parallel reduce-scatter" (vLLM
+ * PR #57428), serving command. The page names the backend only; the readings
+ * taken: topk_indices[b][i] (i < topk) are logical token positions of
+ * request b, shared by all its query heads; an entry outside [0, L) is
+ * padding and is skipped; an entry listed twice is attended twice; one query
+ * token per request. The token selection itself (the indexer) is upstream.
+ *
+ * mla_sparse_plan — plan for B requests of H query heads with topk entries
+ * each (1 <= topk <= 2^20; opts as for mla_decode_plan_ex, q_len 0 or 1;
+ * lengths_are_bounds is implied). The plan serves any lists and lengths, so
+ * a sparse decode can be captured in a CUDA graph and replayed; it cannot be
+ * passed to mla_plan_update, mla_decode, mla_decode_fp8 or
+ * mla_decode_no_alloc. mla_plan_workspace_bytes includes the compact cache
+ * below (B * ceil(topk / 64) * 64 rows of 1152 bytes).
+ * Errors: as mla_decode_plan_ex.
+ */
+mla_status_t mla_sparse_plan(int B, int H, int topk, const mla_plan_options_t* opts,
+                             mla_plan_t* plan_out);
+
+/*
+ * mla_decode_sparse — one sparse decode step. Gathers, for each request, the
+ * cache rows of its valid entries into a compact cache in the workspace (in
+ * list order), then runs the decode kernels over that cache with each
+ * request's length set to its number of valid entries.
+ *
+ *  q_nope, q_pe, out, lse, sm_scale, stream   as for mla_decode ([B, H, ...])
+ *  kv_cache      device cache [num_blocks, block_size, 576]: bf16 when
+ *                kv_fp8 = 0, E4M3 bytes with per-tensor scale kv_scale when
+ *                kv_fp8 = 1 (as for mla_decode_fp8); 16-byte aligned
+ *  block_size    16, 32, 64 or 128; block_table device int32
+ *                [B, max_blocks]; seq_lens device int32 [B] (the lengths L
+ *                the list entries are checked against)
+ *  topk_indices  device int32 [B, topk]
+ *  workspace     device memory of at least mla_plan_workspace_bytes(plan)
+ *                bytes, 256-byte aligned (always needed: it holds the
+ *                compact cache)
+ *
+ * Asynchronous, two or three kernels on `stream` (gather, decode, and the
+ * combine when the plan splits). A selected token whose block id lies
+ * outside [0, num_blocks) is skipped and raises MLA_DEVERR_BAD_BLOCK.
+ * Costs: the gather reads and writes the selected rows once more than the
+ * decode itself reads them.
+ * Errors: MLA_ERR_INVALID_ARG (also for a plan not made by
+ * mla_sparse_plan), MLA_ERR_UNSUPPORTED_DEVICE, MLA_ERR_WORKSPACE_TOO_SMALL,
+ * MLA_ERR_CUDA.
+ */
+mla_status_t mla_decode_sparse(mla_plan_t plan, const void* q_nope, const void* q_pe,
+                               const void* kv_cache, int kv_fp8, float kv_scale,
+                               int64_t num_blocks, int block_size, const int32_t* block_table,
+                               int max_blocks, const int32_t* seq_lens,
+                               const int32_t* topk_indices, float sm_scale, void* out, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device memory behind mla_decode_no_alloc (32 MiB). */
 #define MLA_NO_ALLOC_SCRATCH_BYTES (((size_t)32) << 20)
 

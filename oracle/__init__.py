@@ -70,7 +70,7 @@ def _load():
                                               dbl, p, p, i32]
         lib.oracle_e4m3_decode.argtypes = [i64, p, p]
         lib.oracle_mla_decode_sparse.argtypes = [i32, i32, p, p, p, i64, i32, p, i32, p, p, i32,
-                                                 dbl, p, p, i32]
+                                                 dbl, p, p, i32, p, dbl]
         lib.oracle_mla_decode_sparse.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = [i32]
         for fn in (lib.oracle_mla_decode_rows, lib.oracle_mla_decode, lib.oracle_mla_decode_multi,
@@ -153,11 +153,19 @@ def mla_decode_multi(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale, n_
 
 
 def mla_decode_sparse(q_nope, q_pe, kv_cache, block_table, seq_lens, topk_indices, sm_scale,
-                      n_threads: int = 0):
+                      n_threads: int = 0, kv_fp8=None, kv_scale: float = 1.0):
     """Sparse decode: request b attends to the tokens topk_indices[b] (int32
-    [B, topk]; entries outside [0, L) are padding). Returns (out, lse) float64."""
+    [B, topk]; entries outside [0, L) are padding). With ``kv_fp8`` (uint8 E4M3
+    bytes, same shape as a cache) the cache is that FP8 one with ``kv_scale``
+    and ``kv_cache`` may be None. Returns (out, lse) float64."""
+    f8 = None
+    if kv_fp8 is not None:
+        f8 = np.ascontiguousarray(kv_fp8, dtype=np.uint8)
+        kv_cache = np.zeros((1, f8.shape[1], D), dtype=np.uint16)   # shape check only
     args, keep = _common(q_nope, q_pe, kv_cache, block_table, seq_lens, sm_scale)
     B, H = args[0], args[1]
+    if f8 is not None:
+        args = args[:5] + (f8.shape[0],) + args[6:]
     idx = np.ascontiguousarray(topk_indices, dtype=np.int32)
     assert idx.ndim == 2 and idx.shape[0] == B, idx.shape
     out = np.empty((B, H, D_C), dtype=np.float64)
@@ -165,7 +173,9 @@ def mla_decode_sparse(q_nope, q_pe, kv_cache, block_table, seq_lens, topk_indice
     (_, _, qn, qp, kv, nb, bs, bt, mb, sl, sc) = args
     _check(_load().oracle_mla_decode_sparse(B, H, qn, qp, kv, nb, bs, bt, mb, sl, _ptr(idx),
                                             idx.shape[1], sc, _ptr(out), _ptr(lse),
-                                            int(n_threads)), "oracle_mla_decode_sparse")
+                                            int(n_threads),
+                                            _ptr(f8) if f8 is not None else None,
+                                            float(kv_scale)), "oracle_mla_decode_sparse")
     del keep
     return out, lse
 

@@ -327,14 +327,17 @@ int oracle_mla_decode_fp8(int B, int q_len, int H, const uint16_t* q_nope, const
 // shaped as in oracle_mla_decode. The pages name a sparse MLA backend only;
 // the list form, the padding rule and the shared selection are the readings
 // taken there.
+// With kv_fp8 non-null the cache is the FP8 one of oracle_mla_decode_fp8
+// (kv_cache is then ignored).
 int oracle_mla_decode_sparse(int B, int H, const uint16_t* q_nope, const uint16_t* q_pe,
                              const uint16_t* kv_cache, int64_t num_blocks, int block_size,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                              const int32_t* topk_indices, int topk, double sm_scale, double* out,
-                             double* lse, int n_threads) {
+                             double* lse, int n_threads, const uint8_t* kv_fp8, double kv_scale) {
   if (B < 0 || H < 1 || topk < 0 || (topk > 0 && topk_indices == nullptr)) return ORACLE_ERR_ARG;
-  Inputs in{B, H, q_nope, q_pe, kv_cache, num_blocks, block_size,
-            block_table, max_blocks, seq_lens, sm_scale};
+  if (kv_fp8 != nullptr && !std::isfinite(kv_scale)) return ORACLE_ERR_ARG;
+  Inputs in{B, H, q_nope, q_pe, kv_fp8 != nullptr ? nullptr : kv_cache, num_blocks, block_size,
+            block_table, max_blocks, seq_lens, sm_scale, kv_fp8, kv_scale};
   if (!valid_shape(in)) return ORACLE_ERR_ARG;
   set_threads(n_threads);
   const int64_t n = static_cast<int64_t>(B) * H;

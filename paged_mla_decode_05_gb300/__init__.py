@@ -9,7 +9,7 @@ library has not been built (``python -m paged_mla_decode_05_gb300.build``)
 that first use raises ImportError. There is no fallback path.
 """
 _EXPORTS = ("MLAError", "Plan", "mla_check_device_error", "mla_decode", "mla_decode_fp8",
-            "mla_decode_no_alloc",
+            "mla_decode_no_alloc", "mla_sparse_plan", "mla_decode_sparse",
             "mla_decode_plan",
             "mla_device_supported", "mla_selftest_wait_timeout", "mla_status_string",
             "header_functions",

@@ -64,6 +64,9 @@ def _load() -> ctypes.CDLL:
         "mla_decode_fp8": (i32, [p, p, p, p, ctypes.c_float, i64, p, p, ctypes.c_float, p, p, p,
                                  sz, p]),
         "mla_decode_no_alloc": (i32, [p, p, p, p, i64, p, p, ctypes.c_float, p, p, p, p]),
+        "mla_sparse_plan": (i32, [i32, i32, i32, ctypes.POINTER(PlanOptions), p]),
+        "mla_decode_sparse": (i32, [p, p, p, p, i32, ctypes.c_float, i64, i32, p, i32, p, p,
+                                    ctypes.c_float, p, p, p, sz, p]),
         "mla_check_device_error": (i32, [p, p, ctypes.POINTER(u32)]),
         "mla_plan_destroy": (None, [p]),
         "mla_status_string": (ctypes.c_char_p, [i32]),
@@ -193,6 +196,63 @@ def mla_decode_plan(B: int, H: int, seq_lens_host, block_size: int, max_blocks: 
                                   max_blocks, ctypes.byref(opts), ctypes.byref(h)),
            "mla_decode_plan")
     return Plan(h.value, B, H, block_size, max_blocks, host_only, int(q_len))
+
+
+def mla_sparse_plan(B: int, H: int, topk: int, num_clusters: int = 0, force_splits: int = 0,
+                    host_only: bool = False) -> Plan:
+    """Plan a sparse (top-k) decode: B requests of H heads, topk list entries
+    each (see mla_sparse_plan in include/mla_decode.h). The plan serves any
+    lists and lengths."""
+    opts = PlanOptions(int(num_clusters), int(force_splits), 1 if host_only else 0, 1, 1)
+    h = ctypes.c_void_p()
+    _check(LIB.mla_sparse_plan(B, H, int(topk), ctypes.byref(opts), ctypes.byref(h)),
+           "mla_sparse_plan")
+    plan = Plan(h.value, B, H, 64, -(-int(topk) // 64), host_only, 1)
+    plan.topk = int(topk)
+    return plan
+
+
+def mla_decode_sparse(plan: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, topk_indices,
+                      sm_scale: float, out, lse, workspace, kv_scale: float = None, stream=None):
+    """Enqueue one sparse decode (see mla_decode_sparse in include/mla_decode.h).
+
+    kv_cache: bf16 [num_blocks, block_size, 576], or uint8 / float8_e4m3fn
+    E4M3 bytes with ``kv_scale``; block_table int32 [B, max_blocks]; seq_lens
+    int32 [B]; topk_indices int32 [B, topk]; workspace a CUDA uint8 tensor of
+    at least plan.workspace_bytes bytes."""
+    import torch
+    topk = getattr(plan, "topk", None)
+    if topk is None:
+        raise ValueError("plan was not made by mla_sparse_plan")
+    B, H = plan.B, plan.H
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is not None and kv_cache.dtype == f8:
+        kv_cache = kv_cache.view(torch.uint8)
+    fp8 = kv_cache.dtype == torch.uint8
+    if fp8 != (kv_scale is not None):
+        raise ValueError("an FP8 cache needs kv_scale; a bf16 cache takes none")
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != D:
+        raise ValueError(f"kv_cache must have shape [num_blocks, block_size, {D}]")
+    nb, bs = int(kv_cache.shape[0]), int(kv_cache.shape[1])
+    kv = _tensor(kv_cache, torch.uint8 if fp8 else torch.bfloat16, (nb, bs, D), "kv_cache")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError(f"block_table must have shape [{B}, max_blocks]")
+    mb = int(block_table.shape[1])
+    bt = _tensor(block_table, torch.int32, (B, mb), "block_table")
+    sl = _tensor(seq_lens, torch.int32, (B,), "seq_lens")
+    ti = _tensor(topk_indices, torch.int32, (B, topk), "topk_indices")
+    qn = _tensor(q_nope, torch.bfloat16, (B, H, D_C), "q_nope")
+    qp = _tensor(q_pe, torch.bfloat16, (B, H, D_R), "q_pe")
+    o = _tensor(out, torch.bfloat16, (B, H, D_C), "out")
+    l = _tensor(lse, torch.float32, (B, H), "lse")
+    if workspace is None or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(LIB.mla_decode_sparse(plan.handle, qn, qp, kv, 1 if fp8 else 0,
+                                 ctypes.c_float(kv_scale if fp8 else 1.0), nb, bs, bt, mb, sl, ti,
+                                 ctypes.c_float(sm_scale), o, l,
+                                 ctypes.c_void_p(workspace.data_ptr()), ws_bytes,
+                                 _stream_ptr(stream)), "mla_decode_sparse")
 
 
 def _stream_ptr(stream) -> ctypes.c_void_p:

@@ -66,6 +66,12 @@ struct mla_plan_s {
   const void* tmap_ptr = nullptr;
   int64_t tmap_blocks = -1;
   int tmap_fp8 = -1;
+  // Sparse plans (mla_sparse_plan): the schedule is that of a compact cache of
+  // max_blocks blocks of kSparseBlock rows per request with lengths bounded by
+  // sparse_topk; the workspace holds the decode's partials, then at
+  // sparse_off the compact lengths, block table and cache.
+  int sparse_topk = 0;
+  size_t sparse_off = 0;
 };
 
 namespace {
@@ -639,7 +645,7 @@ mla_status_t mla_decode_plan(int B, int H, const int32_t* seq_lens_host, int blo
 }
 
 mla_status_t mla_plan_update(mla_plan_t p, const int32_t* seq_lens_host, void* stream) {
-  if (!p) return MLA_ERR_INVALID_ARG;
+  if (!p || p->sparse_topk > 0) return MLA_ERR_INVALID_ARG;
   mla_status_t st =
       check_plan_args(p->B, p->heads, seq_lens_host, p->block_size, p->max_blocks, p->q_len);
   if (st != MLA_OK) return st;
@@ -692,8 +698,9 @@ namespace {
 mla_status_t decode_impl(mla_plan_t p, const void* q_nope, const void* q_pe, const void* kv_cache,
                          bool fp8, float kv_scale, int64_t num_blocks, const int32_t* block_table,
                          const int32_t* seq_lens, float sm_scale, void* out, float* lse,
-                         void* workspace, size_t workspace_bytes, void* stream) {
-  if (!p || p->host_only) return MLA_ERR_INVALID_ARG;
+                         void* workspace, size_t workspace_bytes, void* stream,
+                         bool sparse = false) {
+  if (!p || p->host_only || (p->sparse_topk > 0) != sparse) return MLA_ERR_INVALID_ARG;
   if (fp8 && (!(kv_scale > 0.0f) || !std::isfinite(kv_scale))) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !lse)
     return MLA_ERR_INVALID_ARG;
@@ -703,8 +710,9 @@ mla_status_t decode_impl(mla_plan_t p, const void* q_nope, const void* q_pe, con
   if (num_blocks < 1 || num_blocks * p->block_size + 64 >= (int64_t{1} << 31))
     return MLA_ERR_INVALID_ARG;
   if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
-  if (p->workspace_bytes > 0) {
-    if (!workspace || workspace_bytes < p->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  const size_t ws_need = sparse ? p->sparse_off : p->workspace_bytes;   // the decode's own part
+  if (ws_need > 0) {
+    if (!workspace || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   }
   int dev = -1;
@@ -786,6 +794,82 @@ mla_status_t mla_decode_fp8(mla_plan_t p, const void* q_nope, const void* q_pe,
                      seq_lens, sm_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
+mla_status_t mla_sparse_plan(int B, int H, int topk, const mla_plan_options_t* opts,
+                             mla_plan_t* plan_out) {
+  if (!plan_out) return MLA_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  if (B < 1 || topk < 1 || topk > (1 << 20)) return MLA_ERR_INVALID_ARG;
+  mla_plan_options_t o{};
+  if (opts) o = *opts;
+  if (o.q_len > 1) return MLA_ERR_INVALID_ARG;   // one selection per request: one query token
+  o.lengths_are_bounds = 1;
+  const int max_blocks_c = (topk + mla::kSparseBlock - 1) / mla::kSparseBlock;
+  std::vector<int32_t> bounds(B, topk);
+  mla_status_t st = mla_decode_plan_ex(B, H, bounds.data(), mla::kSparseBlock, max_blocks_c, &o,
+                                       plan_out);
+  if (st != MLA_OK) return st;
+  mla_plan_s* p = *plan_out;
+  p->sparse_topk = topk;
+  const size_t rows = static_cast<size_t>(B) * max_blocks_c * mla::kSparseBlock;
+  p->sparse_off = align_up(p->workspace_bytes, 256);
+  p->workspace_bytes = p->sparse_off + align_up(static_cast<size_t>(B) * 4, 256) +
+                       align_up(static_cast<size_t>(B) * max_blocks_c * 4, 256) +
+                       rows * mla::kD * 2;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_sparse(mla_plan_t p, const void* q_nope, const void* q_pe,
+                               const void* kv_cache, int kv_fp8, float kv_scale,
+                               int64_t num_blocks, int block_size, const int32_t* block_table,
+                               int max_blocks, const int32_t* seq_lens,
+                               const int32_t* topk_indices, float sm_scale, void* out, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (!p || p->host_only || p->sparse_topk <= 0) return MLA_ERR_INVALID_ARG;
+  if (!kv_cache || !block_table || !seq_lens || !topk_indices) return MLA_ERR_INVALID_ARG;
+  if (kv_fp8 != 0 && kv_fp8 != 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned(kv_cache, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(topk_indices, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
+    return MLA_ERR_INVALID_ARG;
+  if (max_blocks < 1 || num_blocks < 1 || num_blocks * block_size >= (int64_t{1} << 40))
+    return MLA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < p->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_UNSUPPORTED_DEVICE;
+  if (dev != p->device) return MLA_ERR_INVALID_ARG;
+  mla_status_t st = prepare_device(dev, nullptr);
+  if (st != MLA_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* lens_c = reinterpret_cast<int32_t*>(ws + p->sparse_off);
+  int32_t* table_c = reinterpret_cast<int32_t*>(ws + p->sparse_off + align_up(p->B * 4, 256));
+  uint8_t* cache_c = ws + p->sparse_off + align_up(p->B * 4, 256) +
+                     align_up(static_cast<size_t>(p->B) * p->max_blocks * 4, 256);
+  mla::SparseGatherParams gp;
+  gp.kv_cache = kv_cache;
+  gp.num_blocks = num_blocks;
+  gp.block_size = block_size;
+  gp.max_blocks = max_blocks;
+  gp.block_table = block_table;
+  gp.seq_lens = seq_lens;
+  gp.topk_indices = topk_indices;
+  gp.topk = p->sparse_topk;
+  gp.row_bytes = kv_fp8 ? mla::kD : mla::kD * 2;
+  gp.compact = cache_c;
+  gp.rows_per_request = p->max_blocks * mla::kSparseBlock;
+  gp.compact_lens = lens_c;
+  gp.compact_table = table_c;
+  gp.max_blocks_c = p->max_blocks;
+  gp.err = reinterpret_cast<uint32_t*>(p->d_buf);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mla::launch_sparse_gather(gp, p->B, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return decode_impl(p, q_nope, q_pe, cache_c, kv_fp8 != 0, kv_scale,
+                     static_cast<int64_t>(p->B) * p->max_blocks, table_c, lens_c, sm_scale, out,
+                     lse, workspace, p->sparse_off, stream, true);
+}
+
 // The allocation-free variant: the workspace and the device copy of the work
 // list are carved from the library's fixed device scratch
 // (mla_no_alloc_sm103.cu) instead of caller or plan memory; the error word is
@@ -796,7 +880,7 @@ mla_status_t mla_decode_no_alloc(mla_plan_t p, const void* q_nope, const void* q
                                  const int32_t* block_table, const int32_t* seq_lens,
                                  float sm_scale, void* out, float* lse, uint32_t* err_bits,
                                  void* stream) {
-  if (!p) return MLA_ERR_INVALID_ARG;
+  if (!p || p->sparse_topk > 0) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !lse || !err_bits)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||

@@ -156,7 +156,31 @@ struct CombineParams {
   int H;
 };
 
+// Sparse (top-k) decode, gather step (mla_sparse_sm103.cu): the valid
+// entries of each request's token list, compacted into a cache of
+// rows_per_request rows per request (row_bytes each), with its lengths and an
+// identity block table for the decode kernel.
+struct SparseGatherParams {
+  const void* kv_cache;           // the caller's cache [num_blocks, block_size, 576]
+  int64_t num_blocks;
+  int block_size;
+  int max_blocks;
+  const int32_t* block_table;     // [B, max_blocks]
+  const int32_t* seq_lens;        // [B]
+  const int32_t* topk_indices;    // [B, topk]
+  int topk;
+  int row_bytes;                  // 1152 (bf16) or 576 (FP8)
+  void* compact;                  // [B, rows_per_request, row_bytes]
+  int rows_per_request;           // max_blocks_c * the compact block size
+  int32_t* compact_lens;          // [B]
+  int32_t* compact_table;         // [B, max_blocks_c]
+  int max_blocks_c;
+  uint32_t* err;
+};
+constexpr int kSparseBlock = 64;  // rows per block of the compact cache
+
 // Launchers (defined in the .cu files).
+cudaError_t launch_sparse_gather(const SparseGatherParams& p, int B, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int num_clusters, cudaStream_t stream);
 // max_slots: the largest n_slots of the combine items (at most 4096).
 cudaError_t launch_combine(const CombineParams& p, int num_items, int max_slots,

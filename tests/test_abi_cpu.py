@@ -181,3 +181,21 @@ def test_multi_token_argument_checks(m):
     with pytest.raises(m.MLAError):      # more than 1024 query rows per request
         m.mla_decode_plan(2, 128, np.array([30, 100]), 32, 10, num_clusters=4, host_only=True,
                           q_len=9)
+
+
+def test_sparse_plan_workspace_and_refusals():
+    import paged_mla_decode_05_gb300 as m
+    B, H, topk = 5, 128, 300
+    plan = m.mla_sparse_plan(B, H, topk, num_clusters=76, host_only=True)
+    rows = B * (-(-topk // 64)) * 64
+    assert plan.workspace_bytes >= rows * 576 * 2 + B * 4
+    # every request is planned for topk entries (the bound), in one head group
+    covered = {}
+    for b, t0, t1, slot, cl in plan.work_items():
+        covered[b] = covered.get(b, 0) + (t1 - t0)
+    assert covered == {b: topk for b in range(B)}
+    with pytest.raises(m.MLAError):
+        plan.update(np.full(B, 10, dtype=np.int32))
+    for bad in (0, -1):
+        with pytest.raises(m.MLAError):
+            m.mla_sparse_plan(B, H, bad, num_clusters=76, host_only=True)

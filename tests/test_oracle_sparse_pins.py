@@ -103,3 +103,19 @@ def test_generator_selects_distinct_tokens():
     for b, L in enumerate(w["seq_lens"]):
         sel = idx[b][(idx[b] >= 0) & (idx[b] < L)]
         assert len(sel) == min(64, int(L)) and len(set(sel.tolist())) == len(sel)
+
+
+def test_fp8_cache_sparse_is_the_fp8_decode_of_the_list(oracle_mod):
+    w8 = wl.to_fp8(_spec([40, 17]))
+    rng = np.random.default_rng(5)
+    idx = np.full((2, 40), -1, dtype=np.int32)
+    for b, L in enumerate(w8["seq_lens"]):
+        idx[b, :L] = rng.permutation(int(L))
+    out, lse = oracle_mod.mla_decode_sparse(w8["q_nope"], w8["q_pe"], None, w8["block_table"],
+                                            w8["seq_lens"], idx, w8["sm_scale"],
+                                            kv_fp8=w8["kv_fp8"], kv_scale=w8["kv_scale"])
+    ref_out, ref_lse = oracle_mod.mla_decode_fp8(w8["q_nope"], w8["q_pe"], w8["kv_fp8"],
+                                                 w8["kv_scale"], w8["block_table"], w8["seq_lens"],
+                                                 w8["sm_scale"])
+    np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
