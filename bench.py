@@ -15,6 +15,10 @@ between steps.
 ``--kv fp8`` runs the same workload over an FP8 (E4M3, per-tensor scale)
 cache through ``mla_decode_fp8`` (576 bytes per cached token).
 
+``--config sparse_r1_b64_h128`` runs the sparse (top-k) decode instead: B=64,
+H=128, lengths 8192 + U{0..8192}, each request attending to 2048 listed tokens
+(``mla_decode_sparse``: gather kernel, then the decode kernel).
+
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
 same workload on the host cores (the slow baseline). Under torchrun (N > 1)
 every rank runs its own replica of the workload (the decode needs no
@@ -181,10 +185,35 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def spec_of(name: str):
+    return wl.SPARSE_WORKLOADS[name] if is_sparse(name) else wl.WORKLOADS_BY_NAME[name]
+
+
+def is_sparse(name: str) -> bool:
+    return name in wl.SPARSE_WORKLOADS
+
+
 def load_workload(name: str, kv: str):
-    """The seeded workload, with its cache converted to E4M3 for kv == "fp8"."""
-    w = wl.generate(wl.WORKLOADS_BY_NAME[name])
+    """The seeded workload, with its cache converted to E4M3 for kv == "fp8";
+    a sparse workload also gets its top-k lists (seeded by the spec's seed)."""
+    spec = spec_of(name)
+    w = wl.generate(spec)
+    if is_sparse(name):
+        w = wl.with_topk(w, wl.SPARSE_TOPK, seed=spec.seed)
     return wl.to_fp8(w) if kv == "fp8" else w
+
+
+def counts_of(w):
+    return wl.sparse_counts(w) if "topk_indices" in w else wl.expected_counts(w)
+
+
+def request_work(w):
+    """Tokens each request attends to: its length, or its valid list entries."""
+    seq = np.asarray(w["seq_lens"], dtype=np.int64)
+    if "topk_indices" not in w:
+        return seq
+    idx = np.asarray(w["topk_indices"], dtype=np.int64)
+    return ((idx >= 0) & (idx < seq[:, None])).sum(axis=1)
 
 
 def cache_of(w):
@@ -195,7 +224,11 @@ def workload_config(spec, w, counts, world):
     """The config block both arms report for a workload (identical keys)."""
     cache_bytes = int(cache_of(w).nbytes)
     fp8 = "kv_fp8" in w
+    sparse = {"topk": int(w["topk_indices"].shape[1]),
+              "selection": "min(topk, L) distinct positions per request, uniform"} \
+        if "topk_indices" in w else {}
     return {"workload": spec.name + ("_fp8" if fp8 else ""), "B": int(w["B"]), "H": int(w["H"]),
+            **sparse,
             "kv_cache": (f"fp8 e4m3, per-tensor scale {w['kv_scale']}" if fp8 else "bf16"),
             "block_size": int(w["block_size"]),
             "seq_lens": "1024+U{0..2048}" if spec.name.startswith("r1_") else spec.description,
@@ -218,12 +251,13 @@ def bench_ours(args, world, rank, local):
     from paged_mla_decode_05_gb300 import build as _b
     _b.build()
 
-    spec = wl.WORKLOADS_BY_NAME[args.config]
+    spec = spec_of(args.config)
     t0 = time.time()
     w = load_workload(args.config, args.kv)
     fp8 = args.kv == "fp8"
+    sparse = is_sparse(args.config)
     log(f"[bench] generated {spec.name} ({args.kv} cache) in {time.time() - t0:.1f}s")
-    counts = wl.expected_counts(w)
+    counts = counts_of(w)
     B, H, bs = w["B"], w["H"], w["block_size"]
 
     def bf16(a):
@@ -233,15 +267,26 @@ def bench_ours(args, world, rank, local):
     kv = torch.from_numpy(w["kv_fp8"]).to(dev) if fp8 else bf16(w["kv_cache"])
     table = torch.from_numpy(w["block_table"]).to(dev)
     lens = torch.from_numpy(w["seq_lens"]).to(dev)
-    plan = m.mla_decode_plan(B, H, w["seq_lens"], bs, int(w["max_blocks"]))
+    if sparse:
+        # The plan depends on B, H and topk only; lists and lengths are read
+        # on the device. A step: gather kernel, decode kernel (+ combine).
+        topk_dev = torch.from_numpy(w["topk_indices"]).to(dev)
+        plan = m.mla_sparse_plan(B, H, int(w["topk_indices"].shape[1]))
+        launches_per_step = 2 + (1 if any(plan.num_splits(b) > 1 for b in range(B)) else 0)
+    else:
+        plan = m.mla_decode_plan(B, H, w["seq_lens"], bs, int(w["max_blocks"]))
     out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H), dtype=torch.float32, device=dev)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
-    launches_per_step = 1 + (1 if plan.workspace_bytes else 0)
+    if not sparse:
+        launches_per_step = 1 + (1 if plan.workspace_bytes else 0)
     stream = torch.cuda.current_stream()
 
     def step():
-        if fp8:
+        if sparse:
+            m.mla_decode_sparse(plan, q_nope, q_pe, kv, table, lens, topk_dev, w["sm_scale"], out,
+                                lse, ws, kv_scale=w["kv_scale"] if fp8 else None, stream=stream)
+        elif fp8:
             m.mla_decode_fp8(plan, q_nope, q_pe, kv, w["kv_scale"], table, lens, w["sm_scale"], out,
                              lse, ws, stream)
         else:
@@ -290,17 +335,24 @@ def bench_ours(args, world, rank, local):
     h_qp = torch.from_numpy(w["q_pe"].view(np.int16)).view(torch.bfloat16).pin_memory()
     h_tab = torch.from_numpy(w["block_table"]).pin_memory()
     h_len = torch.from_numpy(w["seq_lens"]).pin_memory()
+    h_idx = torch.from_numpy(w["topk_indices"]).pin_memory() if sparse else None
     h_out = torch.empty((B, H, 512), dtype=torch.bfloat16).pin_memory()
     h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
     lens_np = w["seq_lens"].copy()
     e_steps = max(3, min(args.steps, 20))
 
-    def e2e_step():
+    def copies_in():
         q_nope.copy_(h_qn, non_blocking=True)
         q_pe.copy_(h_qp, non_blocking=True)
         table.copy_(h_tab, non_blocking=True)
         lens.copy_(h_len, non_blocking=True)
-        plan.update(lens_np, stream)
+        if sparse:
+            topk_dev.copy_(h_idx, non_blocking=True)
+
+    def e2e_step():
+        copies_in()
+        if not sparse:   # a sparse plan serves any lists and lengths
+            plan.update(lens_np, stream)
         step()
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
@@ -329,26 +381,24 @@ def bench_ours(args, world, rank, local):
             stream.synchronize()
         return statistics.median(a.elapsed_time(b) * 1e3 for a, b in ev)
 
-    def copies_in():
-        q_nope.copy_(h_qn, non_blocking=True)
-        q_pe.copy_(h_qp, non_blocking=True)
-        table.copy_(h_tab, non_blocking=True)
-        lens.copy_(h_len, non_blocking=True)
 
     def copies_out():
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
-    t_p = time.perf_counter()
-    for _ in range(5):
-        plan.update(lens_np, stream)
-    stream.synchronize()
-    plan_host_us = (time.perf_counter() - t_p) * 1e6 / 5
+    plan_host_us = 0.0
+    if not sparse:
+        t_p = time.perf_counter()
+        for _ in range(5):
+            plan.update(lens_np, stream)
+        stream.synchronize()
+        plan_host_us = (time.perf_counter() - t_p) * 1e6 / 5
     breakdown = {"h2d_us": round(phase_us(copies_in), 1),
                  "plan_update_host_us": round(plan_host_us, 1),
                  "decode_us": round(phase_us(step), 1),
                  "d2h_us": round(phase_us(copies_out), 1)}
-    h2d = sum(t.numel() * t.element_size() for t in (h_qn, h_qp, h_tab, h_len))
+    h2d = sum(t.numel() * t.element_size()
+              for t in (h_qn, h_qp, h_tab, h_len) + ((h_idx,) if sparse else ()))
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
 
     peaks, peak_kind = load_peaks()
@@ -361,7 +411,8 @@ def bench_ours(args, world, rank, local):
     tf_own = tf * (FP8_OVER_BF16 if fp8 else 1.0)
     t_flops_us = counts["flops"] / (tf_own * 1e12) * 1e6
     # Dominant kernel: the decode kernel. Without a split the step is exactly
-    # that one launch, so the step time is its duration.
+    # that one launch, so the step time is its duration. A sparse step also
+    # runs the gather kernel; its bound is taken over the whole step.
     dominant_us = us if launches_per_step == 1 else None
     hbm_bound = t_bytes_us >= t_flops_us
     achieved = (counts["bytes"] / (ms_per_step * 1e-3) / 1e9 if hbm_bound
@@ -406,6 +457,9 @@ def bench_ours(args, world, rank, local):
             "t_flops_bf16_us": round(t_flops_bf16_us, 2),
             "roofline_fraction": round(max(t_bytes_us, t_flops_bf16_us) / us, 4),
             "dominant_kernel": "mla_decode_kernel",
+            "scope": ("whole step: sparse gather + decode" + (" + combine" if launches_per_step > 2
+                                                               else "")) if sparse else
+                     ("decode kernel" if launches_per_step == 1 else "decode + combine"),
             "dominant_kernel_us": round(dominant_us, 2) if dominant_us else None,
         },
         "step_us_min": round(min(per_step) * 1e3, 2),
@@ -429,6 +483,12 @@ def oracle_call(oracle, w, reqs=None):
     sel = slice(None) if reqs is None else np.asarray(reqs)
     qn, qp = w["q_nope"][sel], w["q_pe"][sel]
     bt, sl = w["block_table"][sel], w["seq_lens"][sel]
+    if "topk_indices" in w:
+        idx = w["topk_indices"][sel]
+        if "kv_fp8" in w:
+            return oracle.mla_decode_sparse(qn, qp, None, bt, sl, idx, w["sm_scale"],
+                                            kv_fp8=w["kv_fp8"], kv_scale=w["kv_scale"])
+        return oracle.mla_decode_sparse(qn, qp, w["kv_cache"], bt, sl, idx, w["sm_scale"])
     if "kv_fp8" in w:
         return oracle.mla_decode_fp8(qn, qp, w["kv_fp8"], w["kv_scale"], bt, sl, w["sm_scale"])
     return oracle.mla_decode(qn, qp, w["kv_cache"], bt, sl, w["sm_scale"])
@@ -448,7 +508,7 @@ def cpu_baseline(w, budget_s: float):
     oracle.build()
     B, H = int(w["B"]), int(w["H"])
     cores = oracle.num_threads(0)
-    seq = np.asarray(w["seq_lens"], dtype=np.int64)
+    seq = request_work(w)
     rng = np.random.default_rng(123)
     reqs = sample_requests(rng, seq, max(1, cores // max(1, H // 16)))
     t0 = time.perf_counter()
@@ -473,13 +533,13 @@ def bench_reference(args, world, rank, local):
         init_dist(world, "gloo")
         if rank != 0:
             return None
-    spec = wl.WORKLOADS_BY_NAME[args.config]
+    spec = spec_of(args.config)
     w = load_workload(args.config, args.kv)
     import oracle
     oracle.build()
     B, H = int(w["B"]), int(w["H"])
     cores = oracle.num_threads(0)
-    seq = np.asarray(w["seq_lens"], dtype=np.int64)
+    seq = request_work(w)
     rng = np.random.default_rng(7)
     total_steps = args.warmup + args.steps
     # Pilot: a few requests, to size the steps; when that puts one whole call
@@ -525,7 +585,7 @@ def bench_reference(args, world, rank, local):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(spec, w, wl.expected_counts(w), world),
+        "config": workload_config(spec, w, counts_of(w), world),
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": int(cores), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -540,7 +600,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.WORKLOADS_BY_NAME))
+    ap.add_argument("--config", default=DEFAULT_CONFIG,
+                    choices=sorted(list(wl.WORKLOADS_BY_NAME) + list(wl.SPARSE_WORKLOADS)))
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="cache element type (fp8: E4M3 with a per-tensor scale)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")

@@ -215,36 +215,36 @@ mla_status_t mla_decode_fp8(mla_plan_t plan, const void* q_nope, const void* q_p
  * lengths_are_bounds is implied). The plan serves any lists and lengths, so
  * a sparse decode can be captured in a CUDA graph and replayed; it cannot be
  * passed to mla_plan_update, mla_decode, mla_decode_fp8 or
- * mla_decode_no_alloc. mla_plan_workspace_bytes includes the compact cache
- * below (B * ceil(topk / 64) * 64 rows of 1152 bytes).
+ * mla_decode_no_alloc. mla_plan_workspace_bytes includes the row lists
+ * below (B * topk int32, plus B counts).
  * Errors: as mla_decode_plan_ex.
  */
 mla_status_t mla_sparse_plan(int B, int H, int topk, const mla_plan_options_t* opts,
                              mla_plan_t* plan_out);
 
 /*
- * mla_decode_sparse — one sparse decode step. Gathers, for each request, the
- * cache rows of its valid entries into a compact cache in the workspace (in
- * list order), then runs the decode kernels over that cache with each
- * request's length set to its number of valid entries.
+ * mla_decode_sparse — one sparse decode step. A small kernel turns each
+ * request's list into the cache rows of its valid entries (in list order)
+ * and their count, in the workspace; the decode kernel then fetches those
+ * rows straight from the paged cache (TMA four-row gathers), each request's
+ * length being its number of valid entries.
  *
  *  q_nope, q_pe, out, lse, sm_scale, stream   as for mla_decode ([B, H, ...])
  *  kv_cache      device cache [num_blocks, block_size, 576]: bf16 when
  *                kv_fp8 = 0, E4M3 bytes with per-tensor scale kv_scale when
  *                kv_fp8 = 1 (as for mla_decode_fp8); 16-byte aligned
- *  block_size    16, 32, 64 or 128; block_table device int32
+ *  block_size    16, 32, 64 or 128; num_blocks * block_size < 2^31 - 64
+ *                (rows are 32-bit TMA coordinates); block_table device int32
  *                [B, max_blocks]; seq_lens device int32 [B] (the lengths L
  *                the list entries are checked against)
  *  topk_indices  device int32 [B, topk]
  *  workspace     device memory of at least mla_plan_workspace_bytes(plan)
  *                bytes, 256-byte aligned (always needed: it holds the
- *                compact cache)
+ *                row lists)
  *
- * Asynchronous, two or three kernels on `stream` (gather, decode, and the
+ * Asynchronous, two or three kernels on `stream` (row lists, decode, and the
  * combine when the plan splits). A selected token whose block id lies
  * outside [0, num_blocks) is skipped and raises MLA_DEVERR_BAD_BLOCK.
- * Costs: the gather reads and writes the selected rows once more than the
- * decode itself reads them.
  * Errors: MLA_ERR_INVALID_ARG (also for a plan not made by
  * mla_sparse_plan), MLA_ERR_UNSUPPORTED_DEVICE, MLA_ERR_WORKSPACE_TOO_SMALL,
  * MLA_ERR_CUDA.

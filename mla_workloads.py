@@ -309,3 +309,21 @@ def expected_counts(w: Dict[str, object]) -> Dict[str, float]:
     flops = tokens * H * (2 * D + 2 * D_C)
     return {"tokens": tokens, "kv_bytes": float(kv_bytes), "bytes": float(total),
             "flops": float(flops)}
+
+
+def sparse_counts(w: Dict[str, object]) -> Dict[str, float]:
+    """Algorithmic byte and flop counts of one sparse decode call: the cache
+    rows of the valid list entries read once (a duplicate counts each time),
+    the block-table entry of each, the lists themselves, q_nope+q_pe, out,
+    lse and the lengths. Flops as for the dense decode, over the valid
+    entries."""
+    seq = np.asarray(w["seq_lens"], dtype=np.int64)
+    idx = np.asarray(w["topk_indices"], dtype=np.int64)
+    B, H = int(w["B"]), int(w["H"])
+    tokens = int(((idx >= 0) & (idx < seq[:, None])).sum())
+    kv_bytes = tokens * D * (1 if "kv_fp8" in w else 2)
+    total = (kv_bytes + 4 * tokens + 4 * idx.size + B * H * D * 2 + B * H * D_C * 2 + 4 * B * H
+             + 4 * B)
+    flops = tokens * H * (2 * D + 2 * D_C)
+    return {"tokens": tokens, "kv_bytes": float(kv_bytes), "bytes": float(total),
+            "flops": float(flops)}

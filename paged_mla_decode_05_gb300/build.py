@@ -19,9 +19,9 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libmla_decode_sm103.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
-SOURCES = ["mla_decode_sm103.cu", "mla_combine_sm103.cu", "mla_no_alloc_sm103.cu",
-           "mla_selftest_sm103.cu", "mla_sparse_sm103.cu", "mla_api.cpp"]
-HEADERS = ["mla_internal.h", "ptx_sm103.cuh"]
+SOURCES = ["mla_decode_sm103.cu", "mla_decode_rows_sm103.cu", "mla_combine_sm103.cu",
+           "mla_no_alloc_sm103.cu", "mla_selftest_sm103.cu", "mla_sparse_sm103.cu", "mla_api.cpp"]
+HEADERS = ["mla_internal.h", "ptx_sm103.cuh", "mla_decode_kernel.cuh"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 
 

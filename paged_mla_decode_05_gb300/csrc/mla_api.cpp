@@ -66,10 +66,11 @@ struct mla_plan_s {
   const void* tmap_ptr = nullptr;
   int64_t tmap_blocks = -1;
   int tmap_fp8 = -1;
-  // Sparse plans (mla_sparse_plan): the schedule is that of a compact cache of
-  // max_blocks blocks of kSparseBlock rows per request with lengths bounded by
-  // sparse_topk; the workspace holds the decode's partials, then at
-  // sparse_off the compact lengths, block table and cache.
+  int64_t tmap_gather_rows = 0;   // > 0: row-gather maps over this many rows
+  // Sparse plans (mla_sparse_plan): the schedule is that of requests of
+  // sparse_topk list positions (max_blocks blocks of kSparseBlock); the
+  // workspace holds the decode's partials, then at sparse_off the per-request
+  // counts of valid entries and the compacted row lists [B, sparse_topk].
   int sparse_topk = 0;
   size_t sparse_off = 0;
 };
@@ -524,12 +525,50 @@ bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(pt
 // swizzle), the rope boxes. Splitting the row keeps every box inside it: a
 // 128-column view of the rope columns would read 64 bytes past each row,
 // and past the pool's end on its last row.
-mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_blocks, bool fp8) {
-  if (p->tmap_ptr == kv_cache && p->tmap_blocks == num_blocks && p->tmap_fp8 == (fp8 ? 1 : 0))
+// Row-list mode (gather_rows > 0): 2-D {columns, rows} views of the whole
+// cache, boxes one row high, for four-row gathers (see DecodeParams::rows).
+mla_status_t encode_gather_maps(mla_plan_s* p, const void* kv_cache, int64_t rows, bool fp8,
+                                PFN_cuTensorMapEncodeTiled_v12000 enc) {
+  const cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kD), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kD) * (fp8 ? 1 : 2)};
+  const cuuint32_t box[2] = {fp8 ? 128u : static_cast<cuuint32_t>(mla::kPanelCols), 1};
+  if (enc(&p->tmap_k32, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+          const_cast<void*>(kv_cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MLA_ERR_INVALID_ARG;
+  p->tmap_k16 = p->tmap_k32;
+  if (fp8) {
+    const cuuint64_t rdims[2] = {static_cast<cuuint64_t>(mla::kDr), static_cast<cuuint64_t>(rows)};
+    const cuuint32_t rbox[2] = {static_cast<cuuint32_t>(mla::kDr), 1};
+    void* rope = const_cast<uint8_t*>(static_cast<const uint8_t*>(kv_cache) + mla::kDc);
+    if (enc(&p->tmap_v32, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, rope, rdims, strides, rbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_INVALID_ARG;
+    p->tmap_v16 = p->tmap_v32;
+  }
+  return MLA_OK;
+}
+
+mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_blocks, bool fp8,
+                             int64_t gather_rows = 0) {
+  if (p->tmap_ptr == kv_cache && p->tmap_blocks == num_blocks && p->tmap_fp8 == (fp8 ? 1 : 0) &&
+      p->tmap_gather_rows == gather_rows)
     return MLA_OK;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return MLA_ERR_CUDA;
   p->tmap_ptr = nullptr;
+  if (gather_rows > 0) {
+    mla_status_t st = encode_gather_maps(p, kv_cache, gather_rows, fp8, enc);
+    if (st != MLA_OK) return st;
+    p->tmap_ptr = kv_cache;
+    p->tmap_blocks = num_blocks;
+    p->tmap_fp8 = fp8 ? 1 : 0;
+    p->tmap_gather_rows = gather_rows;
+    return MLA_OK;
+  }
   const cuuint64_t groups = static_cast<cuuint64_t>(num_blocks) * p->block_size / 8;
   const int large = std::min(p->block_size, mla::kRowsLargeBox);
   const cuuint32_t g_small = mla::kRowsSmallBox / 8, g_large = static_cast<cuuint32_t>(large / 8);
@@ -580,6 +619,7 @@ mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_bl
   p->tmap_ptr = kv_cache;
   p->tmap_blocks = num_blocks;
   p->tmap_fp8 = fp8 ? 1 : 0;
+  p->tmap_gather_rows = 0;
   return MLA_OK;
 }
 
@@ -699,15 +739,19 @@ mla_status_t decode_impl(mla_plan_t p, const void* q_nope, const void* q_pe, con
                          bool fp8, float kv_scale, int64_t num_blocks, const int32_t* block_table,
                          const int32_t* seq_lens, float sm_scale, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, void* stream,
-                         bool sparse = false) {
+                         const int32_t* rows = nullptr, int64_t num_rows = 0) {
+  // rows != null: row-list mode (sparse plans only); token t of request b is
+  // cache row rows[b * sparse_topk + t] of num_rows; the block table is unused.
+  const bool sparse = rows != nullptr;
   if (!p || p->host_only || (p->sparse_topk > 0) != sparse) return MLA_ERR_INVALID_ARG;
   if (fp8 && (!(kv_scale > 0.0f) || !std::isfinite(kv_scale))) return MLA_ERR_INVALID_ARG;
-  if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !lse)
+  if (!q_nope || !q_pe || !kv_cache || (!block_table && !sparse) || !seq_lens || !out || !lse)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
       !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
     return MLA_ERR_INVALID_ARG;
-  if (num_blocks < 1 || num_blocks * p->block_size + 64 >= (int64_t{1} << 31))
+  const int64_t cache_rows = sparse ? num_rows : num_blocks * p->block_size;
+  if (num_blocks < 1 || cache_rows < 1 || cache_rows + 64 >= (int64_t{1} << 31))
     return MLA_ERR_INVALID_ARG;
   if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
   const size_t ws_need = sparse ? p->sparse_off : p->workspace_bytes;   // the decode's own part
@@ -721,7 +765,7 @@ mla_status_t decode_impl(mla_plan_t p, const void* q_nope, const void* q_pe, con
   mla_status_t st = prepare_device(dev, nullptr);
   if (st != MLA_OK) return st;
 
-  st = refresh_kv_maps(p, kv_cache, num_blocks, fp8);
+  st = refresh_kv_maps(p, kv_cache, num_blocks, fp8, sparse ? num_rows : 0);
   if (st != MLA_OK) return st;
 
   mla::DecodeParams dp;
@@ -748,9 +792,12 @@ mla_status_t decode_impl(mla_plan_t p, const void* q_nope, const void* q_pe, con
   dp.H = p->H;
   dp.q_len = p->q_len;
   dp.heads = p->heads;
-  dp.block_size = p->block_size;
+  // Row-list mode views the cache as blocks of one row.
+  dp.block_size = sparse ? 1 : p->block_size;
   dp.max_blocks = p->max_blocks;
-  dp.num_blocks = num_blocks;
+  dp.num_blocks = sparse ? num_rows : num_blocks;
+  dp.rows = rows;
+  dp.rows_stride = sparse ? p->sparse_topk : 0;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
   dp.dynamic_lens = p->lengths_are_bounds ? 1 : 0;
   dp.kv_fp8 = fp8 ? 1 : 0;
@@ -810,11 +857,9 @@ mla_status_t mla_sparse_plan(int B, int H, int topk, const mla_plan_options_t* o
   if (st != MLA_OK) return st;
   mla_plan_s* p = *plan_out;
   p->sparse_topk = topk;
-  const size_t rows = static_cast<size_t>(B) * max_blocks_c * mla::kSparseBlock;
   p->sparse_off = align_up(p->workspace_bytes, 256);
   p->workspace_bytes = p->sparse_off + align_up(static_cast<size_t>(B) * 4, 256) +
-                       align_up(static_cast<size_t>(B) * max_blocks_c * 4, 256) +
-                       rows * mla::kD * 2;
+                       static_cast<size_t>(B) * topk * 4;
   return MLA_OK;
 }
 
@@ -832,8 +877,15 @@ mla_status_t mla_decode_sparse(mla_plan_t p, const void* q_nope, const void* q_p
     return MLA_ERR_INVALID_ARG;
   if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
     return MLA_ERR_INVALID_ARG;
-  if (max_blocks < 1 || num_blocks < 1 || num_blocks * block_size >= (int64_t{1} << 40))
+  // Rows are int32 TMA coordinates.
+  if (max_blocks < 1 || num_blocks < 1 || num_blocks * block_size + 64 >= (int64_t{1} << 31))
     return MLA_ERR_INVALID_ARG;
+  // What the decode step checks, checked before the row-list kernel runs.
+  if (!q_nope || !q_pe || !out || !lse || !aligned(q_nope, 16) || !aligned(q_pe, 16) ||
+      !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+  if (kv_fp8 && (!(kv_scale > 0.0f) || !std::isfinite(kv_scale))) return MLA_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < p->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   int dev = -1;
@@ -843,31 +895,24 @@ mla_status_t mla_decode_sparse(mla_plan_t p, const void* q_nope, const void* q_p
   if (st != MLA_OK) return st;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int32_t* lens_c = reinterpret_cast<int32_t*>(ws + p->sparse_off);
-  int32_t* table_c = reinterpret_cast<int32_t*>(ws + p->sparse_off + align_up(p->B * 4, 256));
-  uint8_t* cache_c = ws + p->sparse_off + align_up(p->B * 4, 256) +
-                     align_up(static_cast<size_t>(p->B) * p->max_blocks * 4, 256);
-  mla::SparseGatherParams gp;
-  gp.kv_cache = kv_cache;
-  gp.num_blocks = num_blocks;
-  gp.block_size = block_size;
-  gp.max_blocks = max_blocks;
-  gp.block_table = block_table;
-  gp.seq_lens = seq_lens;
-  gp.topk_indices = topk_indices;
-  gp.topk = p->sparse_topk;
-  gp.row_bytes = kv_fp8 ? mla::kD : mla::kD * 2;
-  gp.compact = cache_c;
-  gp.rows_per_request = p->max_blocks * mla::kSparseBlock;
-  gp.compact_lens = lens_c;
-  gp.compact_table = table_c;
-  gp.max_blocks_c = p->max_blocks;
-  gp.err = reinterpret_cast<uint32_t*>(p->d_buf);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + p->sparse_off);
+  int32_t* rows = reinterpret_cast<int32_t*>(ws + p->sparse_off + align_up(p->B * 4, 256));
+  mla::SparseRowsParams rp;
+  rp.num_blocks = num_blocks;
+  rp.block_size = block_size;
+  rp.max_blocks = max_blocks;
+  rp.block_table = block_table;
+  rp.seq_lens = seq_lens;
+  rp.topk_indices = topk_indices;
+  rp.topk = p->sparse_topk;
+  rp.rows = rows;
+  rp.counts = counts;
+  rp.err = reinterpret_cast<uint32_t*>(p->d_buf);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (mla::launch_sparse_gather(gp, p->B, s) != cudaSuccess) return MLA_ERR_CUDA;
-  return decode_impl(p, q_nope, q_pe, cache_c, kv_fp8 != 0, kv_scale,
-                     static_cast<int64_t>(p->B) * p->max_blocks, table_c, lens_c, sm_scale, out,
-                     lse, workspace, p->sparse_off, stream, true);
+  if (mla::launch_sparse_rows(rp, p->B, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return decode_impl(p, q_nope, q_pe, kv_cache, kv_fp8 != 0, kv_scale, num_blocks, nullptr, counts,
+                     sm_scale, out, lse, workspace, p->sparse_off, stream, rows,
+                     num_blocks * block_size);
 }
 
 // The allocation-free variant: the workspace and the device copy of the work

@@ -1,0 +1,27 @@
+// Row-list MLA decode for sm_103a: the instances of the decode kernel (bf16
+// and FP8 caches) whose producers fetch each tile's rows from a per-request
+// list of cache rows with four-row TMA gathers (the sparse decode's second
+// step); the kernel itself is in mla_decode_kernel.cuh.
+#include "mla_decode_kernel.cuh"
+
+namespace mla {
+
+cudaError_t decode_rows_prepare_device() {
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<false, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_kernel<true, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+cudaError_t launch_decode_rows(const DecodeParams& p, int num_clusters, cudaStream_t stream) {
+  if (p.kv_fp8)
+    mla_decode_kernel<true, true><<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1), kSmemBytes,
+                                    stream>>>(p);
+  else
+    mla_decode_kernel<false, true><<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1),
+                                     kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

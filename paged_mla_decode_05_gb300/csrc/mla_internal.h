@@ -145,6 +145,17 @@ struct DecodeParams {
   int dynamic_lens;               // 1: planned lengths are upper bounds; items end at the device length
   int kv_fp8;                     // 1: the cache holds E4M3 bytes [num_blocks, bs, 576]
   float kv_scale;                 // FP8 cache: element value = kv_scale * e4m3(byte)
+  // Row-list mode (sparse decode), when rows is not null: token t of request
+  // b is cache row rows[b * rows_stride + t] (row = block id * block_size +
+  // slot), the block table is not read, and the tensor maps are 2-D row
+  // views fetched with four-row gathers: bf16 tmap_k32 = {576 columns, rows}
+  // with box {64, 1} and the 128-byte swizzle (K: 9 panels, V: 8); FP8
+  // tmap_k32 = {576, rows} with box {128, 1} and the 128-byte swizzle (c_kv),
+  // tmap_v32 = columns 512..575 as {64, rows}, box {64, 1}, 64-byte swizzle.
+  // Four gathered rows land as half of an 8-row atom, so the shared-memory
+  // layout is that of the paged mode.
+  const int32_t* rows;
+  int rows_stride;
 };
 
 struct CombineParams {
@@ -156,12 +167,10 @@ struct CombineParams {
   int H;
 };
 
-// Sparse (top-k) decode, gather step (mla_sparse_sm103.cu): the valid
-// entries of each request's token list, compacted into a cache of
-// rows_per_request rows per request (row_bytes each), with its lengths and an
-// identity block table for the decode kernel.
-struct SparseGatherParams {
-  const void* kv_cache;           // the caller's cache [num_blocks, block_size, 576]
+// Sparse (top-k) decode, first step (mla_sparse_sm103.cu): per request, the
+// cache rows of the valid list entries, compacted in list order, and their
+// count; the decode kernel then runs in row-list mode over them.
+struct SparseRowsParams {
   int64_t num_blocks;
   int block_size;
   int max_blocks;
@@ -169,19 +178,22 @@ struct SparseGatherParams {
   const int32_t* seq_lens;        // [B]
   const int32_t* topk_indices;    // [B, topk]
   int topk;
-  int row_bytes;                  // 1152 (bf16) or 576 (FP8)
-  void* compact;                  // [B, rows_per_request, row_bytes]
-  int rows_per_request;           // max_blocks_c * the compact block size
-  int32_t* compact_lens;          // [B]
-  int32_t* compact_table;         // [B, max_blocks_c]
-  int max_blocks_c;
+  int32_t* rows;                  // [B, topk]: rows[b][0..count) written
+  int32_t* counts;                // [B]
   uint32_t* err;
 };
-constexpr int kSparseBlock = 64;  // rows per block of the compact cache
+
+// Nominal block size of a sparse plan's schedule: the lists are scheduled
+// as requests of topk tokens over blocks of this many list positions.
+constexpr int kSparseBlock = 64;
 
 // Launchers (defined in the .cu files).
-cudaError_t launch_sparse_gather(const SparseGatherParams& p, int B, cudaStream_t stream);
+cudaError_t launch_sparse_rows(const SparseRowsParams& p, int B, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int num_clusters, cudaStream_t stream);
+// The row-list instances (mla_decode_rows_sm103.cu); launch_decode forwards
+// a DecodeParams with rows set.
+cudaError_t launch_decode_rows(const DecodeParams& p, int num_clusters, cudaStream_t stream);
+cudaError_t decode_rows_prepare_device();
 // max_slots: the largest n_slots of the combine items (at most 4096).
 cudaError_t launch_combine(const CombineParams& p, int num_items, int max_slots,
                            cudaStream_t stream);

@@ -82,7 +82,7 @@ MLA_DEVI bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
 // if the wait ran out of time. The first try is inline; the bounded retry
 // loop is out of line, so the many wait sites stay small in the
 // instruction cache.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {
     if (clock64() - t0 > kWaitLimitCycles) return false;
@@ -93,7 +93,7 @@ MLA_DEVI bool mbar_wait(uint32_t bar, uint32_t parity) {
   return mbar_try(bar, parity) || mbar_wait_slow(bar, parity);
 }
 // Same, with acquire at cluster scope: for barriers completed by the peer CTA.
-__device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity) {
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try_cluster(bar, parity)) {
     if (clock64() - t0 > kWaitLimitCycles) return false;
@@ -135,6 +135,17 @@ MLA_DEVI void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %4}], [%5], %6;"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy) : "memory");
+}
+// Row-gather TMA load (2-D tensor map whose box is one row high): four rows
+// r0..r3, columns [x, x + box width), land as four consecutive box rows at
+// dst, swizzled by the map. A row at or past the map's row count reads zeros.
+MLA_DEVI void tma_gather4(uint32_t dst, const void* tmap, int x, int r0, int r1, int r2, int r3,
+                          uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
+      : "memory");
 }
 MLA_DEVI uint64_t policy_evict_first() {
   uint64_t p;

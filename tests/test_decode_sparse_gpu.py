@@ -111,7 +111,7 @@ def test_sparse_mixed_padding_and_short_requests(lib, oracle_mod, kv):
 @pytest.mark.parametrize("topk", [1, 7, 31, 32, 33, 96, 97, 300, 4096])
 def test_sparse_topk_values(lib, oracle_mod, topk):
     """Lists of every length class: below, at and past a 32-row piece, a tile
-    (96) and a 64-row compact page; 4096 is longer than every request."""
+    (96) and a 64-position plan block; 4096 is longer than every request."""
     w = spec(f"sp_k{topk}", 4, 128, 32, [500, 1, 97, 3000], seed=topk)
     w = wl.with_topk(w, topk, seed=topk + 1)
     sparse_parity(lib, oracle_mod, w, f"sparse topk={topk}")
@@ -127,7 +127,7 @@ def test_sparse_source_block_sizes(lib, oracle_mod, bs):
 @pytest.mark.parametrize("H", [16, 100, 192])
 def test_sparse_head_counts(lib, oracle_mod, H):
     """16 and 100 heads (a group padded inside the kernel) and 192 (two head
-    groups over the same compact rows)."""
+    groups over the same row list)."""
     w = spec(f"sp_h{H}", 3, H, 64, [700, 40, 2500], seed=H)
     w = wl.with_topk(w, 256, seed=H + 3)
     sparse_parity(lib, oracle_mod, w, f"sparse H={H}")
@@ -224,11 +224,13 @@ def test_sparse_argument_errors(lib):
         m.mla_decode_sparse(dense, t["q_nope"], t["q_pe"], t["kv"], t["block_table"],
                             t["seq_lens"], t["topk_indices"], 0.1, out, lse, ws)
     with pytest.raises(m.MLAError):   # a sparse plan does not serve the dense call
-        m.mla_decode(sparse, t["q_nope"], t["q_pe"], t["kv"], t["block_table"], t["seq_lens"],
-                     0.1, out, lse, ws)
+        m.mla_decode(sparse, t["q_nope"], t["q_pe"], t["kv"],
+                     t["block_table"][:, :sparse.max_blocks].contiguous(), t["seq_lens"], 0.1,
+                     out, lse, ws)
     with pytest.raises(m.MLAError):   # workspace too small
         m.mla_decode_sparse(sparse, t["q_nope"], t["q_pe"], t["kv"], t["block_table"],
-                            t["seq_lens"], t["topk_indices"], 0.1, out, lse, ws[:4096])
+                            t["seq_lens"], t["topk_indices"], 0.1, out, lse,
+                            ws[:sparse.workspace_bytes - 1])
     with pytest.raises(ValueError):   # list of the wrong length
         m.mla_decode_sparse(sparse, t["q_nope"], t["q_pe"], t["kv"], t["block_table"],
                             t["seq_lens"], t["topk_indices"][:, :32].contiguous(), 0.1, out,
