@@ -226,7 +226,7 @@ mla_status_t mla_sparse_plan(int B, int H, int topk, const mla_plan_options_t* o
  * mla_decode_sparse — one sparse decode step. A small kernel turns each
  * request's list into the cache rows of its valid entries (in list order)
  * and their count, in the workspace; the decode kernel then fetches those
- * rows straight from the paged cache (TMA four-row gathers), each request's
+ * rows straight from the paged cache (16-byte asynchronous copies), each request's
  * length being its number of valid entries.
  *
  *  q_nope, q_pe, out, lse, sm_scale, stream   as for mla_decode ([B, H, ...])

@@ -66,7 +66,6 @@ struct mla_plan_s {
   const void* tmap_ptr = nullptr;
   int64_t tmap_blocks = -1;
   int tmap_fp8 = -1;
-  int64_t tmap_gather_rows = 0;   // > 0: row-gather maps over this many rows
   // Sparse plans (mla_sparse_plan): the schedule is that of requests of
   // sparse_topk list positions (max_blocks blocks of kSparseBlock); the
   // workspace holds the decode's partials, then at sparse_off the per-request
@@ -525,50 +524,12 @@ bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(pt
 // swizzle), the rope boxes. Splitting the row keeps every box inside it: a
 // 128-column view of the rope columns would read 64 bytes past each row,
 // and past the pool's end on its last row.
-// Row-list mode (gather_rows > 0): 2-D {columns, rows} views of the whole
-// cache, boxes one row high, for four-row gathers (see DecodeParams::rows).
-mla_status_t encode_gather_maps(mla_plan_s* p, const void* kv_cache, int64_t rows, bool fp8,
-                                PFN_cuTensorMapEncodeTiled_v12000 enc) {
-  const cuuint32_t estr[2] = {1, 1};
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kD), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kD) * (fp8 ? 1 : 2)};
-  const cuuint32_t box[2] = {fp8 ? 128u : static_cast<cuuint32_t>(mla::kPanelCols), 1};
-  if (enc(&p->tmap_k32, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-          const_cast<void*>(kv_cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return MLA_ERR_INVALID_ARG;
-  p->tmap_k16 = p->tmap_k32;
-  if (fp8) {
-    const cuuint64_t rdims[2] = {static_cast<cuuint64_t>(mla::kDr), static_cast<cuuint64_t>(rows)};
-    const cuuint32_t rbox[2] = {static_cast<cuuint32_t>(mla::kDr), 1};
-    void* rope = const_cast<uint8_t*>(static_cast<const uint8_t*>(kv_cache) + mla::kDc);
-    if (enc(&p->tmap_v32, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, rope, rdims, strides, rbox, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MLA_ERR_INVALID_ARG;
-    p->tmap_v16 = p->tmap_v32;
-  }
-  return MLA_OK;
-}
-
-mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_blocks, bool fp8,
-                             int64_t gather_rows = 0) {
-  if (p->tmap_ptr == kv_cache && p->tmap_blocks == num_blocks && p->tmap_fp8 == (fp8 ? 1 : 0) &&
-      p->tmap_gather_rows == gather_rows)
+mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_blocks, bool fp8) {
+  if (p->tmap_ptr == kv_cache && p->tmap_blocks == num_blocks && p->tmap_fp8 == (fp8 ? 1 : 0))
     return MLA_OK;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return MLA_ERR_CUDA;
   p->tmap_ptr = nullptr;
-  if (gather_rows > 0) {
-    mla_status_t st = encode_gather_maps(p, kv_cache, gather_rows, fp8, enc);
-    if (st != MLA_OK) return st;
-    p->tmap_ptr = kv_cache;
-    p->tmap_blocks = num_blocks;
-    p->tmap_fp8 = fp8 ? 1 : 0;
-    p->tmap_gather_rows = gather_rows;
-    return MLA_OK;
-  }
   const cuuint64_t groups = static_cast<cuuint64_t>(num_blocks) * p->block_size / 8;
   const int large = std::min(p->block_size, mla::kRowsLargeBox);
   const cuuint32_t g_small = mla::kRowsSmallBox / 8, g_large = static_cast<cuuint32_t>(large / 8);
@@ -619,7 +580,6 @@ mla_status_t refresh_kv_maps(mla_plan_s* p, const void* kv_cache, int64_t num_bl
   p->tmap_ptr = kv_cache;
   p->tmap_blocks = num_blocks;
   p->tmap_fp8 = fp8 ? 1 : 0;
-  p->tmap_gather_rows = 0;
   return MLA_OK;
 }
 
@@ -765,15 +725,19 @@ mla_status_t decode_impl(mla_plan_t p, const void* q_nope, const void* q_pe, con
   mla_status_t st = prepare_device(dev, nullptr);
   if (st != MLA_OK) return st;
 
-  st = refresh_kv_maps(p, kv_cache, num_blocks, fp8, sparse ? num_rows : 0);
-  if (st != MLA_OK) return st;
+  if (!sparse) {   // row-list mode reads rows with plain copies, not tensor maps
+    st = refresh_kv_maps(p, kv_cache, num_blocks, fp8);
+    if (st != MLA_OK) return st;
+  }
 
   mla::DecodeParams dp;
   std::memset(&dp, 0, sizeof(dp));
-  dp.tmap_k16 = p->tmap_k16;
-  dp.tmap_k32 = p->tmap_k32;
-  dp.tmap_v16 = p->tmap_v16;
-  dp.tmap_v32 = p->tmap_v32;
+  if (!sparse) {
+    dp.tmap_k16 = p->tmap_k16;
+    dp.tmap_k32 = p->tmap_k32;
+    dp.tmap_v16 = p->tmap_v16;
+    dp.tmap_v32 = p->tmap_v32;
+  }
   dp.kv_cache = kv_cache;
   dp.q_nope = static_cast<const uint16_t*>(q_nope);
   dp.q_pe = static_cast<const uint16_t*>(q_pe);

@@ -43,9 +43,11 @@
 // Heads below 128 are padded inside the kernel: zero Q rows in tensor memory
 // and zero P rows in shared memory, never stored.
 // Row-list mode (template flag ROWS, sparse decode): the tile's rows come
-// from a per-request list of cache rows, fetched with four-row TMA gathers
-// into the same shared-memory layout; everything past the producers is the
-// same code.
+// from a per-request list of cache rows, copied by six warps of the pair
+// with 16-byte cp.async into the same shared-memory layout (with the
+// swizzle applied in the addresses); everything past the producers is the
+// same code. TMA four-row gathers were measured first: at 512 bytes per
+// instruction they ran at a third of this rate.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -218,29 +220,117 @@ MLA_DEVI int cache_row(const DecodeParams& p, const WorkItem& w, int t, const Pa
   return (blk << sh) + (t & (p.block_size - 1));
 }
 
-// Row-list mode: the cache rows of list positions tile_t0 + 4 * lane + q
-// (q < 4) for lanes 0..kTile/4-1. Positions at or past the item's end take
-// the item's last row (the softmax masks them, so any finite row serves and
-// every gather stays inside the cache); a row outside the cache (not written
-// by the row-list kernel) is replaced by row 0.
-MLA_DEVI void tile_rows(const DecodeParams& p, const WorkItem& w, int tile_t0, int lane,
-                        int (&rr)[4]) {
-  const int n_rows = static_cast<int>(p.num_blocks * p.block_size);
-  const int32_t* rl = p.rows + static_cast<int64_t>(w.b) * p.rows_stride;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int t = min(tile_t0 + 4 * lane + q, w.t1 - 1);
-    int r = 0;
-    if (lane < kTile / 4) r = __ldg(&rl[t]);
-    rr[q] = (r >= 0 && r < n_rows) ? r : 0;
-  }
-}
-
 // Lane 0 waits on a barrier; the whole warp learns the outcome.
 MLA_DEVI bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
   bool ok = true;
   if (lane == 0) ok = mbar_wait(bar, parity);
   return __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+}
+
+// ------------------------------------------------------- row-list producers
+
+// Warps that fetch the rows of a tile in row-list mode: the score CTA's
+// producer and its two idle warps; the output CTA's producer and its five
+// idle warps. Each full barrier counts one arrival per lane of them.
+constexpr int kRowsScoreWarps = 3;
+constexpr int kRowsOutWarps = 6;
+
+// Cache rows of list positions tile_t0 + 32 j + lane (j < 3) of item w:
+// positions at or past the item's end take the item's last row (the softmax
+// masks them; any finite row serves), and a row outside the cache (not
+// written by the row-list kernel) is replaced by row 0.
+MLA_DEVI void tile_rows(const DecodeParams& p, const WorkItem& w, int tile_t0, int lane,
+                        int (&rr)[3]) {
+  const int n_rows = static_cast<int>(p.num_blocks * p.block_size);
+  const int32_t* rl = p.rows + static_cast<int64_t>(w.b) * p.rows_stride;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int t = min(tile_t0 + 32 * j + lane, w.t1 - 1);
+    const int r = __ldg(&rl[t]);
+    rr[j] = (r >= 0 && r < n_rows) ? r : 0;
+  }
+}
+// Row of tile position pos (all lanes call this with positions in one
+// 32-position block).
+MLA_DEVI int row_at(const int (&rr)[3], int pos) {
+  const int j = pos >> 5;
+  const int v = j == 0 ? rr[0] : (j == 1 ? rr[1] : rr[2]);
+  return __shfl_sync(kFullMask, v, pos & 31);
+}
+
+// Row-list producer, one of `parts` warps: each tile's rows are copied from
+// the cache with 16-byte cp.async into the layout the paged mode's TMA boxes
+// produce ([8-row group][128-byte panel][8 rows][128 B], the 128-byte
+// swizzle XORing the 16-byte chunk index with the row's index in its group;
+// FP8 rope columns: [group][8 rows][64 B], the 64-byte swizzle XORing with
+// half the row index). Per warp instruction: 4 rows x 128 bytes, lanes
+// 8q..8q+7 on row q. Warp `part` takes the row quads part, part + parts, ...
+// Every lane arrives on the full barrier once its copies have landed
+// (cp.async.mbarrier.arrive.noinc); the MMA issuer fences the generic-proxy
+// writes before its tensor-core reads.
+// OUT = false: the score CTA's K tiles (576 columns, ring of stages);
+// OUT = true: the output CTA's V (512 columns; bf16 as two 256-column
+// slots per tile, FP8 as one).
+template <bool F8, bool OUT>
+MLA_DEVI void rows_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int lane, int part,
+                            int parts, int it0, int it1) {
+  constexpr int NS = OUT ? kNumVSlots : num_stages<F8>();
+  constexpr int SB = OUT ? kVHalfBytes : stage_bytes<F8>();
+  constexpr int kSlotsPerTile = (OUT && !F8) ? 2 : 1;
+  constexpr int kRowBytes = F8 ? kD : kD * 2;
+  constexpr int kPanels = OUT ? (F8 ? kF8Panels : kVHalfPanels) : (F8 ? kF8Panels : kNumPanels);
+  constexpr int kGroupBytes = F8 ? kF8NopeGroupBytes : (OUT ? kVGroupBytes : kKGroupBytes);
+  const char* cache = static_cast<const char*>(p.kv_cache);
+  const int q = lane >> 3, ch = lane & 7;
+  uint32_t err = 0;
+  int h = 0;
+  bool ok = true;
+  for (int it = it0; it < it1 && ok; ++it) {
+    const WorkItem w = item_at(p, it);
+    if (!OUT && part == 0 && lane == 0) {   // MLA_DEVERR_SEQLEN_MISMATCH: above the bound
+      const int len = __ldg(&p.seq_lens[w.b]);
+      if (len < 0 || len > w.seq_len) err |= 2u;
+    }
+    const int nt = tiles_of(w);
+    for (int i = 0; i < nt && ok; ++i) {
+      const int tile_t0 = w.t0 + i * kTile;
+      int rr[3];
+      tile_rows(p, w, tile_t0, lane, rr);
+      for (int half = 0; half < kSlotsPerTile; ++half, ++h) {
+        const int s = h % NS;
+        const uint32_t empty = smem_addr(OUT ? &c->v_empty[s] : &c->kv_empty[s]);
+        if (h >= NS && !warp_wait(empty, ((h / NS) - 1) & 1, lane)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = smem_addr(data + s * SB);
+        const int col0 = (OUT && !F8) ? half * kVHalfPanels * 128 : 0;   // byte column
+        for (int g4 = part; g4 < kTile / 4; g4 += parts) {
+          const int pos = 4 * g4 + q;
+          const int r8 = pos & 7;
+          const char* src = cache + static_cast<int64_t>(row_at(rr, pos)) * kRowBytes + col0 + ch * 16;
+          const uint32_t dst = st + (pos >> 3) * kGroupBytes + r8 * 128 + ((ch ^ r8) << 4);
+#pragma unroll
+          for (int k = 0; k < kPanels; ++k) cp_async16(dst + k * kAtomBytes, src + k * 128);
+        }
+        if (F8 && !OUT) {   // rope columns: 8 rows x 4 chunks per instruction
+          const int c4 = lane & 3;
+          for (int i8 = part; i8 < kTile / 8; i8 += parts) {
+            const int pos = 8 * i8 + (lane >> 2);
+            const int r8 = pos & 7;
+            cp_async16(st + kF8NopeBytes + (pos >> 3) * kF8RopeGroupBytes + r8 * 64 +
+                           ((c4 ^ (r8 >> 1)) << 4),
+                       cache + static_cast<int64_t>(row_at(rr, pos)) * kRowBytes + kDc + c4 * 16);
+          }
+        }
+        cp_async_arrive_noinc(smem_addr(OUT ? &c->v_full[s] : &c->kv_full[s]));
+      }
+    }
+  }
+  cp_async_wait_all();   // nothing of this warp is in flight when it leaves
+  if (!ok) err |= 4u;
+  err = __reduce_or_sync(kFullMask, err);
+  if (lane == 0) report(p, err);
 }
 
 // ------------------------------------------------------------ score CTA roles
@@ -251,7 +341,7 @@ MLA_DEVI bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
 // rope columns of the same pieces. The stage layout does not depend on how
 // the tile is cut into pieces; one barrier per stage counts the bytes of all
 // pieces.
-template <bool F8, bool ROWS>
+template <bool F8>
 MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int lane, int it0,
                              int it1) {
   constexpr int NS = num_stages<F8>();
@@ -288,15 +378,10 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
       }
       const int s = g % NS;
       const int tile_t0 = w.t0 + i * kTile;
-      int r0 = 0, large = 0, y = 0;
-      int rr[4];
-      if constexpr (ROWS) {
-        tile_rows(p, w, tile_t0, lane, rr);
-      } else {
-        piece_shape(p.block_size, j < n ? j : 0, r0, large);
-        window_cover(p, w, tile_t0, win, lane);
-        y = cache_row(p, w, tile_t0 + r0, win, err);   // a multiple of 8
-      }
+      int r0, large;
+      piece_shape(p.block_size, j < n ? j : 0, r0, large);
+      window_cover(p, w, tile_t0, win, lane);
+      const int y = cache_row(p, w, tile_t0 + r0, win, err);   // a multiple of 8
       MLA_TRACE_AT(0, g);
       if (g >= NS && !warp_wait(smem_addr(&c->kv_empty[s]), ((g / NS) - 1) & 1, lane)) {
         ok = false;
@@ -306,28 +391,7 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
       if (lane == 0) mbar_arrive_expect_tx(full, SB);
       __syncwarp();
       uint8_t* stage = data + s * SB;
-      if constexpr (ROWS) {
-        // Lane l gathers rows 4l..4l+3 of the tile: half of row group l / 2,
-        // every panel (and, FP8, the rope columns).
-        if (lane < kTile / 4) {
-          const uint32_t half = (lane & 1) * 4;
-          if (!F8) {
-            const uint32_t grp = smem_addr(stage) + (lane >> 1) * kKGroupBytes + half * 128;
-#pragma unroll
-            for (int k = 0; k < kNumPanels; ++k)
-              tma_gather4(grp + k * kAtomBytes, &p.tmap_k32, k * kPanelCols, rr[0], rr[1], rr[2],
-                          rr[3], full, policy);
-          } else {
-            const uint32_t grp = smem_addr(stage) + (lane >> 1) * kF8NopeGroupBytes + half * 128;
-#pragma unroll
-            for (int k = 0; k < kF8Panels; ++k)
-              tma_gather4(grp + k * kAtomBytes, &p.tmap_k32, k * 128, rr[0], rr[1], rr[2], rr[3],
-                          full, policy);
-            tma_gather4(smem_addr(stage + kF8NopeBytes) + (lane >> 1) * kF8RopeGroupBytes + half * 64,
-                        &p.tmap_v32, 0, rr[0], rr[1], rr[2], rr[3], full, policy);
-          }
-        }
-      } else if (!F8) {
+      if (!F8) {
         if (lane < n)
           tma_load_4d(smem_addr(stage + (r0 >> 3) * kKGroupBytes),
                       large ? static_cast<const void*>(&p.tmap_k32)
@@ -360,7 +424,7 @@ MLA_DEVI void score_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int 
 // tensor memory) against the same K columns. An item's first tile follows
 // its Q into tensor memory panel by panel; later tiles issue the fully
 // unrolled sequence (one thread issues one MMA every ~45 cycles at best).
-template <bool F8>
+template <bool F8, bool ROWS>
 MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
                         int it1) {
   constexpr int NS = num_stages<F8>();
@@ -381,6 +445,7 @@ MLA_DEVI void score_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t 
       if (!mbar_wait(smem_addr(&c->kv_full[s]), (g / NS) & 1)) { ok = false; break; }
       MLA_TRACE_AT(1, g);
       tc_after_sync();
+      if constexpr (ROWS) fence_proxy_async_smem();   // cp.async (generic proxy) data
       const uint32_t d = tmem + kTmemS0 + sb * kTile;
       const uint32_t a = tmem + kTmemQ;
       uint8_t* stage = data + s * SB;
@@ -849,7 +914,7 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
 // TMA producer warp of the output CTA: V into a ring of kNumVSlots 48 KB
 // slots. bf16: each tile as two half-tiles of 256 columns (4 panels); FP8:
 // each tile's 512 columns in one slot.
-template <bool F8, bool ROWS>
+template <bool F8>
 MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int lane, int it0,
                            int it1) {
   constexpr int kParts = F8 ? 1 : 2;   // slots per tile
@@ -864,15 +929,10 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
     for (int i = 0; i < nt && ok; ++i) {
       const int tile_t0 = w.t0 + i * kTile;
       const int n = pieces_per_tile(p.block_size);
-      int r0 = 0, large = 0, y = 0;
-      int rr[4];
-      if constexpr (ROWS) {
-        tile_rows(p, w, tile_t0, lane, rr);
-      } else {
-        piece_shape(p.block_size, lane < n ? lane : 0, r0, large);
-        window_cover(p, w, tile_t0, win, lane);
-        y = cache_row(p, w, tile_t0 + r0, win, err);
-      }
+      int r0, large;
+      piece_shape(p.block_size, lane < n ? lane : 0, r0, large);
+      window_cover(p, w, tile_t0, win, lane);
+      const int y = cache_row(p, w, tile_t0 + r0, win, err);
       for (int half = 0; half < kParts; ++half, ++h) {
         const int v = h % kNumVSlots;
         if (h >= kNumVSlots &&
@@ -884,20 +944,8 @@ MLA_DEVI void out_producer(const DecodeParams& p, Ctrl* c, uint8_t* data, int la
         const uint32_t full = smem_addr(&c->v_full[v]);
         if (lane == 0) mbar_arrive_expect_tx(full, kVHalfBytes);
         __syncwarp();
-        if constexpr (ROWS) {
-          // Lane l gathers rows 4l..4l+3 of the tile, this slot's panels.
-          if (lane < kTile / 4) {
-            const uint32_t grp = smem_addr(data + v * kVHalfBytes) +
-                                 (lane >> 1) * (F8 ? kF8NopeGroupBytes : kVGroupBytes) +
-                                 (lane & 1) * 4 * 128;
-#pragma unroll
-            for (int k = 0; k < (F8 ? kF8Panels : kVHalfPanels); ++k)
-              tma_gather4(grp + k * kAtomBytes, &p.tmap_k32,
-                          F8 ? k * 128 : (half * kVHalfPanels + k) * kPanelCols, rr[0], rr[1],
-                          rr[2], rr[3], full, policy);
-          }
-        } else if (lane < n) {
-          // One warp instruction: lane j loads piece j.
+        // One warp instruction: lane j loads piece j.
+        if (lane < n) {
           if (F8)
             tma_load_4d(smem_addr(data + v * kVHalfBytes) + (r0 >> 3) * kF8NopeGroupBytes,
                         large ? static_cast<const void*>(&p.tmap_k32)
@@ -986,7 +1034,7 @@ MLA_DEVI void out_prefetcher(const DecodeParams& p, Ctrl* c, int lane, int it0, 
 //
 // FP8 path: one V slot per tile; per 256-column half, the hi and the lo terms
 // of P each take 3 k-steps of 32 tokens (6 MMAs with N = 256).
-template <bool F8>
+template <bool F8, bool ROWS>
 MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem, int it0,
                       int it1) {
   int g = 0, h = 0, r = 0, n_items = 0;
@@ -1030,6 +1078,7 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
           if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
           MLA_TRACE_AT(11 + half, g);
           tc_after_sync();
+          if constexpr (ROWS) fence_proxy_async_smem();
           // V half: MN-major, 128-byte swizzle; 64-column panels 1 KB apart
           // (LBO), 8-token row groups kVGroupBytes apart (SBO); a k-step of
           // 16 tokens is two row groups.
@@ -1047,6 +1096,7 @@ MLA_DEVI void out_mma(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tm
         if (!mbar_wait(smem_addr(&c->v_full[v]), (h / kNumVSlots) & 1)) { ok = false; break; }
         ++h;
         tc_after_sync();
+        if constexpr (ROWS) fence_proxy_async_smem();
         // V tile: MN-major, 128-byte swizzle; 128-column panels 1 KB apart
         // (LBO), 8-token row groups kF8NopeGroupBytes apart (SBO); a k-step
         // of 32 tokens is four row groups, a 256-column half two panels.
@@ -1251,7 +1301,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < num_stages<F8>(); ++s) {
-      mbar_init(smem_addr(&c->kv_full[s]), 1);
+      mbar_init(smem_addr(&c->kv_full[s]), ROWS ? 32 * kRowsScoreWarps : 1);
       mbar_init(smem_addr(&c->kv_empty[s]), 1);
     }
     for (int j = 0; j < kNumPBufs; ++j) {
@@ -1270,17 +1320,17 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
       mbar_init(smem_addr(&c->p_full[k]), 1);
     }
     for (int v = 0; v < kNumVSlots; ++v) {
-      mbar_init(smem_addr(&c->v_full[v]), 1);
+      mbar_init(smem_addr(&c->v_full[v]), ROWS ? 32 * kRowsOutWarps : 1);
       mbar_init(smem_addr(&c->v_empty[v]), 1);
     }
     for (int j = 0; j < kF8QScaleSlots; ++j) mbar_init(smem_addr(&c->qs_ready[j]), 128);
     c->p_seen = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (!ROWS && warp == 0 && lane == 0) {   // row-list mode uses no tensor maps
     prefetch_tmap(&p.tmap_k16);
     prefetch_tmap(&p.tmap_k32);
-  } else if (warp == 0 && lane == 1) {
+  } else if (!ROWS && warp == 0 && lane == 1) {
     prefetch_tmap(&p.tmap_v16);
     prefetch_tmap(&p.tmap_v32);
   }
@@ -1293,25 +1343,33 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   tc_after_sync();
   const uint32_t tmem = c->tmem_base;
 
+  // Row-list mode: the score CTA's warps 0, 6, 7 and the output CTA's
+  // warps 0, 7..11 fetch rows (parts 0..kRows*Warps-1).
   if (rank == 0) {
     if (warp == 0) {
-      score_producer<F8, ROWS>(p, c, data, lane, it0, it1);
+      if constexpr (ROWS) rows_producer<F8, false>(p, c, data, lane, 0, kRowsScoreWarps, it0, it1);
+      else score_producer<F8>(p, c, data, lane, it0, it1);
     } else if (warp == 1) {
-      if (lane == 0) score_mma<F8>(p, c, data, tmem, it0, it1);
+      if (lane == 0) score_mma<F8, ROWS>(p, c, data, tmem, it0, it1);
     } else if (warp < 6) {
       score_softmax<F8>(p, c, data, tmem, warp, lane, it0, it1);
     } else if (warp >= 8) {
       score_qloader<F8>(p, c, data, tmem, warp, lane, it0, it1);
+    } else if (ROWS) {
+      rows_producer<F8, false>(p, c, data, lane, warp - 5, kRowsScoreWarps, it0, it1);
     }
   } else {
     if (warp == 0) {
-      out_producer<F8, ROWS>(p, c, data, lane, it0, it1);
+      if constexpr (ROWS) rows_producer<F8, true>(p, c, data, lane, 0, kRowsOutWarps, it0, it1);
+      else out_producer<F8>(p, c, data, lane, it0, it1);
     } else if (warp == 1) {
-      if (lane == 0) out_mma<F8>(p, c, data, tmem, it0, it1);
+      if (lane == 0) out_mma<F8, ROWS>(p, c, data, tmem, it0, it1);
     } else if (warp < 6) {
       out_correct<F8>(p, c, data, tmem, warp, lane, it0, it1);
     } else if (warp == 6) {
       out_prefetcher<ROWS>(p, c, lane, it0, it1);
+    } else if (ROWS) {
+      rows_producer<F8, true>(p, c, data, lane, warp - 6, kRowsOutWarps, it0, it1);
     }
   }
   __syncwarp();

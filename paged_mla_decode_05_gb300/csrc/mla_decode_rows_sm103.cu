@@ -1,6 +1,7 @@
 // Row-list MLA decode for sm_103a: the instances of the decode kernel (bf16
 // and FP8 caches) whose producers fetch each tile's rows from a per-request
-// list of cache rows with four-row TMA gathers (the sparse decode's second
+// list of cache rows with 16-byte cp.async copies spread over six of the
+// pair's warps (the sparse decode's second
 // step); the kernel itself is in mla_decode_kernel.cuh.
 #include "mla_decode_kernel.cuh"
 

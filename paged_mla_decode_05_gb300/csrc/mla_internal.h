@@ -145,15 +145,11 @@ struct DecodeParams {
   int dynamic_lens;               // 1: planned lengths are upper bounds; items end at the device length
   int kv_fp8;                     // 1: the cache holds E4M3 bytes [num_blocks, bs, 576]
   float kv_scale;                 // FP8 cache: element value = kv_scale * e4m3(byte)
-  // Row-list mode (sparse decode), when rows is not null: token t of request
-  // b is cache row rows[b * rows_stride + t] (row = block id * block_size +
-  // slot), the block table is not read, and the tensor maps are 2-D row
-  // views fetched with four-row gathers: bf16 tmap_k32 = {576 columns, rows}
-  // with box {64, 1} and the 128-byte swizzle (K: 9 panels, V: 8); FP8
-  // tmap_k32 = {576, rows} with box {128, 1} and the 128-byte swizzle (c_kv),
-  // tmap_v32 = columns 512..575 as {64, rows}, box {64, 1}, 64-byte swizzle.
-  // Four gathered rows land as half of an 8-row atom, so the shared-memory
-  // layout is that of the paged mode.
+  // Row-list mode (sparse decode; the kernel's row-list instances): token t
+  // of request b is cache row rows[b * rows_stride + t] (row = block id *
+  // block_size + slot, with block_size 1 and num_blocks the row count in
+  // this mode); the block table and the tensor maps are not used: the rows
+  // are copied with 16-byte cp.async into the layout the TMA boxes produce.
   const int32_t* rows;
   int rows_stride;
 };

@@ -10,8 +10,8 @@
 //
 // This kernel turns each request's list into the cache rows of its valid
 // entries (row = block id * block_size + slot), compacted in list order, and
-// their count. The decode kernel then runs in row-list mode: its TMA producers
-// fetch those rows straight from the paged cache with four-row gathers, and
+// their count. The decode kernel then runs in row-list mode: its producers
+// fetch those rows straight from the paged cache (16-byte cp.async), and
 // the count is the request's length, read on the device. Entries whose block
 // id lies outside [0, num_blocks) are skipped and raise MLA_DEVERR_BAD_BLOCK.
 //

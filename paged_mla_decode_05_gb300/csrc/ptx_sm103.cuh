@@ -136,17 +136,16 @@ MLA_DEVI void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, u
       " [%0], [%1, {%2, %3, %4}], [%5], %6;"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy) : "memory");
 }
-// Row-gather TMA load (2-D tensor map whose box is one row high): four rows
-// r0..r3, columns [x, x + box width), land as four consecutive box rows at
-// dst, swizzled by the map. A row at or past the map's row count reads zeros.
-MLA_DEVI void tma_gather4(uint32_t dst, const void* tmap, int x, int r0, int r1, int r2, int r3,
-                          uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;"
-      :: "r"(dst), "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
-      : "memory");
+// 16-byte asynchronous copy global -> shared (L2 only, not L1).
+MLA_DEVI void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
 }
+// Arrive on the barrier once all prior cp.async of this thread have landed;
+// the arrival is one of the barrier's expected count (noinc).
+MLA_DEVI void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+MLA_DEVI void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 MLA_DEVI uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
