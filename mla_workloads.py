@@ -125,6 +125,12 @@ SPARSE_WORKLOADS: Dict[str, WorkloadSpec] = {
         "sparse_r1_b64_h128", B=64, H=128, block_size=64, seed=6,
         seq_lens=_uniform_lens(64, 8192, 16384), max_len=16384, pool=_pool_125,
         description="B=64, H=128, L=8192+U{0..8192}, bs=64, top-2048 selection per request"),
+    # The same recipe at a quarter of the requests: the case profiled with
+    # multi-pass counters (a 230 MB cache, above the L2 size).
+    "sparse_r1_b16_h128": WorkloadSpec(
+        "sparse_r1_b16_h128", B=16, H=128, block_size=64, seed=7,
+        seq_lens=_uniform_lens(16, 8192, 16384), max_len=16384, pool=_pool_125,
+        description="B=16, H=128, L=8192+U{0..8192}, bs=64, top-2048 selection per request"),
 }
 
 

@@ -6,15 +6,7 @@
 #include "../../include/mla_decode.h"
 #include "mla_internal.h"
 
-// The header's two out-of-line wait loops have external linkage, and the
-// decode kernel's translation unit defines them too: this unit compiles the
-// same source text under its own names so the two copies do not clash at
-// link time.
-#define mbar_wait_slow mbar_wait_slow_selftest
-#define mbar_wait_cluster_slow mbar_wait_cluster_slow_selftest
-#include "ptx_sm103.cuh"
-#undef mbar_wait_slow
-#undef mbar_wait_cluster_slow
+#include "ptx_sm103.cuh"   // the same wait routine (internal linkage per unit)
 
 namespace mla {
 namespace {
