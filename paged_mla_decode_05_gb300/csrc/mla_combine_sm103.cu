@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include "mla_internal.h"
+#include "ptx_sm103.cuh"
 
 namespace mla {
 namespace {
@@ -45,6 +46,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineParams p) {
   extern __shared__ float smem[];                 // [n_slots] weights, then [8][512] sums
   __shared__ float red[kCombineWarps];
+  grid_dep_wait();   // the decode kernel's partials are complete and visible
   const CombineItem ci = p.items[blockIdx.x];
   const int h = blockIdx.y;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -153,8 +155,10 @@ cudaError_t launch_combine(const CombineParams& p, int num_items, int max_slots,
   if (num_items <= 0) return cudaSuccess;
   if (max_slots < 1 || max_slots > kMaxCombineSlots) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(((max_slots + 3) & ~3) + kCombineWarps * kDc) * 4;
-  mla_combine_kernel<<<dim3(num_items, p.H, 1), dim3(kCombineThreads, 1, 1), smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      dependent_launch(dim3(num_items, p.H, 1), dim3(kCombineThreads, 1, 1), smem, stream, attr);
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
 }
 
 }  // namespace mla

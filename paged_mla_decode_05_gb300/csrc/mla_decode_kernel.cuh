@@ -1288,6 +1288,8 @@ template <bool F8, bool ROWS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
+  grid_dep_wait();     // the previous kernel on the stream (e.g. the row lists) is complete
+  grid_dep_launch();   // the combine kernel may be scheduled as pairs finish
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   Ctrl* c = reinterpret_cast<Ctrl*>(base);

@@ -16,13 +16,11 @@ cudaError_t decode_rows_prepare_device() {
 }
 
 cudaError_t launch_decode_rows(const DecodeParams& p, int num_clusters, cudaStream_t stream) {
-  if (p.kv_fp8)
-    mla_decode_kernel<true, true><<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1), kSmemBytes,
-                                    stream>>>(p);
-  else
-    mla_decode_kernel<false, true><<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1),
-                                     kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = dependent_launch(dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1),
+                                                  kSmemBytes, stream, attr);
+  if (p.kv_fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, true>, p);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, true>, p);
 }
 
 }  // namespace mla

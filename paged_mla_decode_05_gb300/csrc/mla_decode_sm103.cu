@@ -41,11 +41,11 @@ cudaError_t decode_max_clusters(int* num_clusters) {
 
 cudaError_t launch_decode(const DecodeParams& p, int num_clusters, cudaStream_t stream) {
   if (p.rows) return launch_decode_rows(p, num_clusters, stream);
-  if (p.kv_fp8)
-    mla_decode_kernel<true, false><<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1), kSmemBytes, stream>>>(p);
-  else
-    mla_decode_kernel<false, false><<<dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1), kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = dependent_launch(dim3(2 * num_clusters, 1, 1), dim3(kThreads, 1, 1),
+                                                  kSmemBytes, stream, attr);
+  if (p.kv_fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, false>, p);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, false>, p);
 }
 
 }  // namespace mla

@@ -183,6 +183,24 @@ struct SparseRowsParams {
 // as requests of topk tokens over blocks of this many list positions.
 constexpr int kSparseBlock = 64;
 
+// Launch configuration shared by the library's kernels: each is launched as
+// a programmatic dependent of the kernel before it on the stream, so its
+// launch overlaps that kernel's tail; every kernel waits for its
+// prerequisites (griddepcontrol.wait) before it touches global memory.
+inline cudaLaunchConfig_t dependent_launch(dim3 grid, dim3 block, size_t smem,
+                                           cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 // Launchers (defined in the .cu files).
 cudaError_t launch_sparse_rows(const SparseRowsParams& p, int B, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int num_clusters, cudaStream_t stream);

@@ -136,6 +136,12 @@ MLA_DEVI void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, u
       " [%0], [%1, {%2, %3, %4}], [%5], %6;"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy) : "memory");
 }
+// Programmatic dependent launch. grid_dep_wait: block until the grids this
+// one depends on have completed and their memory is visible (returns at once
+// for a kernel not launched as a dependent). grid_dep_launch: let the grid
+// launched after this one as a dependent start being scheduled.
+MLA_DEVI void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MLA_DEVI void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // 16-byte asynchronous copy global -> shared (L2 only, not L1).
 MLA_DEVI void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
