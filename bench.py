@@ -48,7 +48,11 @@ METRIC = "MLA decode µs/call + KV-read HBM GB/s at B=512,H=128 vs roofline frac
 UNIT = "us/call"
 DEFAULT_CONFIG = "r1_b512_h128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DECODE_SRC = os.path.join(ROOT, "paged_mla_decode_05_gb300", "csrc", "mla_decode_sm103.cu")
+# The sources the paged decode kernel is compiled from (the recorded DRAM
+# traffic is used only while they are unchanged).
+DECODE_SRCS = [os.path.join(ROOT, "paged_mla_decode_05_gb300", "csrc", f)
+               for f in ("mla_decode_kernel.cuh", "mla_decode_sm103.cu", "ptx_sm103.cuh",
+                         "mla_internal.h")]
 TRAFFIC_FILES = {"bf16": os.path.join(ROOT, "profiles", "decode_r1_b512_h128_traffic.txt"),
                  "fp8": os.path.join(ROOT, "profiles", "decode_r1_b512_h128_fp8_traffic.txt")}
 FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor throughput (4.5 / 2.25 PFLOP/s)
@@ -105,8 +109,11 @@ def load_peaks():
 
 
 def source_digest() -> str:
-    with open(DECODE_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in DECODE_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(config: str, kv: str):
