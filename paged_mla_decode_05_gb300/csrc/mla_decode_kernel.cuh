@@ -1136,6 +1136,10 @@ MLA_DEVI void drain64(const DecodeParams& p, uint32_t taddr, float inv_l, bool t
   tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
   tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
   tmem_wait_ld();
+  // The loads write r after they issue: pin every use of r below the wait
+  // (nothing else orders the arithmetic on r after it).
+#pragma unroll
+  for (int j = 0; j < 64; j += 8) reg_fence8(&r[j]);
   if (out_row == nullptr && part_row == nullptr) return;
   if (to_out) {
     uint4* o = reinterpret_cast<uint4*>(out_row);
