@@ -133,6 +133,21 @@ def test_sparse_head_counts(lib, oracle_mod, H):
     sparse_parity(lib, oracle_mod, w, f"sparse H={H}")
 
 
+@pytest.mark.parametrize("H", [16, 192])
+def test_sparse_fp8_head_counts(lib, oracle_mod, H):
+    """FP8 cache with a padded head group and with two head groups."""
+    w = spec(f"sp8_h{H}", 3, H, 64, [700, 40, 2500], seed=H + 11)
+    w = wl.to_fp8(wl.with_topk(w, 256, seed=H + 13, mixed_padding=True))
+    sparse_parity(lib, oracle_mod, w, f"sparse fp8 H={H}")
+
+
+def test_sparse_fp8_forced_splits(lib, oracle_mod):
+    w = spec("sp8_split", 2, 128, 64, [5000, 3000], seed=98)
+    w = wl.to_fp8(wl.with_topk(w, 2048, seed=99))
+    plan = sparse_parity(lib, oracle_mod, w, "sparse fp8 forced splits", force_splits=3)
+    assert plan.num_splits(1) == 3
+
+
 def test_sparse_duplicates_count_twice(lib, oracle_mod):
     w = spec("sp_dup", 2, 128, 64, [300, 90], seed=77)
     idx = np.array([[5, 5, 5, 299, 0, 17, 17, -1, 100, 101],
@@ -170,13 +185,17 @@ def test_sparse_bad_block_id_is_reported_and_skipped(lib, oracle_mod):
     assert_parity(out, lse, ref_out, ref_lse, "sparse bad block")
 
 
-def test_sparse_graph_replay_with_new_lists(lib, oracle_mod):
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_sparse_graph_replay_with_new_lists(lib, oracle_mod, kv):
     """One captured CUDA graph serves new lists and new lengths: the plan is
     built for topk alone, the lists and lengths are read on the device."""
     import torch
     m = lib
     lens = [3000, 200, 1500]
     w0 = wl.with_topk(spec("sp_graph", 3, 128, 64, lens, seed=93), 512, seed=0)
+    if kv == "fp8":
+        w0 = wl.to_fp8(w0)
+    kv_scale = float(w0["kv_scale"]) if kv == "fp8" else None
     t = _dev(w0)
     B, H, topk = 3, 128, 512
     plan = m.mla_sparse_plan(B, H, topk)
@@ -188,13 +207,13 @@ def test_sparse_graph_replay_with_new_lists(lib, oracle_mod):
     with torch.cuda.stream(s):
         m.mla_decode_sparse(plan, t["q_nope"], t["q_pe"], t["kv"], t["block_table"],
                             t["seq_lens"], t["topk_indices"], float(w0["sm_scale"]), out, lse,
-                            ws, stream=s)
+                            ws, kv_scale=kv_scale, stream=s)
     s.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         m.mla_decode_sparse(plan, t["q_nope"], t["q_pe"], t["kv"], t["block_table"],
                             t["seq_lens"], t["topk_indices"], float(w0["sm_scale"]), out, lse,
-                            ws, stream=s)
+                            ws, kv_scale=kv_scale, stream=s)
     for step, new_lens in enumerate([lens, [2999, 0, 1501], [64, 192, 1]]):
         w = dict(w0)
         w["seq_lens"] = np.array(new_lens, dtype=np.int32)
@@ -207,7 +226,7 @@ def test_sparse_graph_replay_with_new_lists(lib, oracle_mod):
         ref_out, ref_lse = _oracle(oracle_mod, w)
         assert_parity(out.float().cpu().numpy().astype(np.float64),
                       lse.cpu().numpy().astype(np.float64), ref_out, ref_lse,
-                      f"sparse graph replay {step}")
+                      f"sparse graph replay {kv} {step}")
 
 
 def test_sparse_argument_errors(lib):
