@@ -225,18 +225,20 @@ mla_status_t mla_sparse_plan(int B, int H, int topk, const mla_plan_options_t* o
 /*
  * mla_decode_sparse — one sparse decode step. A small kernel turns each
  * request's list into the cache rows of its valid entries (in list order)
- * and their count, in the workspace; the decode kernel then fetches those
- * rows straight from the paged cache (16-byte asynchronous copies), each request's
- * length being its number of valid entries.
+ * and their count, in the workspace; the decode kernel then copies those
+ * rows straight from the paged cache (16-byte asynchronous copies), each
+ * request's length being its number of valid entries.
  *
  *  q_nope, q_pe, out, lse, sm_scale, stream   as for mla_decode ([B, H, ...])
  *  kv_cache      device cache [num_blocks, block_size, 576]: bf16 when
  *                kv_fp8 = 0, E4M3 bytes with per-tensor scale kv_scale when
  *                kv_fp8 = 1 (as for mla_decode_fp8); 16-byte aligned
  *  block_size    16, 32, 64 or 128; num_blocks * block_size < 2^31 - 64
- *                (rows are 32-bit TMA coordinates); block_table device int32
+ *                (cache rows are 32-bit indices); block_table device int32
  *                [B, max_blocks]; seq_lens device int32 [B] (the lengths L
- *                the list entries are checked against)
+ *                the list entries are checked against; L <= max_blocks *
+ *                block_size is the caller's to keep, as for mla_decode: an
+ *                entry whose page lies past the table is skipped)
  *  topk_indices  device int32 [B, topk]
  *  workspace     device memory of at least mla_plan_workspace_bytes(plan)
  *                bytes, 256-byte aligned (always needed: it holds the
