@@ -87,3 +87,25 @@ def test_expected_counts():
     assert c["tokens"] == 257
     assert c["kv_bytes"] == 257 * 1152
     assert c["flops"] == 257 * 16 * (2 * 576 + 2 * 512)
+
+
+def test_sparse_counts_match_dense_counts_on_full_lists():
+    """With every token of every request listed once, the sparse accounting
+    has the dense one's KV bytes, flops and token count; it differs only in
+    the index bytes (4 per list entry) and the table bytes (4 per listed
+    token instead of 4 per page)."""
+    w = wl.generate(wl.custom_spec("cnt", 3, 16, 32, [5, 70, 0], seed=2))
+    topk = 70
+    idx = np.full((3, topk), -1, dtype=np.int32)
+    for b, L in enumerate(w["seq_lens"]):
+        idx[b, :L] = np.arange(L)
+    ws = dict(w, topk_indices=idx)
+    dense, sparse = wl.expected_counts(w), wl.sparse_counts(ws)
+    assert sparse["tokens"] == dense["tokens"] == 75
+    assert sparse["kv_bytes"] == dense["kv_bytes"] and sparse["flops"] == dense["flops"]
+    pages = sum(-(-int(L) // 32) for L in w["seq_lens"])
+    assert sparse["bytes"] - dense["bytes"] == 4 * idx.size + 4 * 75 - 4 * pages
+    # padding and repeats: a repeat counts again, padding not at all
+    idx2 = np.array([[0, 0, -1, 5, 4], [69, 70, 1, 1, 1], [0, -1, -1, -1, -1]], dtype=np.int32)
+    assert wl.sparse_counts(dict(w, topk_indices=idx2))["tokens"] == 3 + 4 + 0
+    assert wl.sparse_counts(wl.to_fp8(ws))["kv_bytes"] == 75 * 576
