@@ -13,7 +13,11 @@ between steps.
                     [--config NAME] [--kv bf16|fp8]
 
 ``--kv fp8`` runs the same workload over an FP8 (E4M3, per-tensor scale)
-cache through ``mla_decode_fp8`` (576 bytes per cached token).
+cache through ``mla_decode_fp8`` (576 bytes per cached token). ``--q-len N``
+gives every request N query tokens (speculative decoding, causal within the
+request's last N tokens; at 128 heads that is N head groups of 128 rows).
+``--graph`` captures one step in a CUDA graph, with a plan built for length
+bounds, and times its replays.
 
 ``--config sparse_r1_b64_h128`` runs the sparse (top-k) decode instead: B=64,
 H=128, lengths 8192 + U{0..8192}, each request attending to 2048 listed tokens
@@ -200,11 +204,17 @@ def is_sparse(name: str) -> bool:
     return name in wl.SPARSE_WORKLOADS
 
 
-def load_workload(name: str, kv: str):
+def load_workload(name: str, kv: str, q_len: int = 1):
     """The seeded workload, with its cache converted to E4M3 for kv == "fp8";
-    a sparse workload also gets its top-k lists (seeded by the spec's seed)."""
+    a sparse workload also gets its top-k lists (seeded by the spec's seed);
+    q_len > 1 gives each request q_len query tokens (speculative decoding)."""
     spec = spec_of(name)
-    w = wl.generate(spec)
+    if q_len > 1:
+        if is_sparse(name):
+            raise SystemExit("--q-len applies to the dense workloads only")
+        w = wl.multi_token(spec, q_len)
+    else:
+        w = wl.generate(spec)
     if is_sparse(name):
         w = wl.with_topk(w, wl.SPARSE_TOPK, seed=spec.seed)
     return wl.to_fp8(w) if kv == "fp8" else w
@@ -227,15 +237,25 @@ def cache_of(w):
     return w["kv_fp8"] if "kv_fp8" in w else w["kv_cache"]
 
 
-def workload_config(spec, w, counts, world):
+def workload_config(spec, w, counts, world, graph=False):
     """The config block both arms report for a workload (identical keys)."""
     cache_bytes = int(cache_of(w).nbytes)
     fp8 = "kv_fp8" in w
+    q_len = int(w.get("q_len", 1))
+    extra = {}
+    if q_len > 1:
+        extra = {"q_len": q_len, "heads": int(w["heads"]),
+                 "query_rows_per_request": int(w["H"]),
+                 "causal": "query token j sees the first L - q_len + 1 + j tokens"}
+    if graph:
+        extra["launch"] = ("CUDA graph replay of one captured step (plan built for length "
+                           "bounds; the kernels read the lengths on the device)")
     sparse = {"topk": int(w["topk_indices"].shape[1]),
               "selection": "min(topk, L) distinct positions per request, uniform"} \
         if "topk_indices" in w else {}
-    return {"workload": spec.name + ("_fp8" if fp8 else ""), "B": int(w["B"]), "H": int(w["H"]),
-            **sparse,
+    name = spec.name + (f"_q{q_len}" if q_len > 1 else "") + ("_fp8" if fp8 else "")
+    return {"workload": name, "B": int(w["B"]), "H": int(w.get("heads", w["H"])),
+            **sparse, **extra,
             "kv_cache": (f"fp8 e4m3, per-tensor scale {w['kv_scale']}" if fp8 else "bf16"),
             "block_size": int(w["block_size"]),
             "seq_lens": "1024+U{0..2048}" if spec.name.startswith("r1_") else spec.description,
@@ -260,9 +280,11 @@ def bench_ours(args, world, rank, local):
 
     spec = spec_of(args.config)
     t0 = time.time()
-    w = load_workload(args.config, args.kv)
+    w = load_workload(args.config, args.kv, args.q_len)
     fp8 = args.kv == "fp8"
     sparse = is_sparse(args.config)
+    q_len = int(w.get("q_len", 1))
+    heads = int(w.get("heads", w["H"]))
     log(f"[bench] generated {spec.name} ({args.kv} cache) in {time.time() - t0:.1f}s")
     counts = counts_of(w)
     B, H, bs = w["B"], w["H"], w["block_size"]
@@ -281,28 +303,52 @@ def bench_ours(args, world, rank, local):
         plan = m.mla_sparse_plan(B, H, int(w["topk_indices"].shape[1]))
         launches_per_step = 2 + (1 if any(plan.num_splits(b) > 1 for b in range(B)) else 0)
     else:
-        plan = m.mla_decode_plan(B, H, w["seq_lens"], bs, int(w["max_blocks"]))
-    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+        plan = m.mla_decode_plan(B, heads, w["seq_lens"], bs, int(w["max_blocks"]), q_len=q_len,
+                                 lengths_are_bounds=args.graph)
+    out = torch.empty(plan.q_shape(512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(plan.q_shape(None), dtype=torch.float32, device=dev)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     if not sparse:
         launches_per_step = 1 + (1 if plan.workspace_bytes else 0)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def call(st):
         if sparse:
             m.mla_decode_sparse(plan, q_nope, q_pe, kv, table, lens, topk_dev, w["sm_scale"], out,
-                                lse, ws, kv_scale=w["kv_scale"] if fp8 else None, stream=stream)
+                                lse, ws, kv_scale=w["kv_scale"] if fp8 else None, stream=st)
         elif fp8:
             m.mla_decode_fp8(plan, q_nope, q_pe, kv, w["kv_scale"], table, lens, w["sm_scale"], out,
-                             lse, ws, stream)
+                             lse, ws, st)
         else:
-            m.mla_decode(plan, q_nope, q_pe, kv, table, lens, w["sm_scale"], out, lse, ws, stream)
+            m.mla_decode(plan, q_nope, q_pe, kv, table, lens, w["sm_scale"], out, lse, ws, st)
+
+    def step():
+        call(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert m.mla_check_device_error(plan) == 0
+    if args.graph:
+        # One step captured on a side stream; every timed step replays it on
+        # the launching stream.
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            call(cap)
+        cap.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            call(cap)
+        torch.cuda.synchronize()
+
+        def step():  # noqa: F811 (the timed step is the replay)
+            graph.replay()
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        assert m.mla_check_device_error(plan) == 0
 
     # A cache several times the L2 size leaves no reuse between steps; a
     # smaller one gets L2 flushed (a write larger than L2) before every step,
@@ -343,8 +389,8 @@ def bench_ours(args, world, rank, local):
     h_tab = torch.from_numpy(w["block_table"]).pin_memory()
     h_len = torch.from_numpy(w["seq_lens"]).pin_memory()
     h_idx = torch.from_numpy(w["topk_indices"]).pin_memory() if sparse else None
-    h_out = torch.empty((B, H, 512), dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    h_out = torch.empty(tuple(out.shape), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(tuple(lse.shape), dtype=torch.float32).pin_memory()
     lens_np = w["seq_lens"].copy()
     e_steps = max(3, min(args.steps, 20))
 
@@ -358,7 +404,7 @@ def bench_ours(args, world, rank, local):
 
     def e2e_step():
         copies_in()
-        if not sparse:   # a sparse plan serves any lists and lengths
+        if not sparse and not args.graph:   # sparse and bounds plans serve any lengths
             plan.update(lens_np, stream)
         step()
         h_out.copy_(out, non_blocking=True)
@@ -394,7 +440,7 @@ def bench_ours(args, world, rank, local):
         h_lse.copy_(lse, non_blocking=True)
 
     plan_host_us = 0.0
-    if not sparse:
+    if not sparse and not args.graph:
         t_p = time.perf_counter()
         for _ in range(5):
             plan.update(lens_np, stream)
@@ -442,7 +488,7 @@ def bench_ours(args, world, rank, local):
                  if fp8 else
                  "synthetic (seeded N(0,1) bf16 latent cache and queries, sentinel-filled spare "
                  "blocks and tail slots)"),
-        "config": workload_config(spec, w, counts, world),
+        "config": workload_config(spec, w, counts, world, args.graph),
         "plan": {"cta_pairs": plan.num_clusters, "work_items": plan.num_work_items,
                  "split_requests": int(sum(plan.num_splits(b) > 1 for b in range(B)))},
         "kv_read_gbs": round(counts["kv_bytes"] / (ms_per_step * 1e-3) / 1e9, 1),
@@ -490,6 +536,8 @@ def oracle_call(oracle, w, reqs=None):
     sel = slice(None) if reqs is None else np.asarray(reqs)
     qn, qp = w["q_nope"][sel], w["q_pe"][sel]
     bt, sl = w["block_table"][sel], w["seq_lens"][sel]
+    if "q_len" in w and "kv_fp8" not in w:
+        return oracle.mla_decode_multi(qn, qp, w["kv_cache"], bt, sl, w["sm_scale"])
     if "topk_indices" in w:
         idx = w["topk_indices"][sel]
         if "kv_fp8" in w:
@@ -529,7 +577,7 @@ def cpu_baseline(w, budget_s: float):
     share = seq[reqs].sum() / seq.sum()
     per_call_s = dt / share
     return {"value": round(per_call_s * 1e6, 1), "unit": UNIT, "cores": int(cores), "kind": "oracle",
-            "sample": f"{reqs.size} of {B} requests (all {H} heads each), {dt:.1f} s, scaled by "
+            "sample": f"{reqs.size} of {B} requests (all {H} query rows each), {dt:.1f} s, scaled by "
                       f"token share {share:.4f}"}
 
 
@@ -541,7 +589,7 @@ def bench_reference(args, world, rank, local):
         if rank != 0:
             return None
     spec = spec_of(args.config)
-    w = load_workload(args.config, args.kv)
+    w = load_workload(args.config, args.kv, args.q_len)
     import oracle
     oracle.build()
     B, H = int(w["B"]), int(w["H"])
@@ -572,7 +620,7 @@ def bench_reference(args, world, rank, local):
             dt = time.perf_counter() - t0
             if s >= args.warmup:
                 times.append(dt)
-        sample = f"the full workload every step ({B} requests x {H} heads)"
+        sample = f"the full workload every step ({B} requests x {H} query rows)"
     else:
         # Each step: a random sample of requests sized so the run stays within
         # the budget, scaled by its token share to one call.
@@ -584,7 +632,7 @@ def bench_reference(args, world, rank, local):
             dt = time.perf_counter() - t0
             if s >= args.warmup:
                 times.append(dt / (seq[reqs].sum() / seq.sum()))
-        sample = (f"{n_req} random requests (all {H} heads) per step, scaled by token share to "
+        sample = (f"{n_req} random requests (all {H} query rows) per step, scaled by token share to "
                   "one full call (the full call would not fit the run's time budget)")
     us = statistics.mean(times) * 1e6
     return {
@@ -592,7 +640,7 @@ def bench_reference(args, world, rank, local):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(spec, w, counts_of(w), world),
+        "config": workload_config(spec, w, counts_of(w), world, args.graph),
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": int(cores), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -611,6 +659,10 @@ def main(argv=None):
                     choices=sorted(list(wl.WORKLOADS_BY_NAME) + list(wl.SPARSE_WORKLOADS)))
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="cache element type (fp8: E4M3 with a per-tensor scale)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per request (speculative decoding; dense workloads)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time CUDA-graph replays of one captured step (length-bounds plan)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)

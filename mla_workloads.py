@@ -134,6 +134,18 @@ SPARSE_WORKLOADS: Dict[str, WorkloadSpec] = {
 }
 
 
+def multi_token(spec: WorkloadSpec, q_len: int) -> Dict[str, object]:
+    """The workload of ``spec`` with q_len query tokens per request (the
+    speculative-decoding shape): the generator's draws for q_len * H query
+    rows, viewed as [B, q_len, H, ...] (``q_len`` and ``heads`` keys added).
+    The lengths count the q_len new tokens, so every L must be >= q_len."""
+    w = dict(generate(dataclasses.replace(spec, H=spec.H * q_len, name=f"{spec.name}_q{q_len}")))
+    w["q_len"], w["heads"] = int(q_len), int(spec.H)
+    w["q_nope"] = w["q_nope"].reshape(spec.B, q_len, spec.H, D_C)
+    w["q_pe"] = w["q_pe"].reshape(spec.B, q_len, spec.H, D_R)
+    return w
+
+
 def custom_spec(name: str, B: int, H: int, block_size: int, seq_lens: Sequence[int],
                 seed: int, spare_blocks: int = 4, peaky_fraction: float = 0.0,
                 max_blocks: Optional[int] = None,
@@ -312,7 +324,13 @@ def expected_counts(w: Dict[str, object]) -> Dict[str, float]:
     pages = int(((seq + bs - 1) // bs).sum())
     kv_bytes = tokens * D * (1 if "kv_fp8" in w else 2)
     total = kv_bytes + B * H * D * 2 + B * H * D_C * 2 + 4 * B * H + 4 * pages + 4 * B
-    flops = tokens * H * (2 * D + 2 * D_C)
+    q_len = int(w.get("q_len", 1))
+    if q_len == 1:
+        flops = tokens * H * (2 * D + 2 * D_C)
+    else:   # H = q_len * heads rows; query token j sees the first L - q_len + 1 + j tokens
+        heads = H // q_len
+        seen = sum(max(0, int(L) - q_len + 1 + j) for L in seq for j in range(q_len))
+        flops = seen * heads * (2 * D + 2 * D_C)
     return {"tokens": tokens, "kv_bytes": float(kv_bytes), "bytes": float(total),
             "flops": float(flops)}
 

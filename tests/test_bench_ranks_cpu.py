@@ -40,7 +40,8 @@ def _reference_rank(rank, world, port, q):
     try:
         import argparse
         import bench
-        args = argparse.Namespace(steps=1, warmup=3, config="tiny_b2_h16", kv="bf16")
+        args = argparse.Namespace(steps=1, warmup=3, config="tiny_b2_h16", kv="bf16", q_len=1,
+                                  graph=False)
         res = bench.bench_reference(args, world, rank, rank)
         q.put((rank, "ref", None if res is None else (res["impl"], res["n_gpus"], res["value"] > 0)))
     except Exception as e:  # pragma: no cover
