@@ -20,10 +20,10 @@ def __getattr__(name):
     if name in _EXPORTS:
         from . import _lib
         return getattr(_lib, name)
-    if name == "decode":
-        from .api import decode
-        return decode
+    if name in ("decode", "decode_sparse"):
+        from . import api
+        return getattr(api, name)
     raise AttributeError(name)
 
 
-__all__ = list(_EXPORTS) + ["decode"]
+__all__ = list(_EXPORTS) + ["decode", "decode_sparse"]

@@ -275,6 +275,32 @@ def test_convenience_decode_matches_oracle(lib, oracle_mod):
                   lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, "decode()")
 
 
+def test_convenience_decode_multi_token_and_sparse(lib, oracle_mod):
+    """decode() with [B, q_len, H, 512] queries and decode_sparse() with a
+    top-k list, each allocating its plan, outputs and workspace."""
+    import torch
+    w = wl.multi_token(wl.custom_spec("api_multi", 3, 32, 32, [40, 300, 97], seed=61), 3)
+    t = to_device(w)
+    out, lse = lib.decode(t["q_nope"], t["q_pe"], t["kv_cache"], t["block_table"], t["seq_lens"],
+                          float(w["sm_scale"]))
+    assert tuple(out.shape) == (3, 3, 32, 512) and tuple(lse.shape) == (3, 3, 32)
+    ref_out, ref_lse = oracle_mod.mla_decode_multi(w["q_nope"], w["q_pe"], w["kv_cache"],
+                                                   w["block_table"], w["seq_lens"], w["sm_scale"])
+    assert_parity(out.float().cpu().numpy().astype(np.float64),
+                  lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, "decode() q_len=3")
+    ws_ = wl.with_topk(spec("api_sparse", 3, 128, 64, [700, 40, 2500], seed=62), 256, seed=63,
+                       mixed_padding=True)
+    ts = to_device(ws_)
+    idx = torch.from_numpy(ws_["topk_indices"]).cuda()
+    out, lse = lib.decode_sparse(ts["q_nope"], ts["q_pe"], ts["kv_cache"], ts["block_table"],
+                                 ts["seq_lens"], idx, float(ws_["sm_scale"]))
+    ref_out, ref_lse = oracle_mod.mla_decode_sparse(ws_["q_nope"], ws_["q_pe"], ws_["kv_cache"],
+                                                    ws_["block_table"], ws_["seq_lens"],
+                                                    ws_["topk_indices"], ws_["sm_scale"])
+    assert_parity(out.float().cpu().numpy().astype(np.float64),
+                  lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, "decode_sparse()")
+
+
 def test_plan_update_growth_keeps_error_word_and_parity(lib, oracle_mod):
     """mla_plan_update on lengths whose schedule outgrows the plan's device
     buffer: the buffer is replaced without a device synchronisation, the
