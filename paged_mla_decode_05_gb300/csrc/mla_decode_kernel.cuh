@@ -1141,23 +1141,40 @@ MLA_DEVI void drain64(const DecodeParams& p, uint32_t taddr, float inv_l, bool t
 #pragma unroll
   for (int j = 0; j < 64; j += 8) reg_fence8(&r[j]);
   if (out_row == nullptr && part_row == nullptr) return;
+  // Each store instruction writes 32 rows (one per lane), so its cost grows
+  // with the rows it touches, not with its bytes: 32-byte stores (whole
+  // sectors) take half as many instructions as 16-byte ones.
   if (to_out) {
-    uint4* o = reinterpret_cast<uint4*>(out_row);
+    if ((reinterpret_cast<uintptr_t>(out_row) & 31u) == 0) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint32_t v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          v[k] = pack_bf16x2(__uint_as_float(r[16 * e + 2 * k]) * inv_l,
+                             __uint_as_float(r[16 * e + 2 * k + 1]) * inv_l);
+        st_global_v8(out_row + 16 * e, v);
+      }
+    } else {   // the caller's out is only 16-byte aligned
+      uint4* o = reinterpret_cast<uint4*>(out_row);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
+        v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
+        v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
+        v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
+        o[e] = v;
+      }
+    }
+  } else {   // the split partials sit in the 256-byte aligned workspace
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      uint4 v;
-      v.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
-      v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
-      v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
-      v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
-      o[e] = v;
-    }
-  } else {
-    float4* o = reinterpret_cast<float4*>(part_row);
+      uint32_t v[8];
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
-      o[e] = make_float4(__uint_as_float(r[4 * e + 0]) * inv_l, __uint_as_float(r[4 * e + 1]) * inv_l,
-                         __uint_as_float(r[4 * e + 2]) * inv_l, __uint_as_float(r[4 * e + 3]) * inv_l);
+      for (int k = 0; k < 8; ++k) v[k] = __float_as_uint(__uint_as_float(r[8 * e + k]) * inv_l);
+      st_global_v8(part_row + 8 * e, v);
+    }
   }
 }
 
@@ -1291,7 +1308,9 @@ MLA_DEVI void out_correct(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_
 // Warm L2 with the Q rows of the pair's first item, at kernel entry: the
 // loader warps start only after the prologue's barrier, and their three round
 // trips to DRAM otherwise set the start of every pair (about 13 us from launch
-// for 128 heads). Out of line, so the kernel body keeps its code layout.
+// for 128 heads). The calling warp has already arrived on that barrier, so
+// the read of the work list here does not delay it. Out of line, so the
+// kernel body keeps its code layout.
 __device__ __noinline__ void prefetch_first_q(const DecodeParams& p, int it0, int it1) {
   for (int it = it0; it < it1; ++it) {
     const WorkItem w = item_at(p, it);
@@ -1360,9 +1379,17 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p) {
     tmem_alloc(smem_addr(&c->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (rank == 0 && warp == 8 && lane == 0) prefetch_first_q(p, it0, it1);
   tc_before_sync();
-  cluster_barrier();
+  if (rank == 0 && warp == 8) {
+    // This warp arrives first: the prefetch (which reads the work list)
+    // does not hold up the pair's start.
+    cluster_arrive();
+    if (lane == 0) prefetch_first_q(p, it0, it1);
+    __syncwarp();
+    cluster_wait();
+  } else {
+    cluster_barrier();
+  }
   tc_after_sync();
   const uint32_t tmem = c->tmem_base;
 

@@ -37,6 +37,8 @@ MLA_DEVI uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
   return r;
 }
 
+MLA_DEVI void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+MLA_DEVI void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 MLA_DEVI void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -142,6 +144,12 @@ MLA_DEVI void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, u
 // launched after this one as a dependent start being scheduled.
 MLA_DEVI void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 MLA_DEVI void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// 32-byte global stores (sm_100+; the address must be 32-byte aligned).
+MLA_DEVI void st_global_v8(void* ptr, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(ptr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                  "r"(w[6]), "r"(w[7]) : "memory");
+}
 // 16-byte asynchronous copy global -> shared (L2 only, not L1).
 MLA_DEVI void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
