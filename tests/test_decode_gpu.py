@@ -53,6 +53,38 @@ def test_large_configs_full(lib, oracle_mod, idx):
         assert plan.num_splits(0) > 1
 
 
+def test_output_only_16_byte_aligned(lib, oracle_mod):
+    """The epilogue writes 32 bytes per lane where out is 32-byte aligned and
+    16 bytes per lane otherwise: an out that starts 16 bytes past a 32-byte
+    boundary takes the second path, with the same results (bit for bit) as
+    an aligned out, and nothing is written before its first element."""
+    import torch
+    import paged_mla_decode_05_gb300 as m
+    from gpu_helpers import decode_into
+    w = spec("a16", 3, 128, 32, [1, 300, 1000], seed=21)
+    t = to_device(w)
+    B, H = int(w["B"]), int(w["H"])
+    plan = m.mla_decode_plan(B, H, w["seq_lens"], int(w["block_size"]), int(w["max_blocks"]))
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+    n = B * H * 512
+    buf = torch.full((n + 16,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    out16 = buf[8:8 + n].view(B, H, 512)          # 16 bytes past a 32-byte boundary
+    assert out16.data_ptr() % 32 == 16
+    out32 = torch.full((B, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse16 = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    lse32 = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    decode_into(m, plan, w, t, t["q_nope"], t["q_pe"], out16, lse16, ws)
+    decode_into(m, plan, w, t, t["q_nope"], t["q_pe"], out32, lse32, ws)
+    assert m.mla_check_device_error(plan) == 0
+    assert torch.isnan(buf[:8]).all() and torch.isnan(buf[8 + n:]).all()
+    assert torch.equal(out16.view(torch.int16), out32.view(torch.int16))
+    assert torch.equal(lse16, lse32)
+    ref_out, ref_lse = oracle_mod.mla_decode(*oracle_args(w))
+    assert_parity(out16.float().cpu().numpy().astype(np.float64),
+                  lse16.cpu().numpy().astype(np.float64), ref_out, ref_lse, "a16")
+
+
 @pytest.mark.parametrize("H", [1, 7, 32, 100, 128])
 def test_head_counts(lib, oracle_mod, H):
     full_parity(oracle_mod, spec(f"h{H}", 3, H, 32, [1, 97, 300], seed=H))
