@@ -627,39 +627,44 @@ __device__ __noinline__ bool load_q_f8(const DecodeParams& p, Ctrl* c, float* qs
   uint4 nxt[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) nxt[e] = chunk(e);
+  // One 64-column panel (two steps of 32 columns, both terms) per pass, each
+  // step in its own registers, so that one wait for the tensor-memory stores
+  // per panel (before the panel is announced) covers both steps.
 #pragma unroll 1
-  for (int cc = 0; cc < kD / 32; ++cc) {   // 32 columns: four 16-byte pieces
-    uint4 v[4];
+  for (int pc = 0; pc < kD / 64; ++pc) {
+    uint32_t hw[2][8], lw[2][8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) v[e] = nxt[e];
-    if (cc + 1 < kD / 32) {
+    for (int h = 0; h < 2; ++h) {
+      const int cc = 2 * pc + h;
+      uint4 v[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) nxt[e] = chunk(4 * (cc + 1) + e);
-    }
-    uint32_t hw[8], lw[8];
+      for (int e = 0; e < 4; ++e) v[e] = nxt[e];
+      if (cc + 1 < kD / 32) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t wd[4] = {v[e].x, v[e].y, v[e].z, v[e].w};
-#pragma unroll
-      for (int k = 0; k < 4; k += 2) {
-        // bf16 pairs (2 elements per word) -> fp32, scaled by 2^-k (exact).
-        const uint32_t a = split_e4m3x2(mul_f32x2(pack_b32x2(wd[k] << 16, wd[k] & 0xFFFF0000u), is2));
-        const uint32_t b =
-            split_e4m3x2(mul_f32x2(pack_b32x2(wd[k + 1] << 16, wd[k + 1] & 0xFFFF0000u), is2));
-        hw[2 * e + k / 2] = (a & 0xFFFFu) | (b << 16);
-        lw[2 * e + k / 2] = (a >> 16) | (b & 0xFFFF0000u);
+        for (int e = 0; e < 4; ++e) nxt[e] = chunk(4 * (cc + 1) + e);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t wd[4] = {v[e].x, v[e].y, v[e].z, v[e].w};
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {
+          // bf16 pairs (2 elements per word) -> fp32, scaled by 2^-k (exact).
+          const uint32_t a = split_e4m3x2(mul_f32x2(pack_b32x2(wd[k] << 16, wd[k] & 0xFFFF0000u), is2));
+          const uint32_t b =
+              split_e4m3x2(mul_f32x2(pack_b32x2(wd[k + 1] << 16, wd[k + 1] & 0xFFFF0000u), is2));
+          hw[h][2 * e + k / 2] = (a & 0xFFFFu) | (b << 16);
+          lw[h][2 * e + k / 2] = (a >> 16) | (b & 0xFFFF0000u);
+        }
+      }
+      tmem_st8(trow + kTmemQ + cc * 8, hw[h]);
+      tmem_st8(trow + kTmemQ + kF8QLoCol + cc * 8, lw[h]);
     }
-    tmem_st8(trow + kTmemQ + cc * 8, hw);
-    tmem_st8(trow + kTmemQ + kF8QLoCol + cc * 8, lw);
     // tcgen05.st reads its source registers asynchronously: complete the
-    // stores before the next chunk reuses hw and lw.
+    // stores before the registers are reused and before the panel is announced.
     tmem_wait_st();
-    if (cc & 1) {
-      tc_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&c->q_ready[cc >> 1]));
-    }
+    tc_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&c->q_ready[pc]));
   }
   return true;
 }
