@@ -582,6 +582,69 @@ __device__ __noinline__ bool load_q(const DecodeParams& p, Ctrl* c, const WorkIt
   return true;
 }
 
+// Panels [pc0, pc1) of the FP8 path's Q of item w, row `row` (64 columns
+// each: two steps of 32 columns), scaled by inv_s = 2^-k and split into hi
+// and lo E4M3 codes, into tensor memory; each panel is announced on its
+// q_ready barrier. Called by the Q loader warps for panels 0..4 and by the
+// softmax warps, idle until the item's first S tile, for panels 5..8: both
+// halves of the conversion run at once at every item boundary.
+constexpr int kQPanelsByLoader = 5;
+__device__ __noinline__ bool convert_q_f8(const DecodeParams& p, Ctrl* c, const WorkItem& w,
+                                          int row, uint32_t trow, float inv_s, int pc0, int pc1) {
+  const int lane = row & 31;
+  const bool active = row < heads_of(p, w);
+  const int64_t r = static_cast<int64_t>(w.b) * p.H + w.h0 + (active ? row : 0);
+  const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + r * kDc);   // 64 x 16 B
+  const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + r * kDr);     // 8 x 16 B
+  auto chunk = [&](int j) -> uint4 {   // 16-byte piece j < 72 of the row
+    return active ? __ldg(j < kDc / 8 ? qn + j : qp + (j - kDc / 8)) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  const uint64_t is2 = pack_f32x2(inv_s, inv_s);
+  uint4 nxt[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) nxt[e] = chunk(8 * pc0 + e);
+  // One 64-column panel (two steps of 32 columns, both terms) per pass, each
+  // step in its own registers, so that one wait for the tensor-memory stores
+  // per panel (before the panel is announced) covers both steps.
+#pragma unroll 1
+  for (int pc = pc0; pc < pc1; ++pc) {
+    uint32_t hw[2][8], lw[2][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int cc = 2 * pc + h;
+      uint4 v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = nxt[e];
+      if (cc + 1 < 2 * pc1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) nxt[e] = chunk(4 * (cc + 1) + e);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t wd[4] = {v[e].x, v[e].y, v[e].z, v[e].w};
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {
+          // bf16 pairs (2 elements per word) -> fp32, scaled by 2^-k (exact).
+          const uint32_t a = split_e4m3x2(mul_f32x2(pack_b32x2(wd[k] << 16, wd[k] & 0xFFFF0000u), is2));
+          const uint32_t b =
+              split_e4m3x2(mul_f32x2(pack_b32x2(wd[k + 1] << 16, wd[k + 1] & 0xFFFF0000u), is2));
+          hw[h][2 * e + k / 2] = (a & 0xFFFFu) | (b << 16);
+          lw[h][2 * e + k / 2] = (a >> 16) | (b & 0xFFFF0000u);
+        }
+      }
+      tmem_st8(trow + kTmemQ + cc * 8, hw[h]);
+      tmem_st8(trow + kTmemQ + kF8QLoCol + cc * 8, lw[h]);
+    }
+    // tcgen05.st reads its source registers asynchronously: complete the
+    // stores before the registers are reused and before the panel is announced.
+    tmem_wait_st();
+    tc_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&c->q_ready[pc]));
+  }
+  return true;
+}
+
 // FP8 path: Q of item w as two E4M3 terms per element in tensor memory, hi
 // codes in columns [0, 144) and lo codes in [144, 288) of lane `row`, with a
 // per-row power-of-two scale: q = 2^k (hi + lo), where 2^k puts max|q| of
@@ -591,8 +654,8 @@ __device__ __noinline__ bool load_q(const DecodeParams& p, Ctrl* c, const WorkIt
 // (as the largest bf16 magnitude pattern, whose order is that of the
 // values), writes 2^k into qscale (the ring slot of this item) and arrives on
 // qs_ready[slot]; then, when wait_parity >= 0, the warp waits on q_free and
-// converts the row 32 columns at a time, announcing each 64 columns (both
-// terms) on q_ready. Rows past the group's heads are zero.
+// converts panels 0..4 of the row (convert_q_f8; the softmax warps convert
+// panels 5..8 at the same time). Rows past the group's heads are zero.
 __device__ __noinline__ bool load_q_f8(const DecodeParams& p, Ctrl* c, float* qscale,
                                        const WorkItem& w, int row, uint32_t trow,
                                        int wait_parity, int slot) {
@@ -623,50 +686,7 @@ __device__ __noinline__ bool load_q_f8(const DecodeParams& p, Ctrl* c, float* qs
       return false;
     tc_after_sync();
   }
-  const uint64_t is2 = pack_f32x2(inv_s, inv_s);
-  uint4 nxt[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) nxt[e] = chunk(e);
-  // One 64-column panel (two steps of 32 columns, both terms) per pass, each
-  // step in its own registers, so that one wait for the tensor-memory stores
-  // per panel (before the panel is announced) covers both steps.
-#pragma unroll 1
-  for (int pc = 0; pc < kD / 64; ++pc) {
-    uint32_t hw[2][8], lw[2][8];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int cc = 2 * pc + h;
-      uint4 v[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = nxt[e];
-      if (cc + 1 < kD / 32) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) nxt[e] = chunk(4 * (cc + 1) + e);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t wd[4] = {v[e].x, v[e].y, v[e].z, v[e].w};
-#pragma unroll
-        for (int k = 0; k < 4; k += 2) {
-          // bf16 pairs (2 elements per word) -> fp32, scaled by 2^-k (exact).
-          const uint32_t a = split_e4m3x2(mul_f32x2(pack_b32x2(wd[k] << 16, wd[k] & 0xFFFF0000u), is2));
-          const uint32_t b =
-              split_e4m3x2(mul_f32x2(pack_b32x2(wd[k + 1] << 16, wd[k + 1] & 0xFFFF0000u), is2));
-          hw[h][2 * e + k / 2] = (a & 0xFFFFu) | (b << 16);
-          lw[h][2 * e + k / 2] = (a >> 16) | (b & 0xFFFF0000u);
-        }
-      }
-      tmem_st8(trow + kTmemQ + cc * 8, hw[h]);
-      tmem_st8(trow + kTmemQ + kF8QLoCol + cc * 8, lw[h]);
-    }
-    // tcgen05.st reads its source registers asynchronously: complete the
-    // stores before the registers are reused and before the panel is announced.
-    tmem_wait_st();
-    tc_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&c->q_ready[pc]));
-  }
-  return true;
+  return convert_q_f8(p, c, w, row, trow, inv_s, 0, kQPanelsByLoader);
 }
 
 // Q loader warps (one per tensor-memory lane quadrant): the Q of each of the
@@ -785,11 +805,13 @@ MLA_DEVI float tile_max(const uint32_t (&r)[kTile]) {
 //
 // FP8 path: the raw scores carry the row's Q scale 2^k and the cache scale,
 // so the multiplier is c = sm_scale * log2(e) * kv_scale * 2^k (2^k read
-// from the Q loaders' ring slot of the item on its first tile, before the S
-// buffer is released: the loaders reuse a slot four items later, after the
-// S MMAs of a later tile, which wait for that release). P is shipped as
-// p' = p * 2^kF8PShift, and the record's m is m - kF8PShift, so that
-// lse = m + log2(l) and out = O / l hold unchanged.
+// from the Q loaders' ring slot of the item at the item's start, before any
+// of its S buffers is released: the loaders reuse a slot four items later,
+// after the S MMAs of a later tile, which wait for that release). At the
+// item's start these warps also convert panels 5..8 of the item's Q (the
+// loaders convert 0..4). P is shipped as p' = p * 2^kF8PShift, and the
+// record's m is m - kF8PShift, so that lse = m + log2(l) and out = O / l
+// hold unchanged.
 template <bool F8>
 MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint32_t tmem,
                             int warp, int lane, int it0, int it1) {
@@ -818,6 +840,37 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
     while (nxt < it1 && tiles_of(item_at(p, nxt)) == 0) ++nxt;
     float m_used = -INFINITY, l = 0.0f;
     const int item = n_items++;
+    if constexpr (F8) {
+      // The row's Q scale 2^k (the loaders' ring slot of this item), then the
+      // second part of the item's Q conversion once the previous item's S
+      // MMAs are done with Q.
+      const int slot = item % kF8QScaleSlots;
+      if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->qs_ready[slot]),
+                                           (item / kF8QScaleSlots) & 1))) {
+        ok = false;
+        break;
+      }
+      // (a 32-bit shared-memory address keeps this path within the
+      // register budget of the role)
+      float qs;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qs)
+                   : "r"(smem_addr(data) + kF8NumStages * kF8StageBytes +
+                         (slot * kMaxHeads + row) * 4)
+                   : "memory");
+      c_row = sl2 * p.kv_scale * qs;
+      if (item > 0 && !__all_sync(kFullMask, mbar_wait(smem_addr(&c->q_free),
+                                                       static_cast<uint32_t>((item - 1) & 1)))) {
+        ok = false;
+        break;
+      }
+      tc_after_sync();
+      // qs = 2^k exactly, so 2^-k has the exponent field 254 - (k + 127).
+      const float inv_s = __uint_as_float((254u << 23) - __float_as_uint(qs));
+      if (!convert_q_f8(p, c, w, row, trow, inv_s, kQPanelsByLoader, kNumPanels)) {
+        ok = false;
+        break;
+      }
+    }
     for (int i = 0; i < nt; ++i, ++g) {
       const int s = g & 1;
       const int k = g % kNumPBufs;
@@ -838,22 +891,6 @@ MLA_DEVI void score_softmax(const DecodeParams& p, Ctrl* c, uint8_t* data, uint3
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < kTile; j += 8) reg_fence8(&r[j]);
-      if (F8 && i == 0) {
-        const int slot = item % kF8QScaleSlots;
-        if (!__all_sync(kFullMask, mbar_wait(smem_addr(&c->qs_ready[slot]),
-                                             (item / kF8QScaleSlots) & 1))) {
-          ok = false;
-          break;
-        }
-        // (a 32-bit shared-memory address keeps this path within the
-        // register budget of the role)
-        float qs;
-        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qs)
-                     : "r"(smem_addr(data) + kF8NumStages * kF8StageBytes +
-                           (slot * kMaxHeads + row) * 4)
-                     : "memory");
-        c_row = sl2 * p.kv_scale * qs;
-      }
       // The scores are in registers: the S buffer may take tile g + 2.
       tc_before_sync();
       mbar_arrive(smem_addr(&c->s_free[s]));
